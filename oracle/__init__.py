@@ -1,0 +1,152 @@
+"""CPU fp64 oracle for speculative-decoding block attention over a paged KV cache.
+
+TEST INFRASTRUCTURE ONLY.  The oracle is the slow, plainly-written definition
+of what the CUDA library computes; only ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may load it.  It shares no code with
+the CUDA library and never serves as a fallback for it.
+
+The arithmetic lives in ``spec_attn_oracle.c`` (plain C, fp64, OpenMP over
+independent output rows only); this module compiles it with gcc into
+``oracle/_build/libspec_attn_oracle.so`` and wraps it with ctypes.
+
+Parity pins (tests/test_oracle_pins.py) hold every function here to values
+fixed independently of this code: torch's fp64 scaled-dot-product attention on
+CPU for W=1 decode, a pure-Python brute force on tiny shapes, closed forms
+(zero queries, one visible key, constant power-of-two values), invariances
+(page permutation, row-wise reduction to decode, last-row agreement of the two
+masks) and the OCP e2m1 / e4m3 format definitions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libspec_attn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math) and return the .so path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32, f64, vp = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+            lib.spec_attn_oracle_run.restype = i32
+            lib.spec_attn_oracle_run.argtypes = [
+                i32, i32, i32, i32, i32, i32, i32, i32, i32, f64,
+                vp, vp, vp, vp, vp, f64, f64, vp, i32, vp, vp, vp, vp, vp, vp]
+            lib.oracle_e2m1.restype = f64
+            lib.oracle_e2m1.argtypes = [ctypes.c_uint]
+            lib.oracle_e4m3.restype = f64
+            lib.oracle_e4m3.argtypes = [ctypes.c_uint]
+            lib.oracle_bf16_value.restype = f64
+            lib.oracle_bf16_value.argtypes = [ctypes.c_uint]
+            lib.oracle_round_bf16.restype = ctypes.c_uint
+            lib.oracle_round_bf16.argtypes = [f64]
+            lib.spec_attn_oracle_num_threads.restype = i32
+            lib.spec_attn_oracle_num_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _np(t, dtype):
+    """torch tensor or numpy array -> contiguous numpy array of ``dtype`` bits."""
+    if t is None:
+        return None
+    if hasattr(t, "detach"):  # torch tensor
+        import torch
+        t = t.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        t = t.numpy()
+    a = np.ascontiguousarray(t)
+    return a.view(dtype) if a.dtype.itemsize == np.dtype(dtype).itemsize else a.astype(dtype)
+
+
+def e2m1(code: int) -> float:
+    return _load().oracle_e2m1(code)
+
+
+def e4m3(byte: int) -> float:
+    return _load().oracle_e4m3(byte)
+
+
+def round_bf16_bits(x: float) -> int:
+    return _load().oracle_round_bf16(float(x))
+
+
+def num_threads() -> int:
+    return _load().spec_attn_oracle_num_threads()
+
+
+def run(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, mask_mode, kv_dtype,
+        sm_scale, q, k_pool, v_pool, block_table, seq_lens, q_indptr, k_scales=None,
+        v_scales=None, k_gscale=1.0, v_gscale=1.0, row_select=None, want_o=True,
+        want_lse=True, want_trace=False):
+    """Run the oracle.  Arrays may be torch tensors (bf16 is taken bit-wise) or
+    numpy arrays.  Returns ``(o, lse, trace)`` as numpy arrays (fp64, fp64,
+    int64) or ``None`` for outputs not requested.  ``o`` and ``lse`` rows that
+    ``row_select`` skips hold NaN."""
+    lib = _load()
+    qn = _np(q, np.uint16)
+    total_rows = qn.shape[0]
+    kn = _np(k_pool, np.uint16 if kv_dtype == 0 else np.uint8)
+    vn = _np(v_pool, np.uint16 if kv_dtype == 0 else np.uint8)
+    ksn = _np(k_scales, np.uint8)
+    vsn = _np(v_scales, np.uint8)
+    btn = _np(block_table, np.int32)
+    sln = _np(seq_lens, np.int32)
+    qin = _np(q_indptr, np.int32)
+    num_reqs = sln.shape[0]
+    bt_stride = btn.shape[1] if btn.ndim == 2 else btn.shape[0]
+    sel = None if row_select is None else np.ascontiguousarray(
+        np.asarray(row_select, dtype=np.uint8).reshape(total_rows * num_q_heads))
+    o = np.full((total_rows, num_q_heads, head_dim), np.nan) if want_o else None
+    lse = np.full((total_rows, num_q_heads), np.nan) if want_lse else None
+    trace = np.zeros((total_rows, num_q_heads, 2), dtype=np.int64) if want_trace else None
+    rc = lib.spec_attn_oracle_run(
+        num_reqs, total_rows, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+        mask_mode, kv_dtype, float(sm_scale), _ptr(qn), _ptr(kn), _ptr(vn), _ptr(ksn),
+        _ptr(vsn), float(k_gscale), float(v_gscale), _ptr(btn), bt_stride, _ptr(sln),
+        _ptr(qin), _ptr(sel), _ptr(o), _ptr(lse), _ptr(trace))
+    if rc != 0:
+        raise ValueError(f"spec_attn_oracle_run failed with code {rc}")
+    return o, lse, trace
+
+
+def run_workload(wl, **kw):
+    """Run the oracle on a :class:`Workload` from the seeded input generators."""
+    return run(num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
+               page_size=wl.page_size, num_pages=wl.num_pages, mask_mode=wl.mask_mode,
+               kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale, q=wl.q, k_pool=wl.k_pool,
+               v_pool=wl.v_pool, block_table=wl.block_table, seq_lens=wl.seq_lens,
+               q_indptr=wl.q_indptr, k_scales=wl.k_scales, v_scales=wl.v_scales,
+               k_gscale=wl.k_gscale, v_gscale=wl.v_gscale, **kw)

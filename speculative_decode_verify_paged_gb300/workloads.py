@@ -1,0 +1,285 @@
+"""Seeded synthetic inputs for speculative-decoding block attention.
+
+This module only draws inputs: query rows, paged K/V pools, block tables,
+sequence lengths and window offsets.  It holds none of the attention
+arithmetic; the CUDA library and the CPU oracle both consume exactly the
+tensors it returns.  Everything is generated on the CPU from
+``torch.Generator().manual_seed(seed)``; values are fp32 N(0, 1) cast to bf16
+(round to nearest even).
+
+The named workloads mirror the shapes the pages measure or describe:
+
+* ``tiny``           1 request, ctx 256, W 4, Hq 4, Hkv 1, d 64, causal,
+                     17-page pool with a contiguous block table.
+* ``verify_sweep``   1 request, ctx 16384, W in {1, 8, 16}, Hq 24, Hkv 4,
+                     d 256, causal, block table = the first ceil(seq_len/16)
+                     entries of a seeded permutation of a 2048-page pool
+                     (page "ChunkedSmallT re-streams full KV per query chunk",
+                     section "Measurement": q24, batch 1, 16K bf16 and 16K
+                     fragmented rows).
+* ``long_verify``    1 request, ctx 65536, W in {8, 9, 12, 16}, same heads,
+                     K multiplied by 3 (before the bf16 cast) on a seeded 1%
+                     of key positions, 4608-page shuffled pool (same page and
+                     section, 64K bf16 row).
+* ``batched_draft``  8 requests, ctx_r uniform in [1024, 1600], W 9 (k = 8),
+                     Hq 32, Hkv 8, d 128, non-causal, one shared shuffled pool
+                     with 10% slack, block-table rows padded with -1 (page
+                     "DFlash2 leaves the paged graph fast path at every c>1",
+                     sections "The cost" and "Scope": k = 8, ctx ~ 1300,
+                     non-causal draft layers, shared paged pool).
+* ``nvfp4``          4 requests, ctx 16384, W 8, Hq 24, Hkv 4, d 256, causal,
+                     K/V quantised to e2m1 codes + one e4m3 scale per 16
+                     head_dim elements + one fp32 scale per tensor, shuffled
+                     pool (page "ChunkedSmallT ...", section "Measurement",
+                     16K nvfp4 row; the format is this library's reading).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import torch
+
+MASK_CAUSAL_IN_BLOCK = 0
+MASK_NON_CAUSAL = 1
+KV_BF16 = 0
+KV_NVFP4 = 1
+
+
+@dataclass
+class Workload:
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    mask_mode: int
+    kv_dtype: int
+    sm_scale: float
+    q: torch.Tensor               # [sum W, Hq, d] bf16
+    k_pool: torch.Tensor          # [pages, Hkv, ps, d] bf16 | [pages, Hkv, ps, d/2] uint8
+    v_pool: torch.Tensor
+    block_table: torch.Tensor     # [P, max_pages_per_req] int32, -1 past a request's pages
+    seq_lens: torch.Tensor        # [P] int32, keys in cache incl. the window's own
+    q_indptr: torch.Tensor        # [P + 1] int32 window offsets into Q rows
+    k_scales: Optional[torch.Tensor] = None   # [pages, Hkv, ps, d/16] uint8 (e4m3)
+    v_scales: Optional[torch.Tensor] = None
+    k_gscale: float = 1.0
+    v_gscale: float = 1.0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_reqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pool.shape[0])
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def max_w(self) -> int:
+        w = self.q_indptr[1:] - self.q_indptr[:-1]
+        return int(w.max().item()) if w.numel() else 0
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max().item()) if self.seq_lens.numel() else 0
+
+    @property
+    def bytes_per_token_head(self) -> int:
+        """Bytes of one key (or one value) for one KV head in the pool."""
+        if self.kv_dtype == KV_BF16:
+            return 2 * self.head_dim
+        return self.head_dim // 2 + self.head_dim // 16
+
+    @property
+    def kv_bytes(self) -> int:
+        """Algorithmic K+V bytes one call reads: every cached key of every
+        request, every KV head, K and V once (a single sweep)."""
+        return int(self.seq_lens.sum().item()) * self.num_kv_heads * 2 * self.bytes_per_token_head
+
+    def window_lengths(self):
+        return (self.q_indptr[1:] - self.q_indptr[:-1]).tolist()
+
+
+# --------------------------------------------------------------------------- #
+# NVFP4 input quantiser (test-input preparation only)
+# --------------------------------------------------------------------------- #
+_E2M1_MIDPOINTS = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def _quantise_nvfp4(x: torch.Tensor):
+    """fp32 [..., d] -> (codes uint8 [..., d/2], scales uint8 [..., d/16], gscale).
+
+    Global scale = amax / (6 * 448); block scale = e4m3(amax_block / (6 * gscale))
+    rounded to nearest even and saturated at 448; code = nearest e2m1 grid
+    point of x / (block scale * gscale), ties to the even code, saturating at
+    +-6.  An all-zero block gets scale 0 and code 0.
+    """
+    d = x.shape[-1]
+    assert d % 16 == 0
+    amax = float(x.abs().max().item())
+    gscale = amax / (6.0 * 448.0) if amax > 0 else 1.0
+    blocks = x.reshape(*x.shape[:-1], d // 16, 16)
+    amax_blk = blocks.abs().amax(dim=-1)
+    s = (amax_blk / (6.0 * gscale)).clamp(max=448.0)
+    s8 = s.to(torch.float8_e4m3fn)
+    s_dec = s8.to(torch.float32)
+    scales = s8.view(torch.uint8)
+    denom = (s_dec * gscale).unsqueeze(-1)
+    a = torch.where(denom > 0, blocks / torch.where(denom > 0, denom, torch.ones_like(denom)),
+                    torch.zeros_like(blocks))
+    mag = a.abs()
+    idx = torch.bucketize(mag, _E2M1_MIDPOINTS, right=False)
+    lower = idx.clamp(max=6)
+    tie = (idx < 7) & (mag == _E2M1_MIDPOINTS[lower])
+    idx = torch.where(tie & (idx % 2 == 1), idx + 1, idx)
+    code = idx.to(torch.uint8) | torch.where(a < 0, 8, 0).to(torch.uint8)
+    code = code.reshape(*x.shape[:-1], d)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    return packed.contiguous(), scales.contiguous(), gscale
+
+
+# --------------------------------------------------------------------------- #
+# Generic generator
+# --------------------------------------------------------------------------- #
+def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
+                  num_kv_heads: int, head_dim: int, mask_mode: int, kv_dtype: int = KV_BF16,
+                  page_size: int = 16, seed: int = 0, pool_pages: Optional[int] = None,
+                  pool_slack: float = 0.0, fragmented: bool = True, peaky_frac: float = 0.0,
+                  peaky_mult: float = 3.0, poison_unread: bool = False,
+                  sm_scale: Optional[float] = None, bt_stride: Optional[int] = None,
+                  q_mode: str = "randn", v_mode: str = "randn") -> Workload:
+    """Draw one seeded workload.
+
+    ``windows`` is one int (same W for every request) or a per-request list.
+    ``poison_unread`` fills every pool slot no request may read (slots past a
+    request's seq_len in its last page, and pages no request owns) with NaN
+    (bf16) or NaN block scales (NVFP4).  ``q_mode``/``v_mode`` 'zero' and
+    'const' (V only: a per-(kv head, dim) power of two) produce the closed-form
+    cases.
+    """
+    P = len(ctx_lens)
+    if isinstance(windows, int):
+        windows = [windows] * P
+    assert len(windows) == P
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    seq = [int(c) + int(w) for c, w in zip(ctx_lens, windows)]
+    pages_needed = [math.ceil(s / page_size) for s in seq]
+    need = sum(pages_needed)
+    if pool_pages is None:
+        pool_pages = need + int(math.ceil(need * pool_slack))
+    assert pool_pages >= need, "pool too small"
+    perm = torch.randperm(pool_pages, generator=g) if fragmented else torch.arange(pool_pages)
+    stride = bt_stride if bt_stride is not None else max(max(pages_needed, default=1), 1)
+    block_table = torch.full((P, stride), -1, dtype=torch.int32)
+    off = 0
+    for r in range(P):
+        block_table[r, : pages_needed[r]] = perm[off: off + pages_needed[r]].to(torch.int32)
+        off += pages_needed[r]
+    seq_lens = torch.tensor(seq, dtype=torch.int32)
+    q_indptr = torch.zeros(P + 1, dtype=torch.int32)
+    q_indptr[1:] = torch.cumsum(torch.tensor(windows, dtype=torch.int32), 0)
+    total_rows = int(q_indptr[-1].item())
+
+    Hq, Hkv, d, ps = num_q_heads, num_kv_heads, head_dim, page_size
+    qf = torch.randn(total_rows, Hq, d, generator=g, dtype=torch.float32)
+    if q_mode == "zero":
+        qf.zero_()
+    kf = torch.randn(pool_pages, Hkv, ps, d, generator=g, dtype=torch.float32)
+    vf = torch.randn(pool_pages, Hkv, ps, d, generator=g, dtype=torch.float32)
+    if v_mode == "const":
+        # per (kv head, dim) a power of two in [2^-3, 2^3], sign alternating
+        expo = torch.randint(-3, 4, (Hkv, d), generator=g).to(torch.float32)
+        sign = torch.where(torch.arange(d) % 2 == 0, 1.0, -1.0)
+        vf[:] = (torch.pow(2.0, expo) * sign)[None, :, None, :]
+    if peaky_frac > 0:
+        for r in range(P):
+            n = max(1, int(round(peaky_frac * seq[r])))
+            pos = torch.randperm(seq[r], generator=g)[:n]
+            pg = block_table[r, (pos // ps).long()].long()
+            sl = (pos % ps).long()
+            kf[pg, :, sl, :] *= peaky_mult
+
+    owned = torch.zeros(pool_pages, ps, dtype=torch.bool)
+    for r in range(P):
+        for p_i in range(pages_needed[r]):
+            first = p_i * ps
+            n_valid = min(ps, seq[r] - first)
+            owned[int(block_table[r, p_i]), :n_valid] = True
+
+    q = qf.to(torch.bfloat16)
+    wl_kw = {}
+    if kv_dtype == KV_BF16:
+        k_pool = kf.to(torch.bfloat16)
+        v_pool = vf.to(torch.bfloat16)
+        if poison_unread:
+            bad = (~owned)[:, None, :, None].expand_as(k_pool)
+            k_pool[bad] = float("nan")
+            v_pool[bad] = float("nan")
+    else:
+        kc, ks, kg = _quantise_nvfp4(kf)
+        vc, vs, vg = _quantise_nvfp4(vf)
+        if poison_unread:
+            bad = (~owned)[:, None, :, None]
+            ks[bad.expand_as(ks)] = 0xFF  # e4m3 NaN
+            vs[bad.expand_as(vs)] = 0xFF
+        k_pool, v_pool = kc, vc
+        wl_kw = dict(k_scales=ks, v_scales=vs, k_gscale=kg, v_gscale=vg)
+    return Workload(name=name, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, page_size=ps,
+                    mask_mode=mask_mode, kv_dtype=kv_dtype,
+                    sm_scale=(1.0 / math.sqrt(d)) if sm_scale is None else float(sm_scale),
+                    q=q, k_pool=k_pool, v_pool=v_pool, block_table=block_table,
+                    seq_lens=seq_lens, q_indptr=q_indptr,
+                    meta=dict(seed=seed, ctx_lens=list(map(int, ctx_lens)),
+                              windows=list(map(int, windows)), fragmented=fragmented,
+                              peaky_frac=peaky_frac, poison_unread=poison_unread), **wl_kw)
+
+
+# --------------------------------------------------------------------------- #
+# Named workloads
+# --------------------------------------------------------------------------- #
+def tiny(seed: int = 0, **kw) -> Workload:
+    return make_workload("tiny", [256], 4, 4, 1, 64, MASK_CAUSAL_IN_BLOCK, seed=seed,
+                         pool_pages=17, fragmented=False, **kw)
+
+
+def verify_sweep(w: int, seed: int = 0, ctx: int = 16384, **kw) -> Workload:
+    return make_workload(f"verify_sweep_ctx{ctx}_w{w}", [ctx], w, 24, 4, 256,
+                         MASK_CAUSAL_IN_BLOCK, seed=seed, pool_pages=2048, **kw)
+
+
+def long_verify(w: int, seed: int = 0, ctx: int = 65536, **kw) -> Workload:
+    return make_workload(f"long_verify_ctx{ctx}_w{w}", [ctx], w, 24, 4, 256,
+                         MASK_CAUSAL_IN_BLOCK, seed=seed, pool_pages=4608, peaky_frac=0.01, **kw)
+
+
+def batched_draft(seed: int = 0, num_reqs: int = 8, w: int = 9, **kw) -> Workload:
+    g = torch.Generator(device="cpu").manual_seed(seed + 1_000_003)
+    ctx = torch.randint(1024, 1601, (num_reqs,), generator=g).tolist()
+    return make_workload("batched_draft", ctx, w, 32, 8, 128, MASK_NON_CAUSAL, seed=seed,
+                         pool_slack=0.10, **kw)
+
+
+def nvfp4(seed: int = 0, num_reqs: int = 4, ctx: int = 16384, w: int = 8, **kw) -> Workload:
+    return make_workload(f"nvfp4_ctx{ctx}", [ctx] * num_reqs, w, 24, 4, 256,
+                         MASK_CAUSAL_IN_BLOCK, kv_dtype=KV_NVFP4, seed=seed, **kw)
+
+
+NAMED = {
+    "tiny": lambda seed=0: tiny(seed),
+    "verify_sweep_w1": lambda seed=0: verify_sweep(1, seed),
+    "verify_sweep_w8": lambda seed=0: verify_sweep(8, seed),
+    "verify_sweep_w16": lambda seed=0: verify_sweep(16, seed),
+    "long_verify_w8": lambda seed=0: long_verify(8, seed),
+    "long_verify_w9": lambda seed=0: long_verify(9, seed),
+    "long_verify_w12": lambda seed=0: long_verify(12, seed),
+    "long_verify_w16": lambda seed=0: long_verify(16, seed),
+    "batched_draft": lambda seed=0: batched_draft(seed),
+    "nvfp4": lambda seed=0: nvfp4(seed),
+}
