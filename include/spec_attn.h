@@ -1,0 +1,237 @@
+/*
+ * spec_attn.h -- C ABI of a GB300 (sm_103a) library for the attention of
+ * speculative-decoding windows against a paged KV cache.
+ *
+ * The operation.  A batch holds P requests.  Request r brings a window of
+ * W_r = q_indptr[r+1] - q_indptr[r] query rows (0 <= W_r <= 16: the seed
+ * token plus k proposed tokens) and owns seq_len[r] keys in a paged K/V cache
+ * shared by all requests.  The window's own W_r keys are already in the
+ * cache as its last W_r keys, so ctx_r = seq_len[r] - W_r keys precede it.
+ * Every window row attends to its request's cache under one of two masks:
+ *
+ *   causal-in-block: window row i sees keys 0 .. ctx_r + i (inclusive)
+ *   non-causal:      every window row sees all seq_len[r] keys
+ *
+ * and outputs are produced for window rows only, never for context rows.
+ * Sources (titles of the pages this library restates):
+ *   - "DFlash2 leaves the paged graph fast path at every c>1 and re-attends
+ *     the whole batch context every decode step", sections "The route
+ *     change" (paged store, Tq = 1+k rows, graph-captured), "The cost" (no
+ *     outputs for context rows; non-causal draft layers see their request's
+ *     whole span) and "Scope" (one shared paged pool, a batched block table,
+ *     per-request seq_lens, P x (1+k) query rows).
+ *   - "ChunkedSmallT re-streams full KV per query chunk (DFlash K>=8 verify
+ *     at long context)", sections "Finding" (key-splitting plus a reduce
+ *     kernel; the K/V sweep must not repeat per query chunk) and
+ *     "Measurement" (q24 verify windows W = 8 and 16, bf16 and nvfp4 KV).
+ *   - "perf(dflash): widen the verify window past the compact graph's
+ *     four-row limit", section "What changed" (an unsupported width must not
+ *     silently truncate; attention reads only seq_len entries).
+ *
+ * For each query row and head h (KV head h / (Hq/Hkv)):
+ *   s_j = sm_scale * <q, k_j>,  O = sum_j softmax(s)_j v_j,
+ *   LSE = max_j s_j + ln(sum_j exp(s_j - max_j s_j))     (natural log)
+ * with fp32 accumulation; O is written as bf16 (round to nearest even),
+ * LSE as fp32.
+ *
+ * Layouts (all row-major, dense):
+ *   Q, O       [total_q_rows, Hq, head_dim] bf16; the rows of request r are
+ *              q_indptr[r] .. q_indptr[r+1]-1, in window order.
+ *   LSE        [total_q_rows, Hq] fp32.
+ *   K/V pools  bf16:  [num_pages, Hkv, page_size, head_dim]
+ *              NVFP4: codes [num_pages, Hkv, page_size, head_dim/2] bytes
+ *                     (two e2m1 codes per byte, low nibble = even element),
+ *                     scales [num_pages, Hkv, page_size, head_dim/16] bytes
+ *                     (one OCP e4m3 scale per 16 contiguous elements), and
+ *                     one fp32 global scale per tensor:
+ *                     value = e2m1(code) * e4m3(scale) * gscale.
+ *   block_table [P, block_table_stride] int32: key j of request r lives in
+ *              page block_table[r][j / page_size], slot j % page_size.
+ *              Entries past ceil(seq_len[r] / page_size) are never read.
+ *   seq_lens   [P] int32;  q_indptr [P+1] int32 (q_indptr[0] == 0).
+ *
+ * Ownership: every buffer is allocated and owned by the caller.  The library
+ * allocates no device memory, makes no host<->device copy and never
+ * synchronises inside spec_attn_run / spec_attn_run_traced, so both may be
+ * captured into a CUDA graph.  A plan is a host object owned by the library
+ * between spec_attn_plan_create() and spec_attn_plan_destroy().
+ *
+ * Errors: every function returns a spec_attn_status.  Host-side checks run
+ * in spec_attn_plan_create() (shapes, limits, host copies of seq_lens and
+ * q_indptr when given) and spec_attn_run() (null or misaligned pointers,
+ * workspace size).  Device-side checks (a page id outside [0, num_pages), a
+ * seq_len above the plan's max_seq_len or below its window, a window wider
+ * than max_w) never fault: the kernels clamp the access, set a sticky error
+ * word in the workspace and go on; spec_attn_check_device_status() reads and
+ * clears it.
+ */
+#ifndef SPEC_ATTN_H
+#define SPEC_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA
+ * include.  NULL means the legacy default stream. */
+typedef struct CUstream_st* spec_attn_stream_t;
+
+typedef enum spec_attn_status {
+    SPEC_ATTN_OK = 0,
+    SPEC_ATTN_E_INVALID_ARG = -1,          /* bad shape, pointer, alignment or value */
+    SPEC_ATTN_E_UNSUPPORTED = -2,          /* valid but outside this build's limits */
+    SPEC_ATTN_E_WORKSPACE_TOO_SMALL = -3,  /* workspace_bytes below the plan's need */
+    SPEC_ATTN_E_CUDA = -4,                 /* a CUDA runtime call failed; see spec_attn_last_cuda_error */
+    SPEC_ATTN_E_DEVICE_CHECK = -5          /* a device-side check tripped (check_device_status) */
+} spec_attn_status;
+
+typedef enum spec_attn_mask_mode {
+    SPEC_ATTN_MASK_CAUSAL_IN_BLOCK = 0,
+    SPEC_ATTN_MASK_NON_CAUSAL = 1
+} spec_attn_mask_mode;
+
+typedef enum spec_attn_kv_dtype {
+    SPEC_ATTN_KV_BF16 = 0,
+    SPEC_ATTN_KV_NVFP4 = 1
+} spec_attn_kv_dtype;
+
+typedef enum spec_attn_kernel_variant {
+    SPEC_ATTN_VARIANT_AUTO = 0,       /* the library's choice for the shape */
+    SPEC_ATTN_VARIANT_CUDA_CORE = 1,  /* fp32 FMA on CUDA cores */
+    SPEC_ATTN_VARIANT_TCGEN05 = 2     /* 5th-generation tensor cores, TMEM accumulators */
+} spec_attn_kernel_variant;
+
+/* Device-status bits set by the kernels (spec_attn_check_device_status). */
+#define SPEC_ATTN_DEV_BAD_PAGE      0x1u  /* block-table entry outside [0, num_pages) */
+#define SPEC_ATTN_DEV_BAD_SEQ_LEN   0x2u  /* seq_len > max_seq_len or table capacity, or < W_r */
+#define SPEC_ATTN_DEV_BAD_WINDOW    0x4u  /* W_r < 0, W_r > max_w, or rows past total_q_rows */
+#define SPEC_ATTN_DEV_WAIT_TIMEOUT  0x8u  /* a pipeline wait gave up (bounded spin) */
+
+/* Limits of this build. */
+#define SPEC_ATTN_MAX_W 16
+#define SPEC_ATTN_MAX_GROUP 16       /* Hq / Hkv */
+#define SPEC_ATTN_PAGE_SIZE 16
+
+typedef struct spec_attn_problem {
+    int32_t num_reqs;            /* P >= 0 */
+    int32_t total_q_rows;        /* rows of Q and O (sum of all W_r) */
+    int32_t max_w;               /* upper bound on every W_r, 1..16 */
+    int32_t num_q_heads;         /* Hq */
+    int32_t num_kv_heads;        /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 16 */
+    int32_t head_dim;            /* 64, 128 or 256 */
+    int32_t page_size;           /* 16 */
+    int32_t num_pages;           /* pages in each pool (device bounds check) */
+    int32_t block_table_stride;  /* int32 entries per block-table row */
+    int32_t mask_mode;           /* spec_attn_mask_mode */
+    int32_t kv_dtype;            /* spec_attn_kv_dtype */
+    float sm_scale;              /* softmax scale; 0 selects 1/sqrt(head_dim) */
+    int64_t max_seq_len;         /* upper bound on every seq_len the plan will see */
+    int32_t force_splits;        /* 0: heuristic; n > 0: split the longest request's keys n ways */
+    int32_t kernel_variant;      /* spec_attn_kernel_variant */
+} spec_attn_problem;
+
+typedef struct spec_attn_plan spec_attn_plan;   /* opaque */
+
+/* What a plan decided; for tests, benches and logs. */
+typedef struct spec_attn_plan_info {
+    int32_t kernel_variant;      /* the variant that will run (never AUTO) */
+    int32_t keys_per_split;      /* keys of one request one CTA sweeps (multiple of 64) */
+    int32_t max_splits;          /* splits of the longest request */
+    int32_t row_groups;          /* CTAs sharing one (request, KV head, split); 1 for tcgen05 */
+    int32_t grid_x, grid_y, grid_z;
+    int32_t block_threads;
+    int32_t smem_bytes;          /* dynamic shared memory of the split kernel */
+    int32_t uses_merge;          /* 1 when a second (LSE-merge) kernel runs */
+    int32_t num_sms;
+    size_t workspace_bytes;
+} spec_attn_plan_info;
+
+/*
+ * Validate a problem and choose the split count (keys per split) and the
+ * kernel variant.  Host only; no device allocation.  h_seq_lens [P] and
+ * h_q_indptr [P+1] are optional host copies: when given they are checked
+ * and used by the split heuristic; otherwise max_seq_len and max_w stand in
+ * for every request.  A plan may be reused for every layer of a step and
+ * replayed inside a CUDA graph while every device seq_len stays at or below
+ * max_seq_len.  *out receives the plan; *workspace_bytes (nullable) receives
+ * the bytes spec_attn_run needs.  The CUDA device current at this call is
+ * the one the plan targets.
+ */
+int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq_lens,
+                          const int32_t* h_q_indptr, spec_attn_plan** out,
+                          size_t* workspace_bytes);
+
+int spec_attn_plan_destroy(spec_attn_plan* plan);
+
+int spec_attn_plan_get_info(const spec_attn_plan* plan, spec_attn_plan_info* info);
+
+/*
+ * Run one attention call asynchronously on `stream`.
+ *   q         [total_q_rows, Hq, d] bf16, 16-byte aligned
+ *   k_pool, v_pool   pools as above, 16-byte aligned (NVFP4: code pools)
+ *   k_scales, v_scales  NVFP4 scale pools, 16-byte aligned; NULL for bf16
+ *   k_gscale, v_gscale  NVFP4 global scales; ignored for bf16
+ *   block_table [P, block_table_stride] int32, seq_lens [P], q_indptr [P+1]
+ *   o         [total_q_rows, Hq, d] bf16 output, 16-byte aligned
+ *   lse       [total_q_rows, Hq] fp32 output, or NULL
+ *   workspace caller-owned device scratch of at least the plan's
+ *             workspace_bytes, 256-byte aligned; its first 256 bytes hold the
+ *             sticky device-status word, which the caller zeroes once after
+ *             allocating it (spec_attn_reset_device_status).  One workspace
+ *             must not be shared by runs that may overlap on the GPU.
+ * All device pointers must belong to the plan's device.  Returns
+ * SPEC_ATTN_E_CUDA if a launch fails.
+ */
+int spec_attn_run(const spec_attn_plan* plan, const void* q, const void* k_pool,
+                  const void* v_pool, const void* k_scales, const void* v_scales,
+                  float k_gscale, float v_gscale, const int32_t* block_table,
+                  const int32_t* seq_lens, const int32_t* q_indptr, void* o, float* lse,
+                  void* workspace, size_t workspace_bytes, spec_attn_stream_t stream);
+
+/*
+ * spec_attn_run plus an index/mask trace: trace [total_q_rows, Hq, 2] int64
+ * (zeroed by the caller) receives, for every output (row, head), the number
+ * of keys the kernels let into its softmax and the sum of their physical
+ * slot ids (page * page_size + slot), accumulated over all splits.  This is
+ * the floating-point-free check that every row saw exactly its mask's keys
+ * through the block table.  Slower than spec_attn_run; for validation.
+ */
+int spec_attn_run_traced(const spec_attn_plan* plan, const void* q, const void* k_pool,
+                         const void* v_pool, const void* k_scales, const void* v_scales,
+                         float k_gscale, float v_gscale, const int32_t* block_table,
+                         const int32_t* seq_lens, const int32_t* q_indptr, void* o,
+                         float* lse, int64_t* trace, void* workspace,
+                         size_t workspace_bytes, spec_attn_stream_t stream);
+
+/*
+ * Optional timing hooks: when set (both non-NULL; cudaEvent_t values), every
+ * later run records `split_begin` on its stream just before the split-KV
+ * kernel launch and `split_end` just after it, so a caller can time that
+ * kernel alone with cudaEventElapsedTime.  Pass NULLs to clear.
+ */
+int spec_attn_plan_set_timing_events(spec_attn_plan* plan, void* split_begin, void* split_end);
+
+/* Zero the workspace's device-status word (asynchronous on `stream`). */
+int spec_attn_reset_device_status(void* workspace, spec_attn_stream_t stream);
+
+/* Synchronise `stream`, read the device-status word into *bits (nullable)
+ * and clear it.  Returns SPEC_ATTN_E_DEVICE_CHECK when any bit was set. */
+int spec_attn_check_device_status(void* workspace, spec_attn_stream_t stream, uint32_t* bits);
+
+/* Name of a status code; never NULL. */
+const char* spec_attn_status_string(int status);
+
+/* The last CUDA error code this thread saw inside the library (0 if none). */
+int spec_attn_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int spec_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_ATTN_H */
