@@ -1,0 +1,443 @@
+// Host side of the C ABI (include/spec_attn.h): validation, the split-count
+// heuristic, workspace layout and the kernel launches.
+//
+// The split heuristic restates the key-splitting idea of the page
+// "ChunkedSmallT re-streams full KV per query chunk (DFlash K>=8 verify at
+// long context)" (section "Finding": keys are split across CTAs and a reduce
+// kernel merges the partials) without its width cap: every CTA holds all
+// W x G query rows of one KV head, so the K/V of a window is swept once for
+// any W <= 16, and an unsupported width is an explicit error rather than a
+// silent truncation (page "perf(dflash): widen the verify window past the
+// compact graph's four-row limit", section "What changed").
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/spec_attn.h"
+#include "spec_attn_internal.h"
+
+using namespace spec_attn;
+
+struct spec_attn_plan {
+    spec_attn_problem prob;
+    int device;
+    int num_sms;
+    int variant;
+    int keys_per_split;
+    int max_splits;
+    int row_groups;
+    int rows_per_cta;
+    CcConfig cc;
+    dim3 grid;
+    int threads;
+    int smem;
+    bool uses_merge;
+    size_t ws_bytes;
+    size_t ws_lse_off;
+    size_t ws_o_off;
+    float sm_scale;
+    cudaEvent_t ev_begin;
+    cudaEvent_t ev_end;
+};
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return SPEC_ATTN_E_CUDA;
+}
+
+constexpr size_t kStatusBytes = 256;
+constexpr int kSplitUnit = 64;  // keys; a multiple of the page size and of every kernel's key tile
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t bytes_per_token_head(int kv_dtype, int d) {
+    return kv_dtype == SPEC_ATTN_KV_BF16 ? static_cast<size_t>(2 * d) : static_cast<size_t>(d / 2 + d / 16);
+}
+
+// Rough cost (microseconds) of one call with `c` keys per split.  Terms:
+//   waves of CTAs, each paying a fixed start/finish cost plus its keys at the
+//   per-CTA streaming (or compute) rate; the whole job can not beat HBM; and
+//   the merge reads every partial once more.
+struct CostModel {
+    double hbm_bytes_per_us = 6.5e6;   // ~6.5 TB/s
+    double l2_bytes_per_us = 2.0e7;    // partials stay in L2
+    double cta_fixed_us = 3.0;
+    double merge_fixed_us = 2.0;
+    double key_us = 0.0;               // one CTA's time per key (set per variant)
+};
+
+int choose_keys_per_split(const std::vector<int64_t>& lens, int64_t max_seq, int hkv, int row_groups,
+                          int slots, double total_bytes, double partial_bytes_per_split,
+                          const CostModel& cm) {
+    const int64_t max_units = std::max<int64_t>(1, (max_seq + kSplitUnit - 1) / kSplitUnit);
+    double best = 1e300;
+    int best_c = static_cast<int>(max_units * kSplitUnit);
+    for (int64_t u = 1; u <= max_units; ++u) {
+        const int64_t c = u * kSplitUnit;
+        int64_t ctas = 0;
+        for (int64_t L : lens) ctas += static_cast<int64_t>(hkv) * row_groups * ((L + c - 1) / c);
+        const int64_t splits = (max_seq + c - 1) / c;
+        const int64_t waves = (ctas + slots - 1) / slots;
+        const double t_cta = cm.cta_fixed_us + static_cast<double>(c) * cm.key_us;
+        const double t_waves = static_cast<double>(waves) * t_cta;
+        const double t_bw = total_bytes / cm.hbm_bytes_per_us;
+        const double t_merge = splits > 1
+            ? cm.merge_fixed_us + static_cast<double>(splits) * partial_bytes_per_split / cm.l2_bytes_per_us
+            : 0.0;
+        const double cost = std::max(t_waves, t_bw) + t_merge;
+        if (cost < best * (1.0 - 1e-9)) {
+            best = cost;
+            best_c = static_cast<int>(c);
+        }
+    }
+    return best_c;
+}
+
+int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, const int32_t* h_q_indptr) {
+    if (!p) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->num_reqs < 0 || p->total_q_rows < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
+        p->head_dim <= 0 || p->page_size <= 0 || p->max_w < 1 || p->max_seq_len < 0 ||
+        p->block_table_stride < 0 || p->num_pages < 0 || p->force_splits < 0)
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->mask_mode != SPEC_ATTN_MASK_CAUSAL_IN_BLOCK && p->mask_mode != SPEC_ATTN_MASK_NON_CAUSAL)
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (p->kv_dtype != SPEC_ATTN_KV_BF16 && p->kv_dtype != SPEC_ATTN_KV_NVFP4) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->kernel_variant < SPEC_ATTN_VARIANT_AUTO || p->kernel_variant > SPEC_ATTN_VARIANT_TCGEN05)
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (!(p->sm_scale >= 0.f) || std::isinf(p->sm_scale)) return SPEC_ATTN_E_INVALID_ARG;
+    // limits of this build: fail loudly, never truncate a window
+    if (p->max_w > SPEC_ATTN_MAX_W) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->num_q_heads / p->num_kv_heads > SPEC_ATTN_MAX_GROUP) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->page_size != SPEC_ATTN_PAGE_SIZE) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->max_seq_len > INT32_MAX) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->num_kv_heads > 65535 || p->num_reqs > 65535) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->num_reqs > 0) {
+        if (p->max_seq_len < 1 || p->num_pages < 1) return SPEC_ATTN_E_INVALID_ARG;
+        const int64_t need_pages = (p->max_seq_len + p->page_size - 1) / p->page_size;
+        if (p->block_table_stride < need_pages) return SPEC_ATTN_E_INVALID_ARG;
+    }
+    if (h_q_indptr) {
+        if (h_q_indptr[0] != 0) return SPEC_ATTN_E_INVALID_ARG;
+        for (int r = 0; r < p->num_reqs; ++r) {
+            const int w = h_q_indptr[r + 1] - h_q_indptr[r];
+            if (w < 0) return SPEC_ATTN_E_INVALID_ARG;
+            if (w > SPEC_ATTN_MAX_W) return SPEC_ATTN_E_UNSUPPORTED;
+            if (w > p->max_w) return SPEC_ATTN_E_INVALID_ARG;
+        }
+        if (h_q_indptr[p->num_reqs] > p->total_q_rows) return SPEC_ATTN_E_INVALID_ARG;
+    }
+    if (h_seq_lens) {
+        for (int r = 0; r < p->num_reqs; ++r) {
+            if (h_seq_lens[r] < 0 || h_seq_lens[r] > p->max_seq_len) return SPEC_ATTN_E_INVALID_ARG;
+            if (h_q_indptr && h_seq_lens[r] < h_q_indptr[r + 1] - h_q_indptr[r]) return SPEC_ATTN_E_INVALID_ARG;
+        }
+    }
+    return SPEC_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_attn_version(void) { return 100; }
+
+int spec_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* spec_attn_status_string(int status) {
+    switch (status) {
+        case SPEC_ATTN_OK: return "ok";
+        case SPEC_ATTN_E_INVALID_ARG: return "invalid argument";
+        case SPEC_ATTN_E_UNSUPPORTED: return "unsupported by this build (W > 16, head_dim not in {64,128,256}, page_size != 16, group > 16, ...)";
+        case SPEC_ATTN_E_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case SPEC_ATTN_E_CUDA: return "CUDA runtime error";
+        case SPEC_ATTN_E_DEVICE_CHECK: return "a device-side check tripped";
+        default: return "unknown status";
+    }
+}
+
+int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq_lens,
+                          const int32_t* h_q_indptr, spec_attn_plan** out, size_t* workspace_bytes) {
+    if (!out) return SPEC_ATTN_E_INVALID_ARG;
+    *out = nullptr;
+    int st = validate_problem(problem, h_seq_lens, h_q_indptr);
+    if (st != SPEC_ATTN_OK) return st;
+    const spec_attn_problem& p = *problem;
+
+    spec_attn_plan* plan = new (std::nothrow) spec_attn_plan();
+    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    plan->prob = p;
+    plan->sm_scale = p.sm_scale > 0.f ? p.sm_scale : 1.0f / std::sqrt(static_cast<float>(p.head_dim));
+    plan->ev_begin = nullptr;
+    plan->ev_end = nullptr;
+
+    cudaError_t e = cudaGetDevice(&plan->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device);
+    if (e != cudaSuccess) {
+        delete plan;
+        return cuda_fail(e);
+    }
+
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const int max_rows = p.max_w * G;
+    // Only the CUDA-core variant exists in this build; AUTO resolves to it.
+    if (p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05) {
+        delete plan;
+        return SPEC_ATTN_E_UNSUPPORTED;
+    }
+    plan->variant = SPEC_ATTN_VARIANT_CUDA_CORE;
+    plan->cc = cc_config(p.head_dim, p.kv_dtype, max_rows);
+    plan->rows_per_cta = 8 * plan->cc.rows_per_warp;
+    plan->row_groups = (max_rows + plan->rows_per_cta - 1) / plan->rows_per_cta;
+    plan->threads = plan->cc.threads;
+    plan->smem = plan->cc.smem_bytes;
+    e = cc_prepare(p.head_dim, p.kv_dtype, plan->cc);
+    if (e != cudaSuccess) {
+        delete plan;
+        return cuda_fail(e);
+    }
+
+    // ---- split heuristic ----
+    std::vector<int64_t> lens;
+    lens.reserve(static_cast<size_t>(p.num_reqs));
+    for (int r = 0; r < p.num_reqs; ++r) {
+        int64_t L = h_seq_lens ? h_seq_lens[r] : p.max_seq_len;
+        if (h_q_indptr && h_q_indptr[r + 1] == h_q_indptr[r]) L = 0;  // empty window: no CTAs do work
+        lens.push_back(L);
+    }
+    const int64_t max_seq = std::max<int64_t>(1, p.max_seq_len);
+    const size_t bkh = bytes_per_token_head(p.kv_dtype, p.head_dim);
+    double total_bytes = 0;
+    for (int64_t L : lens) total_bytes += static_cast<double>(L) * p.num_kv_heads * 2.0 * bkh;
+    int occ = 1;
+    {
+        // CTAs the split kernel fits per SM (smem bound for the CUDA-core variant)
+        int max_smem = 0;
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, plan->device);
+        occ = std::max(1, std::min(max_smem / std::max(1, plan->smem + 1024), 2048 / plan->threads));
+    }
+    CostModel cm;
+    {
+        // CUDA cores: ~2 FMA per element per row (QK and PV) at ~128 FMA/clk/SM,
+        // ~1.9 GHz, shared by `occ` CTAs, times an instruction-overhead factor.
+        const double fma_per_us = 128.0 * 1.9e3 / occ;
+        const double rows = std::min(max_rows, plan->rows_per_cta);
+        const double t_compute = rows * 2.0 * p.head_dim * 2.0 / fma_per_us;
+        const double t_stream = 2.0 * bkh / (6.5e6 / (plan->num_sms * occ));
+        cm.key_us = std::max(t_compute, t_stream);
+    }
+    const double partial_bytes = static_cast<double>(p.total_q_rows) * p.num_q_heads * (p.head_dim + 1) * 4.0 * 2.0;
+    if (p.force_splits > 0) {
+        int64_t c = (max_seq + p.force_splits - 1) / p.force_splits;
+        c = (c + kSplitUnit - 1) / kSplitUnit * kSplitUnit;
+        plan->keys_per_split = static_cast<int>(std::max<int64_t>(c, kSplitUnit));
+    } else {
+        plan->keys_per_split = choose_keys_per_split(lens, max_seq, p.num_kv_heads, plan->row_groups,
+                                                     plan->num_sms * occ, total_bytes, partial_bytes, cm);
+    }
+    plan->max_splits = static_cast<int>((max_seq + plan->keys_per_split - 1) / plan->keys_per_split);
+    plan->uses_merge = plan->max_splits > 1;
+    plan->grid = dim3(static_cast<unsigned>(plan->max_splits * plan->row_groups),
+                      static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(std::max(1, p.num_reqs)));
+
+    // ---- workspace layout: [status 256 B][lse partials][O partials] ----
+    plan->ws_lse_off = kStatusBytes;
+    size_t ws = kStatusBytes;
+    if (plan->uses_merge) {
+        const size_t pairs = static_cast<size_t>(p.total_q_rows) * p.num_q_heads;
+        ws = align_up(plan->ws_lse_off + static_cast<size_t>(plan->max_splits) * pairs * sizeof(float), 256);
+        plan->ws_o_off = ws;
+        ws += static_cast<size_t>(plan->max_splits) * pairs * p.head_dim * sizeof(float);
+    } else {
+        plan->ws_o_off = kStatusBytes;
+    }
+    plan->ws_bytes = align_up(ws, 256);
+    if (workspace_bytes) *workspace_bytes = plan->ws_bytes;
+    *out = plan;
+    return SPEC_ATTN_OK;
+}
+
+int spec_attn_plan_destroy(spec_attn_plan* plan) {
+    delete plan;
+    return SPEC_ATTN_OK;
+}
+
+int spec_attn_plan_get_info(const spec_attn_plan* plan, spec_attn_plan_info* info) {
+    if (!plan || !info) return SPEC_ATTN_E_INVALID_ARG;
+    std::memset(info, 0, sizeof(*info));
+    info->kernel_variant = plan->variant;
+    info->keys_per_split = plan->keys_per_split;
+    info->max_splits = plan->max_splits;
+    info->row_groups = plan->row_groups;
+    info->grid_x = static_cast<int32_t>(plan->grid.x);
+    info->grid_y = static_cast<int32_t>(plan->grid.y);
+    info->grid_z = static_cast<int32_t>(plan->grid.z);
+    info->block_threads = plan->threads;
+    info->smem_bytes = plan->smem;
+    info->uses_merge = plan->uses_merge ? 1 : 0;
+    info->num_sms = plan->num_sms;
+    info->workspace_bytes = plan->ws_bytes;
+    return SPEC_ATTN_OK;
+}
+
+int spec_attn_plan_set_timing_events(spec_attn_plan* plan, void* split_begin, void* split_end) {
+    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    if ((split_begin == nullptr) != (split_end == nullptr)) return SPEC_ATTN_E_INVALID_ARG;
+    plan->ev_begin = static_cast<cudaEvent_t>(split_begin);
+    plan->ev_end = static_cast<cudaEvent_t>(split_end);
+    return SPEC_ATTN_OK;
+}
+
+static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                    const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
+                    const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                    void* o, float* lse, int64_t* trace, void* workspace, size_t workspace_bytes,
+                    spec_attn_stream_t stream_handle) {
+    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    const spec_attn_problem& p = plan->prob;
+    if (p.num_reqs == 0 || p.total_q_rows == 0) return SPEC_ATTN_OK;
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !q_indptr || !o || !workspace)
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(q_indptr, 4) ||
+        !aligned(workspace, 256) || (lse && !aligned(lse, 4)) || (trace && !aligned(trace, 8)))
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (p.kv_dtype == SPEC_ATTN_KV_NVFP4) {
+        if (!k_scales || !v_scales || !aligned(k_scales, 16) || !aligned(v_scales, 16))
+            return SPEC_ATTN_E_INVALID_ARG;
+        if (!(k_gscale > 0.f) || !(v_gscale > 0.f) || std::isinf(k_gscale) || std::isinf(v_gscale))
+            return SPEC_ATTN_E_INVALID_ARG;
+    }
+    if (workspace_bytes < plan->ws_bytes) return SPEC_ATTN_E_WORKSPACE_TOO_SMALL;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev != plan->device) return SPEC_ATTN_E_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    SplitParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.q = static_cast<const uint16_t*>(q);
+    sp.k_pool = k_pool;
+    sp.v_pool = v_pool;
+    sp.k_scales = static_cast<const uint8_t*>(k_scales);
+    sp.v_scales = static_cast<const uint8_t*>(v_scales);
+    sp.block_table = block_table;
+    sp.seq_lens = seq_lens;
+    sp.q_indptr = q_indptr;
+    sp.o = static_cast<uint16_t*>(o);
+    sp.lse = lse;
+    sp.trace = reinterpret_cast<long long*>(trace);
+    sp.status = reinterpret_cast<unsigned int*>(ws);
+    sp.ws_lse = reinterpret_cast<float*>(ws + plan->ws_lse_off);
+    sp.ws_o = reinterpret_cast<float*>(ws + plan->ws_o_off);
+    sp.num_reqs = p.num_reqs;
+    sp.total_rows = p.total_q_rows;
+    sp.max_w = p.max_w;
+    sp.num_q_heads = p.num_q_heads;
+    sp.num_kv_heads = p.num_kv_heads;
+    sp.group = p.num_q_heads / p.num_kv_heads;
+    sp.head_dim = p.head_dim;
+    sp.page_size = p.page_size;
+    sp.num_pages = p.num_pages;
+    sp.bt_stride = p.block_table_stride;
+    sp.mask_mode = p.mask_mode;
+    sp.keys_per_split = plan->keys_per_split;
+    sp.max_splits = plan->max_splits;
+    sp.row_groups = plan->row_groups;
+    sp.rows_per_cta = plan->rows_per_cta;
+    sp.max_seq_len = p.max_seq_len;
+    const float log2e = 1.4426950408889634f;
+    const bool fp4 = p.kv_dtype == SPEC_ATTN_KV_NVFP4;
+    sp.score_scale_log2 = plan->sm_scale * log2e * (fp4 ? k_gscale : 1.0f);
+    sp.out_scale = fp4 ? v_gscale : 1.0f;
+
+    if (plan->ev_begin) {
+        e = cudaEventRecord(plan->ev_begin, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = cc_launch(sp, p.kv_dtype, plan->cc, trace != nullptr, plan->grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (plan->ev_end) {
+        e = cudaEventRecord(plan->ev_end, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (plan->uses_merge) {
+        MergeParams mp;
+        std::memset(&mp, 0, sizeof(mp));
+        mp.seq_lens = seq_lens;
+        mp.q_indptr = q_indptr;
+        mp.ws_o = sp.ws_o;
+        mp.ws_lse = sp.ws_lse;
+        mp.o = sp.o;
+        mp.lse = lse;
+        mp.num_reqs = p.num_reqs;
+        mp.total_rows = p.total_q_rows;
+        mp.max_w = p.max_w;
+        mp.num_q_heads = p.num_q_heads;
+        mp.head_dim = p.head_dim;
+        mp.keys_per_split = plan->keys_per_split;
+        mp.max_splits = plan->max_splits;
+        mp.max_seq_len = p.max_seq_len;
+        mp.bt_capacity_keys = p.block_table_stride * p.page_size;
+        // programmatic launch lets the merge's CTAs become resident while the
+        // split kernel drains; it is skipped when a timing event sits between.
+        e = merge_launch(mp, stream, plan->ev_end == nullptr);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return SPEC_ATTN_OK;
+}
+
+int spec_attn_run(const spec_attn_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                  const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
+                  const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                  void* o, float* lse, void* workspace, size_t workspace_bytes,
+                  spec_attn_stream_t stream) {
+    return run_impl(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
+                    seq_lens, q_indptr, o, lse, nullptr, workspace, workspace_bytes, stream);
+}
+
+int spec_attn_run_traced(const spec_attn_plan* plan, const void* q, const void* k_pool,
+                         const void* v_pool, const void* k_scales, const void* v_scales,
+                         float k_gscale, float v_gscale, const int32_t* block_table,
+                         const int32_t* seq_lens, const int32_t* q_indptr, void* o, float* lse,
+                         int64_t* trace, void* workspace, size_t workspace_bytes,
+                         spec_attn_stream_t stream) {
+    if (!trace) return SPEC_ATTN_E_INVALID_ARG;
+    return run_impl(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
+                    seq_lens, q_indptr, o, lse, trace, workspace, workspace_bytes, stream);
+}
+
+int spec_attn_reset_device_status(void* workspace, spec_attn_stream_t stream) {
+    if (!workspace) return SPEC_ATTN_E_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPEC_ATTN_OK : cuda_fail(e);
+}
+
+int spec_attn_check_device_status(void* workspace, spec_attn_stream_t stream_handle, uint32_t* bits) {
+    if (!workspace) return SPEC_ATTN_E_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(v), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (bits) *bits = v;
+    return v ? SPEC_ATTN_E_DEVICE_CHECK : SPEC_ATTN_OK;
+}
+
+}  // extern "C"

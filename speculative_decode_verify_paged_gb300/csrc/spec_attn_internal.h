@@ -1,0 +1,87 @@
+// Internal interface between the host library (plan / run) and the kernels.
+// Not installed; the public ABI is include/spec_attn.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace spec_attn {
+
+// Everything one split-KV launch needs.  Plain pointers and ints only.
+struct SplitParams {
+    const uint16_t* q;          // [total_rows, Hq, d] bf16 bits
+    const void* k_pool;         // bf16 [pages, Hkv, ps, d] | nvfp4 codes [pages, Hkv, ps, d/2]
+    const void* v_pool;
+    const uint8_t* k_scales;    // nvfp4 e4m3 [pages, Hkv, ps, d/16]
+    const uint8_t* v_scales;
+    const int32_t* block_table; // [P, bt_stride]
+    const int32_t* seq_lens;    // [P]
+    const int32_t* q_indptr;    // [P + 1]
+    uint16_t* o;                // [total_rows, Hq, d] bf16 bits
+    float* lse;                 // [total_rows, Hq] or nullptr
+    long long* trace;           // [total_rows, Hq, 2] or nullptr
+    float* ws_o;                // [max_splits, total_rows, Hq, d] fp32 partials
+    float* ws_lse;              // [max_splits, total_rows, Hq] fp32 partial LSE (log2 units)
+    unsigned int* status;       // sticky device-status word
+    int num_reqs;
+    int total_rows;
+    int max_w;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                  // Hq / Hkv
+    int head_dim;
+    int page_size;
+    int num_pages;
+    int bt_stride;
+    int mask_mode;
+    int keys_per_split;         // multiple of 64
+    int max_splits;
+    int row_groups;             // CTAs per (request, KV head, split) (CUDA-core path)
+    int rows_per_cta;
+    long long max_seq_len;
+    float score_scale_log2;     // sm_scale * log2(e) [* k_gscale for NVFP4]
+    float out_scale;            // 1, or v_gscale for NVFP4
+};
+
+struct MergeParams {
+    const int32_t* seq_lens;
+    const int32_t* q_indptr;
+    const float* ws_o;
+    const float* ws_lse;
+    uint16_t* o;
+    float* lse;
+    int num_reqs;
+    int total_rows;
+    int max_w;
+    int num_q_heads;
+    int head_dim;
+    int keys_per_split;
+    int max_splits;
+    long long max_seq_len;
+    int bt_capacity_keys;       // bt_stride * page_size
+};
+
+// Device-status bits (mirror the public SPEC_ATTN_DEV_* values).
+constexpr unsigned int kDevBadPage = 0x1u;
+constexpr unsigned int kDevBadSeqLen = 0x2u;
+constexpr unsigned int kDevBadWindow = 0x4u;
+constexpr unsigned int kDevWaitTimeout = 0x8u;
+
+// ---- CUDA-core split-KV kernel (split_attn_cc.cu) ----
+struct CcConfig {
+    int rows_per_warp;   // 1, 2 or 4
+    int stages;          // pages in the cp.async ring
+    int smem_bytes;
+    int threads;
+};
+CcConfig cc_config(int head_dim, int kv_dtype, int max_rows);
+// Prepare (max dynamic smem attribute) the instance a config uses; returns a CUDA error code.
+cudaError_t cc_prepare(int head_dim, int kv_dtype, const CcConfig& cfg);
+cudaError_t cc_launch(const SplitParams& p, int kv_dtype, const CcConfig& cfg, bool traced,
+                      dim3 grid, cudaStream_t stream);
+
+// ---- LSE merge (merge_lse.cu) ----
+cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic);
+
+}  // namespace spec_attn

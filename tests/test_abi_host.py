@@ -1,0 +1,108 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+symbol include/spec_attn.h declares, and host-side validation rejects bad
+problems before touching a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import speculative_decode_verify_paged_gb300 as sa
+from speculative_decode_verify_paged_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return sa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(spec_attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert sorted(sa.EXPORTED_SYMBOLS) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sa.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_version(lib):
+    assert sa.spec_attn_version() == 100
+    for st in (0, -1, -2, -3, -4, -5):
+        assert sa.status_string(st) and sa.status_string(st) != "unknown status"
+    assert sa.status_string(12345) == "unknown status"
+
+
+def _problem(**over):
+    base = dict(num_reqs=1, total_q_rows=4, max_w=4, num_q_heads=4, num_kv_heads=1, head_dim=64,
+                page_size=16, num_pages=17, block_table_stride=17, mask_mode=0, kv_dtype=0,
+                sm_scale=0.0, max_seq_len=260, force_splits=0, kernel_variant=0)
+    base.update(over)
+    return base
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(max_w=17), sa.SPEC_ATTN_E_UNSUPPORTED),            # W > 16 fails loudly
+    (dict(head_dim=96), sa.SPEC_ATTN_E_UNSUPPORTED),
+    (dict(page_size=32), sa.SPEC_ATTN_E_UNSUPPORTED),
+    (dict(num_q_heads=34, num_kv_heads=2), sa.SPEC_ATTN_E_UNSUPPORTED),  # group 17
+    (dict(num_q_heads=6, num_kv_heads=4), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(max_w=0), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(mask_mode=2), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(kv_dtype=3), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(block_table_stride=16), sa.SPEC_ATTN_E_INVALID_ARG),  # 260 keys need 17 pages
+    (dict(sm_scale=-1.0), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(kernel_variant=7), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(num_reqs=-1), sa.SPEC_ATTN_E_INVALID_ARG),
+])
+def test_plan_rejects_bad_problems_on_the_host(lib, over, status):
+    pr = sa.spec_attn_problem(**_problem(**over))
+    handle = ctypes.c_void_p()
+    st = lib.spec_attn_plan_create(ctypes.byref(pr), None, None, ctypes.byref(handle), None)
+    assert st == status
+    assert not handle.value
+
+
+def test_plan_checks_host_windows_and_lengths(lib):
+    import numpy as np
+    pr = sa.spec_attn_problem(**_problem(num_reqs=2, total_q_rows=8))
+    handle = ctypes.c_void_p()
+    qi = np.array([0, 4, 21], dtype=np.int32)   # second window 17 rows
+    st = lib.spec_attn_plan_create(ctypes.byref(pr), None, qi.ctypes.data_as(ctypes.c_void_p),
+                                   ctypes.byref(handle), None)
+    assert st == sa.SPEC_ATTN_E_UNSUPPORTED
+    qi = np.array([0, 4, 8], dtype=np.int32)
+    sl = np.array([260, 3], dtype=np.int32)     # seq_len below its window
+    st = lib.spec_attn_plan_create(ctypes.byref(pr), sl.ctypes.data_as(ctypes.c_void_p),
+                                   qi.ctypes.data_as(ctypes.c_void_p), ctypes.byref(handle), None)
+    assert st == sa.SPEC_ATTN_E_INVALID_ARG
+    sl = np.array([261, 100], dtype=np.int32)   # above max_seq_len
+    st = lib.spec_attn_plan_create(ctypes.byref(pr), sl.ctypes.data_as(ctypes.c_void_p),
+                                   qi.ctypes.data_as(ctypes.c_void_p), ctypes.byref(handle), None)
+    assert st == sa.SPEC_ATTN_E_INVALID_ARG
+
+
+def test_null_arguments(lib):
+    assert lib.spec_attn_plan_create(None, None, None, None, None) == sa.SPEC_ATTN_E_INVALID_ARG
+    assert lib.spec_attn_plan_get_info(None, None) == sa.SPEC_ATTN_E_INVALID_ARG
+    assert lib.spec_attn_reset_device_status(None, None) == sa.SPEC_ATTN_E_INVALID_ARG
+    assert lib.spec_attn_check_device_status(None, None, None) == sa.SPEC_ATTN_E_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        sa.load_library(str(tmp_path / "nope.so"))

@@ -1,0 +1,325 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Tolerances (bf16 output, fp32 accumulation): |dO| <= 1e-2 max and <= 1e-3
+mean over the compared elements; |dLSE| <= 1e-4 * max(1, |LSE|).  Index and
+mask decisions are compared bit-exactly through the traced run (count of
+keys let into each row's softmax and the sum of their physical slot ids).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decode_verify_paged_gb300 as sa
+from speculative_decode_verify_paged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_REL = 1e-2, 1e-3, 1e-4
+VARIANTS = [sa.SPEC_ATTN_VARIANT_AUTO, sa.SPEC_ATTN_VARIANT_CUDA_CORE]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decode_verify_paged_gb300 import build as libbuild
+    libbuild.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def check_close(o_gpu, lse_gpu, o_ref, lse_ref, sel=None):
+    o = o_gpu.float().cpu().numpy().astype(np.float64)
+    lse = lse_gpu.cpu().numpy().astype(np.float64)
+    if sel is not None:
+        m = sel.astype(bool)
+        o, o_ref, lse, lse_ref = o[m], o_ref[m], lse[m], lse_ref[m]
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    err = np.abs(o - o_ref)
+    assert err.max() <= O_MAX, f"max |dO| {err.max():.3e}"
+    assert err.mean() <= O_MEAN, f"mean |dO| {err.mean():.3e}"
+    rel = np.abs(lse - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+    assert rel.max() <= LSE_REL, f"max rel dLSE {rel.max():.3e}"
+    return err.max(), rel.max()
+
+
+def run_and_check(wl, variant=0, force_splits=0, trace=True, sel=None, host_lens=True):
+    dw = sa.DeviceWorkload(wl, "cuda", force_splits=force_splits, kernel_variant=variant,
+                           host_lens=host_lens)
+    if trace:
+        tr = torch.zeros(wl.total_rows, wl.num_q_heads, 2, dtype=torch.int64, device="cuda")
+        dw.run_traced(tr)
+    else:
+        dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() == 0
+    o_ref, lse_ref, tr_ref = oracle.run_workload(wl, row_select=sel, want_trace=trace)
+    check_close(dw.o, dw.lse, o_ref, lse_ref, sel)
+    if trace:
+        t = tr.cpu().numpy()
+        if sel is not None:
+            assert np.array_equal(t[sel.astype(bool)], tr_ref[sel.astype(bool)])
+        else:
+            assert np.array_equal(t, tr_ref)
+    return dw
+
+
+# --------------------------------------------------------------------------- #
+# Small shapes that the oracle finishes in seconds (several splits, ragged tails)
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_tiny(variant):
+    run_and_check(W.tiny(0), variant)
+
+
+SHAPES = [
+    # ctx list, W list, Hq, Hkv, d, mask
+    ([300], [1], 8, 8, 64, 0),
+    ([517, 16], [16, 3], 24, 4, 256, 0),
+    ([77, 1000, 0], [8, 9, 5], 24, 4, 256, 0),
+    ([1234, 45, 700], [9, 9, 9], 32, 8, 128, 1),
+    ([150, 63], [12, 16], 16, 1, 64, 1),
+    ([801], [16], 64, 4, 128, 0),          # G = 16, W = 16: 256 rows per KV head
+    ([129, 64, 255], [2, 1, 7], 8, 1, 256, 1),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"s{i}" for i in range(len(SHAPES))])
+def test_random_shapes_bf16(shape, variant):
+    ctx, win, hq, hkv, d, mask = shape
+    wl = W.make_workload("shape", ctx, win, hq, hkv, d, mask, seed=len(ctx) + d, pool_slack=0.2)
+    run_and_check(wl, variant)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", SHAPES[1:5], ids=[f"s{i}" for i in range(1, 5)])
+def test_random_shapes_nvfp4(shape, variant):
+    ctx, win, hq, hkv, d, mask = shape
+    wl = W.make_workload("fp4", ctx, win, hq, hkv, d, mask, kv_dtype=W.KV_NVFP4, seed=3,
+                         pool_slack=0.2)
+    run_and_check(wl, variant)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+def test_split_count_invariance(splits):
+    wl = W.make_workload("splits", [2000, 333], [8, 16], 24, 4, 256, 0, seed=5, pool_slack=0.1)
+    dw = run_and_check(wl, force_splits=splits, trace=True)
+    if splits:
+        assert dw.plan.info["max_splits"] <= splits
+
+
+def test_empty_windows_and_zero_context():
+    wl = W.make_workload("edge", [0, 40, 0, 5], [1, 0, 16, 0], 8, 2, 64, 0, seed=6)
+    run_and_check(wl)
+
+
+def test_plan_without_host_lengths():
+    wl = W.make_workload("nohost", [900, 31], [4, 11], 12, 2, 128, 1, seed=7, pool_slack=0.2)
+    run_and_check(wl, host_lens=False)
+
+
+# --------------------------------------------------------------------------- #
+# Invariants on the GPU
+# --------------------------------------------------------------------------- #
+def test_page_permutation_is_bitwise_invariant():
+    wl = W.make_workload("perm", [1500, 200], [16, 8], 24, 4, 256, 0, seed=8, pool_slack=0.3)
+    a = sa.DeviceWorkload(wl, "cuda")
+    a.run()
+    g = torch.Generator().manual_seed(1)
+    perm = torch.randperm(wl.num_pages, generator=g)
+    inv = torch.argsort(perm)
+    bt2 = torch.where(wl.block_table >= 0, perm[wl.block_table.clamp(min=0).long()].to(torch.int32),
+                      wl.block_table)
+    wl2 = W.Workload(**{**wl.__dict__, "k_pool": wl.k_pool[inv], "v_pool": wl.v_pool[inv],
+                        "block_table": bt2})
+    b = sa.DeviceWorkload(wl2, "cuda")
+    assert a.plan.info == b.plan.info
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.o, b.o) and torch.equal(a.lse, b.lse)
+
+
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_NVFP4])
+def test_poisoned_unread_slots_change_nothing(kv):
+    kw = dict(ctx_lens=[700, 41], windows=[9, 4], num_q_heads=24, num_kv_heads=4, head_dim=256,
+              mask_mode=1, kv_dtype=kv, seed=9, pool_slack=0.4)
+    a = sa.DeviceWorkload(W.make_workload("clean", **kw), "cuda")
+    b = sa.DeviceWorkload(W.make_workload("poison", poison_unread=True, **kw), "cuda")
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.o, b.o) and torch.equal(a.lse, b.lse)
+    assert torch.isfinite(b.o.float()).all()
+
+
+def test_causal_row_i_matches_decode_at_ctx_plus_i_plus_1():
+    ctx, Wn = 1000, 12
+    wl = W.make_workload("rowwise", [ctx], Wn, 24, 4, 256, 0, seed=10)
+    full = sa.DeviceWorkload(wl, "cuda")
+    full.run()
+    for i in (0, 5, 11):
+        one = W.Workload(**{**wl.__dict__, "q": wl.q[i:i + 1].clone(),
+                            "seq_lens": torch.tensor([ctx + i + 1], dtype=torch.int32),
+                            "q_indptr": torch.tensor([0, 1], dtype=torch.int32)})
+        d1 = sa.DeviceWorkload(one, "cuda")
+        d1.run()
+        torch.cuda.synchronize()
+        diff = (d1.o[0].float() - full.o[i].float()).abs().max().item()
+        assert diff <= O_MAX
+        assert torch.allclose(d1.lse[0], full.lse[i], rtol=LSE_REL, atol=LSE_REL)
+
+
+def test_non_causal_and_causal_agree_on_last_row():
+    kw = dict(ctx_lens=[333, 1200], windows=[7, 16], num_q_heads=8, num_kv_heads=2, head_dim=128,
+              seed=11)
+    c = sa.DeviceWorkload(W.make_workload("c", mask_mode=0, **kw), "cuda")
+    n = sa.DeviceWorkload(W.make_workload("n", mask_mode=1, **kw), "cuda")
+    c.run()
+    n.run()
+    torch.cuda.synchronize()
+    for last in (6, 22):
+        assert torch.equal(c.o[last], n.o[last]) and torch.equal(c.lse[last], n.lse[last])
+
+
+def test_zero_queries_count_visible_keys_exactly():
+    wl = W.make_workload("q0", [1000, 77], [16, 5], 24, 4, 256, 0, seed=12, q_mode="zero")
+    dw = run_and_check(wl, trace=False)
+    lse = dw.lse.cpu().numpy().astype(np.float64)
+    for r, (c, w) in enumerate(zip([1000, 77], [16, 5])):
+        row0 = int(wl.q_indptr[r])
+        for i in range(w):
+            assert np.all(np.round(np.exp(lse[row0 + i])) == c + i + 1)
+
+
+@pytest.mark.parametrize("kv", [W.KV_BF16])
+def test_constant_values_come_back_bit_exactly(kv):
+    wl = W.make_workload("vconst", [2100, 9], [16, 3], 24, 4, 256, 0, seed=13, v_mode="const")
+    dw = sa.DeviceWorkload(wl, "cuda")
+    dw.run()
+    torch.cuda.synchronize()
+    v = wl.v_pool[int(wl.block_table[0, 0]), :, 0, :]  # [Hkv, d], same for every key
+    want = v.repeat_interleave(6, dim=0)                 # query head h -> KV head h // 6
+    got = dw.o.cpu()
+    for row in range(wl.total_rows):
+        assert torch.equal(got[row], want)
+
+
+# --------------------------------------------------------------------------- #
+# Device-side checks: bad inputs become a status bit, never a fault
+# --------------------------------------------------------------------------- #
+def test_bad_page_id_sets_status_and_keeps_going():
+    wl = W.make_workload("badpage", [200], [4], 8, 2, 128, 0, seed=14)
+    dw = sa.DeviceWorkload(wl, "cuda")
+    dw.block_table[0, 3] = wl.num_pages + 1000
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() & sa.SPEC_ATTN_DEV_BAD_PAGE
+    dw.block_table.copy_(wl.block_table.cuda())
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() == 0
+
+
+def test_seq_len_above_plan_sets_status():
+    wl = W.make_workload("badlen", [200, 50], [4, 4], 8, 2, 128, 0, seed=15, pool_slack=1.0,
+                         bt_stride=40)
+    dw = sa.DeviceWorkload(wl, "cuda")
+    dw.seq_lens[1] = wl.max_seq_len + 100     # above the plan's max_seq_len
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() & sa.SPEC_ATTN_DEV_BAD_SEQ_LEN
+    dw.seq_lens[1] = 2                         # below its window
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() & sa.SPEC_ATTN_DEV_BAD_SEQ_LEN
+
+
+def test_window_wider_than_plan_sets_status():
+    wl = W.make_workload("badw", [100, 100], [4, 4], 8, 2, 128, 0, seed=16)
+    dw = sa.DeviceWorkload(wl, "cuda")
+    dw.q_indptr.copy_(torch.tensor([0, 1, 8], dtype=torch.int32))  # W = 1 and 7 > max_w 4
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() & sa.SPEC_ATTN_DEV_BAD_WINDOW
+
+
+def test_run_rejects_small_workspace_and_misalignment():
+    wl = W.make_workload("ws", [3000], [8], 24, 4, 256, 0, seed=17)
+    dw = sa.DeviceWorkload(wl, "cuda")
+    assert dw.plan.workspace_bytes > 256
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sa.SpecAttnError) as ei:
+        sa.spec_attn_run(dw.plan, dw.q, dw.k_pool, dw.v_pool, dw.block_table, dw.seq_lens,
+                         dw.q_indptr, dw.o, dw.lse, small)
+    assert ei.value.status == sa.SPEC_ATTN_E_WORKSPACE_TOO_SMALL
+    qv = torch.zeros(dw.q.numel() + 8, dtype=torch.bfloat16, device="cuda")[1:1 + dw.q.numel()].view_as(dw.q)
+    with pytest.raises(sa.SpecAttnError) as ei:
+        sa.spec_attn_run(dw.plan, qv, dw.k_pool, dw.v_pool, dw.block_table, dw.seq_lens,
+                         dw.q_indptr, dw.o, dw.lse, dw.workspace)
+    assert ei.value.status == sa.SPEC_ATTN_E_INVALID_ARG
+
+
+# --------------------------------------------------------------------------- #
+# CUDA graph capture and replay
+# --------------------------------------------------------------------------- #
+def test_graph_capture_replay_matches_eager():
+    wl = W.make_workload("graph", [1800, 900, 60], [9, 9, 9], 32, 8, 128, 1, seed=18, pool_slack=0.1)
+    dw = sa.DeviceWorkload(wl, "cuda")
+    dw.run()
+    torch.cuda.synchronize()
+    o_eager = dw.o.clone()
+    dw.o.zero_()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dw.run(stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(dw.o, o_eager)
+    # new lengths (<= the plan's max) and replay again
+    dw.seq_lens.copy_(torch.tensor([1000, 900, 60], dtype=torch.int32))
+    g.replay()
+    torch.cuda.synchronize()
+    wl2 = W.Workload(**{**wl.__dict__, "seq_lens": torch.tensor([1000, 900, 60], dtype=torch.int32)})
+    o_ref, lse_ref, _ = oracle.run_workload(wl2)
+    check_close(dw.o, dw.lse, o_ref, lse_ref)
+
+
+# --------------------------------------------------------------------------- #
+# Full-size workloads in the bench's launch configuration, sampled rows
+# --------------------------------------------------------------------------- #
+def _sample(wl, n_rows=6, seed=0):
+    g = np.random.default_rng(seed)
+    sel = np.zeros((wl.total_rows, wl.num_q_heads), dtype=np.uint8)
+    rows = set()
+    for r in range(wl.num_reqs):  # first and last row of every window
+        a, b = int(wl.q_indptr[r]), int(wl.q_indptr[r + 1])
+        if b > a:
+            rows.update([a, b - 1])
+    rows.update(g.integers(0, wl.total_rows, size=n_rows).tolist())
+    for row in rows:
+        sel[row, g.integers(0, wl.num_q_heads, size=3)] = 1
+        sel[row, 0] = 1
+        sel[row, wl.num_q_heads - 1] = 1
+    return sel
+
+
+FULL = [
+    ("verify_sweep_w1", lambda: W.verify_sweep(1)),
+    ("verify_sweep_w8", lambda: W.verify_sweep(8)),
+    ("verify_sweep_w16", lambda: W.verify_sweep(16)),
+    ("long_verify_w8", lambda: W.long_verify(8)),
+    ("long_verify_w9", lambda: W.long_verify(9)),
+    ("long_verify_w12", lambda: W.long_verify(12)),
+    ("long_verify_w16", lambda: W.long_verify(16)),
+    ("batched_draft", lambda: W.batched_draft()),
+    ("nvfp4", lambda: W.nvfp4()),
+]
+
+
+@pytest.mark.parametrize("name,make", FULL, ids=[n for n, _ in FULL])
+def test_full_size_sampled(name, make):
+    wl = make()
+    run_and_check(wl, trace=True, sel=_sample(wl))
