@@ -1,0 +1,380 @@
+"""Benchmark: verify-attention microseconds per layer call and KV-read GB/s.
+
+One step = one layer call per window width of the 16K verify sweep
+(1 request, ctx 16384, W in {1, 8, 16}, Hq 24, Hkv 4, d 256, causal-in-block,
+bf16, 2048-page shuffled pool), each call cold in L2: a 2 x L2 buffer is
+written before every step, outside the timed events.  GB/s counts the
+algorithmic K/V bytes of one sweep (every cached key, every KV head, K and V
+once) divided by device time, the definition of the page "ChunkedSmallT
+re-streams full KV per query chunk (DFlash K>=8 verify at long context)",
+section "Measurement".
+
+Prints ONE JSON line (rank 0).  Extra keys: per-workload table of the other
+shapes (64K verify W 8/9/12/16, batched non-causal draft, NVFP4), roofline of
+the split-KV kernel, CPU-oracle baseline, end-to-end figure through host
+buffers, clocks sampled during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--quick]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn µs/layer call & KV-read GB/s (% of GB300 HBM peak) vs W and ctx"
+MAIN_WORKLOAD = "verify_sweep: 1 request, ctx 16384, W in {1,8,16}, Hq 24, Hkv 4, d 256, causal-in-block, bf16 KV, page 16, block table = seeded permutation of a 2048-page pool"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="main workload only (no table)")
+    ap.add_argument("--variant", type=int, default=0, help="kernel variant (0 auto, 1 cuda-core, 2 tcgen05)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    return 6800.0, "fallback 6.8 TB/s"
+
+
+# --------------------------------------------------------------------------- #
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# CPU-oracle arm
+# --------------------------------------------------------------------------- #
+def oracle_step_seconds(wls):
+    import oracle
+    t0 = time.perf_counter()
+    for wl in wls:
+        oracle.run_workload(wl, want_trace=False)
+    return time.perf_counter() - t0
+
+
+def main_workloads():
+    from speculative_decode_verify_paged_gb300 import workloads as W
+    return [W.verify_sweep(w) for w in (1, 8, 16)]
+
+
+def table_workloads():
+    from speculative_decode_verify_paged_gb300 import workloads as W
+    return [("long_verify_w8", lambda: W.long_verify(8)), ("long_verify_w9", lambda: W.long_verify(9)),
+            ("long_verify_w12", lambda: W.long_verify(12)), ("long_verify_w16", lambda: W.long_verify(16)),
+            ("batched_draft", W.batched_draft), ("nvfp4", W.nvfp4)]
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle on the host cores, same workload and metric."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wls = main_workloads()
+    kv = sum(w.kv_bytes for w in wls)
+    for _ in range(args.warmup):
+        oracle_step_seconds(wls)
+    times = [oracle_step_seconds(wls) for _ in range(args.steps)]
+    sec = statistics.mean(times)
+    value = kv / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": MAIN_WORKLOAD, "calls_per_step": 3, "kv_bytes_per_step": kv},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "the whole step: the three layer calls W=1,8,16 at ctx 16384, every row and head"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# GPU arm
+# --------------------------------------------------------------------------- #
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decode_verify_paged_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes of the split kernel from the committed ncu summary,
+    if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "split_attn_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d
+
+
+def time_calls(dws, flush, steps, warmup, stream, timing_events=False):
+    """Per-step device time (ms) of one call per DeviceWorkload, L2 flushed before each step."""
+    import torch
+    per_step = []
+    split_ms = [0.0] * len(dws)
+    evs = []
+    for dw in dws:
+        b = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        b.record(stream)
+        e.record(stream)
+        evs.append((b, e))
+        dw.plan.set_timing_events(b, e) if timing_events else dw.plan.set_timing_events(None, None)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    for it in range(warmup + steps):
+        flush.zero_()
+        start.record(stream)
+        for dw in dws:
+            dw.run(stream)
+        end.record(stream)
+        if it >= warmup:
+            end.synchronize()
+            per_step.append(start.elapsed_time(end))
+            if timing_events:
+                for k, (b, e) in enumerate(evs):
+                    split_ms[k] += b.elapsed_time(e)
+    for dw in dws:
+        dw.plan.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    return per_step, [s / steps for s in split_ms]
+
+
+def e2e_step(dws, host, stream):
+    """One step through host buffers: H2D copy of every input, the calls, D2H of O and LSE."""
+    for dw, h in zip(dws, host):
+        for name in ("q", "k_pool", "v_pool", "block_table", "seq_lens", "q_indptr"):
+            getattr(dw, name).copy_(h[name], non_blocking=True)
+        dw.run(stream)
+        h["o"].copy_(dw.o, non_blocking=True)
+        h["lse"].copy_(dw.lse, non_blocking=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import speculative_decode_verify_paged_gb300 as sa
+    from speculative_decode_verify_paged_gb300 import build as libbuild
+
+    libbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    peak, peak_src = measured_peaks()
+
+    wls = main_workloads()
+    dws = [sa.DeviceWorkload(wl, dev, kernel_variant=args.variant) for wl in wls]
+    kv_bytes = [wl.kv_bytes for wl in wls]
+    launches_per_step = sum(1 + dw.plan.info["uses_merge"] for dw in dws)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        per_step, _ = time_calls(dws, flush, args.steps, args.warmup, stream)
+        torch.cuda.synchronize()
+    step_ms = statistics.mean(per_step)
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+        torch.distributed.barrier()
+    value = world * sum(kv_bytes) / (step_ms * 1e-3) / 1e9
+
+    # per-call medians and the split kernel alone (timing events around its launch)
+    per_call = []
+    for dw, wl in zip(dws, wls):
+        ts, _ = time_calls([dw], flush, max(10, args.steps), 3, stream)
+        _, sk = time_calls([dw], flush, max(10, args.steps), 3, stream, timing_events=True)
+        us = statistics.median(ts) * 1e3
+        per_call.append({"workload": wl.name, "w": wl.max_w, "us": round(us, 2),
+                         "gbs": round(wl.kv_bytes / (us * 1e-6) / 1e9, 1),
+                         "pct_peak": round(100 * wl.kv_bytes / (us * 1e-6) / 1e9 / peak, 1),
+                         "split_kernel_us": round(sk[0] * 1e3, 2), "plan": dw.plan.info})
+    split_us_total = sum(c["split_kernel_us"] for c in per_call)
+    achieved = sum(kv_bytes) / (split_us_total * 1e-6) / 1e9
+    tr = committed_traffic()
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": (tr["dram_bytes_per_launch"] if tr else None),
+                "kernel": "split_attn (split-KV attention over the paged cache)",
+                "peak_source": peak_src + ", of measured",
+                "algorithmic_bytes_per_launch": {c["workload"]: wl.kv_bytes for c, wl in zip(per_call, wls)}}
+
+    table = []
+    if not args.quick:
+        for name, make in table_workloads():
+            wl = make()
+            dw = sa.DeviceWorkload(wl, dev, kernel_variant=args.variant)
+            ts, _ = time_calls([dw], flush, max(10, args.steps), 3, stream)
+            us = statistics.median(ts) * 1e3
+            gbs = wl.kv_bytes / (us * 1e-6) / 1e9
+            table.append({"workload": name, "us": round(us, 2), "gbs": round(gbs, 1),
+                          "pct_peak": round(100 * gbs / peak, 1), "kv_bytes": wl.kv_bytes,
+                          "splits": dw.plan.info["max_splits"], "variant": dw.plan.info["kernel_variant"]})
+            del dw
+            torch.cuda.empty_cache()
+        lv = {t["workload"]: t["us"] for t in table}
+        if "long_verify_w8" in lv and "long_verify_w16" in lv:
+            table.append({"ratio_w16_over_w8_ctx64k": round(lv["long_verify_w16"] / lv["long_verify_w8"], 3)})
+
+    # end to end through host buffers (pinned), same step
+    host = []
+    h2d = d2h = 0
+    for dw in dws:
+        h = {n: getattr(dw, n).cpu().pin_memory() for n in ("q", "k_pool", "v_pool", "block_table",
+                                                            "seq_lens", "q_indptr")}
+        h["o"] = torch.empty_like(dw.o, device="cpu").pin_memory()
+        h["lse"] = torch.empty_like(dw.lse, device="cpu").pin_memory()
+        h2d += sum(h[n].numel() * h[n].element_size() for n in ("q", "k_pool", "v_pool", "block_table",
+                                                                "seq_lens", "q_indptr"))
+        d2h += h["o"].numel() * 2 + h["lse"].numel() * 4
+        host.append(h)
+    e2e_times = []
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    for it in range(3 + max(5, args.steps // 3)):
+        flush.zero_()
+        s0.record(stream)
+        e2e_step(dws, host, stream)
+        s1.record(stream)
+        s1.synchronize()
+        if it >= 3:
+            e2e_times.append(s0.elapsed_time(s1))
+    e2e_ms = statistics.mean(e2e_times)
+    e2e = {"value": round(world * sum(kv_bytes) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        oracle_step_seconds(wls[:1])
+        sec = oracle_step_seconds(wls)
+        cpu = {"value": round(sum(kv_bytes) / sec / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "seconds_per_step": round(sec, 3),
+               "sample": "one whole step (the three layer calls W=1,8,16 at ctx 16384, every row and head)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1), bf16)",
+            "config": {"workload": MAIN_WORKLOAD, "calls_per_step": len(dws),
+                       "kv_bytes_per_step": sum(kv_bytes), "l2": "flushed before every step (2 x L2 write, untimed)",
+                       "us_per_call": {c["workload"]: c["us"] for c in per_call},
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_peak": round(100 * value / world / peak, 1),
+            "per_call": per_call,
+            "table": table,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -277,6 +277,12 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
             for (int j = 0; j < 16; ++j) {
                 float vx[DPL];
                 load_row_slice<D, KV>(st + Stage::kHalf, j, lane, vx);
+                // Slots past seq_len hold stale data (possibly non-finite);
+                // their weight is 0, but 0 * NaN is NaN, so drop the values.
+                if (kbase + j >= key_hi) {
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) vx[e] = 0.f;
+                }
 #pragma unroll
                 for (int t = 0; t < RPW; ++t) {
                     const float w = __shfl_sync(kFullMask, pj[t], 2 * j);
