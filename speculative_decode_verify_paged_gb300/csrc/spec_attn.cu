@@ -192,18 +192,29 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
 
     const int G = p.num_q_heads / p.num_kv_heads;
     const int max_rows = p.max_w * G;
-    // Only the CUDA-core variant exists in this build; AUTO resolves to it.
-    if (p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05) {
+    const bool tc_ok = tc_supported(p.head_dim, p.kv_dtype, max_rows);
+    if (p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05 && !tc_ok) {
         delete plan;
         return SPEC_ATTN_E_UNSUPPORTED;
     }
-    plan->variant = SPEC_ATTN_VARIANT_CUDA_CORE;
-    plan->cc = cc_config(p.head_dim, p.kv_dtype, max_rows);
-    plan->rows_per_cta = 8 * plan->cc.rows_per_warp;
-    plan->row_groups = (max_rows + plan->rows_per_cta - 1) / plan->rows_per_cta;
-    plan->threads = plan->cc.threads;
-    plan->smem = plan->cc.smem_bytes;
-    e = cc_prepare(p.head_dim, p.kv_dtype, plan->cc);
+    // AUTO keeps the CUDA-core kernel until the tensor-core kernel is qualified.
+    const bool use_tc = p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05;
+    if (use_tc) {
+        plan->variant = SPEC_ATTN_VARIANT_TCGEN05;
+        plan->rows_per_cta = 128;
+        plan->row_groups = 1;
+        plan->threads = tc_threads();
+        plan->smem = tc_smem_bytes(p.head_dim);
+        e = tc_prepare(p.head_dim);
+    } else {
+        plan->variant = SPEC_ATTN_VARIANT_CUDA_CORE;
+        plan->cc = cc_config(p.head_dim, p.kv_dtype, max_rows);
+        plan->rows_per_cta = 8 * plan->cc.rows_per_warp;
+        plan->row_groups = (max_rows + plan->rows_per_cta - 1) / plan->rows_per_cta;
+        plan->threads = plan->cc.threads;
+        plan->smem = plan->cc.smem_bytes;
+        e = cc_prepare(p.head_dim, p.kv_dtype, plan->cc);
+    }
     if (e != cudaSuccess) {
         delete plan;
         return cuda_fail(e);
@@ -229,7 +240,12 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         occ = std::max(1, std::min(max_smem / std::max(1, plan->smem + 1024), 2048 / plan->threads));
     }
     CostModel cm;
-    {
+    if (use_tc) {
+        // tensor cores keep up with HBM: a CTA streams its keys at roughly
+        // its SM's share of HBM bandwidth (one CTA per SM).
+        occ = 1;
+        cm.key_us = 2.0 * bkh / (6.5e6 / plan->num_sms);
+    } else {
         // CUDA cores: ~2 FMA per element per row (QK and PV) at ~128 FMA/clk/SM,
         // ~1.9 GHz, shared by `occ` CTAs, times an instruction-overhead factor.
         const double fma_per_us = 128.0 * 1.9e3 / occ;
@@ -369,7 +385,10 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         e = cudaEventRecord(plan->ev_begin, stream);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    e = cc_launch(sp, p.kv_dtype, plan->cc, trace != nullptr, plan->grid, stream);
+    if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05)
+        e = tc_launch(sp, trace != nullptr, plan->grid, stream);
+    else
+        e = cc_launch(sp, p.kv_dtype, plan->cc, trace != nullptr, plan->grid, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (plan->ev_end) {
         e = cudaEventRecord(plan->ev_end, stream);

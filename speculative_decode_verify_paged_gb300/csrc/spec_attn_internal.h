@@ -81,6 +81,13 @@ cudaError_t cc_prepare(int head_dim, int kv_dtype, const CcConfig& cfg);
 cudaError_t cc_launch(const SplitParams& p, int kv_dtype, const CcConfig& cfg, bool traced,
                       dim3 grid, cudaStream_t stream);
 
+// ---- tcgen05 split-KV kernel (split_attn_tc.cu) ----
+bool tc_supported(int head_dim, int kv_dtype, int max_rows);
+int tc_smem_bytes(int head_dim);
+int tc_threads();
+cudaError_t tc_prepare(int head_dim);
+cudaError_t tc_launch(const SplitParams& p, bool traced, dim3 grid, cudaStream_t stream);
+
 // ---- LSE merge (merge_lse.cu) ----
 cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic);
 

@@ -18,7 +18,7 @@ from speculative_decode_verify_paged_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 O_MAX, O_MEAN, LSE_REL = 1e-2, 1e-3, 1e-4
-VARIANTS = [sa.SPEC_ATTN_VARIANT_AUTO, sa.SPEC_ATTN_VARIANT_CUDA_CORE]
+VARIANTS = [sa.SPEC_ATTN_VARIANT_AUTO, sa.SPEC_ATTN_VARIANT_CUDA_CORE, sa.SPEC_ATTN_VARIANT_TCGEN05]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,9 +44,17 @@ def check_close(o_gpu, lse_gpu, o_ref, lse_ref, sel=None):
     return err.max(), rel.max()
 
 
+def make_dw(wl, variant=0, **kw):
+    try:
+        return sa.DeviceWorkload(wl, "cuda", kernel_variant=variant, **kw)
+    except sa.SpecAttnError as e:
+        if e.status == sa.SPEC_ATTN_E_UNSUPPORTED and variant != sa.SPEC_ATTN_VARIANT_AUTO:
+            pytest.skip("variant does not support this shape")
+        raise
+
+
 def run_and_check(wl, variant=0, force_splits=0, trace=True, sel=None, host_lens=True):
-    dw = sa.DeviceWorkload(wl, "cuda", force_splits=force_splits, kernel_variant=variant,
-                           host_lens=host_lens)
+    dw = make_dw(wl, variant, force_splits=force_splits, host_lens=host_lens)
     if trace:
         tr = torch.zeros(wl.total_rows, wl.num_q_heads, 2, dtype=torch.int64, device="cuda")
         dw.run_traced(tr)
@@ -102,30 +110,34 @@ def test_random_shapes_nvfp4(shape, variant):
     run_and_check(wl, variant)
 
 
+@pytest.mark.parametrize("variant", VARIANTS[1:])
 @pytest.mark.parametrize("splits", [1, 2, 7, 0])
-def test_split_count_invariance(splits):
+def test_split_count_invariance(splits, variant):
     wl = W.make_workload("splits", [2000, 333], [8, 16], 24, 4, 256, 0, seed=5, pool_slack=0.1)
-    dw = run_and_check(wl, force_splits=splits, trace=True)
+    dw = run_and_check(wl, variant, force_splits=splits, trace=True)
     if splits:
         assert dw.plan.info["max_splits"] <= splits
 
 
-def test_empty_windows_and_zero_context():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_empty_windows_and_zero_context(variant):
     wl = W.make_workload("edge", [0, 40, 0, 5], [1, 0, 16, 0], 8, 2, 64, 0, seed=6)
-    run_and_check(wl)
+    run_and_check(wl, variant)
 
 
-def test_plan_without_host_lengths():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_plan_without_host_lengths(variant):
     wl = W.make_workload("nohost", [900, 31], [4, 11], 12, 2, 128, 1, seed=7, pool_slack=0.2)
-    run_and_check(wl, host_lens=False)
+    run_and_check(wl, variant, host_lens=False)
 
 
 # --------------------------------------------------------------------------- #
 # Invariants on the GPU
 # --------------------------------------------------------------------------- #
-def test_page_permutation_is_bitwise_invariant():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_page_permutation_is_bitwise_invariant(variant):
     wl = W.make_workload("perm", [1500, 200], [16, 8], 24, 4, 256, 0, seed=8, pool_slack=0.3)
-    a = sa.DeviceWorkload(wl, "cuda")
+    a = make_dw(wl, variant)
     a.run()
     g = torch.Generator().manual_seed(1)
     perm = torch.randperm(wl.num_pages, generator=g)
@@ -134,19 +146,20 @@ def test_page_permutation_is_bitwise_invariant():
                       wl.block_table)
     wl2 = W.Workload(**{**wl.__dict__, "k_pool": wl.k_pool[inv], "v_pool": wl.v_pool[inv],
                         "block_table": bt2})
-    b = sa.DeviceWorkload(wl2, "cuda")
+    b = make_dw(wl2, variant)
     assert a.plan.info == b.plan.info
     b.run()
     torch.cuda.synchronize()
     assert torch.equal(a.o, b.o) and torch.equal(a.lse, b.lse)
 
 
+@pytest.mark.parametrize("variant", VARIANTS[1:])
 @pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_NVFP4])
-def test_poisoned_unread_slots_change_nothing(kv):
+def test_poisoned_unread_slots_change_nothing(kv, variant):
     kw = dict(ctx_lens=[700, 41], windows=[9, 4], num_q_heads=24, num_kv_heads=4, head_dim=256,
               mask_mode=1, kv_dtype=kv, seed=9, pool_slack=0.4)
-    a = sa.DeviceWorkload(W.make_workload("clean", **kw), "cuda")
-    b = sa.DeviceWorkload(W.make_workload("poison", poison_unread=True, **kw), "cuda")
+    a = make_dw(W.make_workload("clean", **kw), variant)
+    b = make_dw(W.make_workload("poison", poison_unread=True, **kw), variant)
     a.run()
     b.run()
     torch.cuda.synchronize()
@@ -154,16 +167,17 @@ def test_poisoned_unread_slots_change_nothing(kv):
     assert torch.isfinite(b.o.float()).all()
 
 
-def test_causal_row_i_matches_decode_at_ctx_plus_i_plus_1():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_causal_row_i_matches_decode_at_ctx_plus_i_plus_1(variant):
     ctx, Wn = 1000, 12
     wl = W.make_workload("rowwise", [ctx], Wn, 24, 4, 256, 0, seed=10)
-    full = sa.DeviceWorkload(wl, "cuda")
+    full = make_dw(wl, variant)
     full.run()
     for i in (0, 5, 11):
         one = W.Workload(**{**wl.__dict__, "q": wl.q[i:i + 1].clone(),
                             "seq_lens": torch.tensor([ctx + i + 1], dtype=torch.int32),
                             "q_indptr": torch.tensor([0, 1], dtype=torch.int32)})
-        d1 = sa.DeviceWorkload(one, "cuda")
+        d1 = make_dw(one, variant)
         d1.run()
         torch.cuda.synchronize()
         diff = (d1.o[0].float() - full.o[i].float()).abs().max().item()
@@ -171,11 +185,12 @@ def test_causal_row_i_matches_decode_at_ctx_plus_i_plus_1():
         assert torch.allclose(d1.lse[0], full.lse[i], rtol=LSE_REL, atol=LSE_REL)
 
 
-def test_non_causal_and_causal_agree_on_last_row():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_non_causal_and_causal_agree_on_last_row(variant):
     kw = dict(ctx_lens=[333, 1200], windows=[7, 16], num_q_heads=8, num_kv_heads=2, head_dim=128,
               seed=11)
-    c = sa.DeviceWorkload(W.make_workload("c", mask_mode=0, **kw), "cuda")
-    n = sa.DeviceWorkload(W.make_workload("n", mask_mode=1, **kw), "cuda")
+    c = make_dw(W.make_workload("c", mask_mode=0, **kw), variant)
+    n = make_dw(W.make_workload("n", mask_mode=1, **kw), variant)
     c.run()
     n.run()
     torch.cuda.synchronize()
@@ -183,9 +198,10 @@ def test_non_causal_and_causal_agree_on_last_row():
         assert torch.equal(c.o[last], n.o[last]) and torch.equal(c.lse[last], n.lse[last])
 
 
-def test_zero_queries_count_visible_keys_exactly():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_zero_queries_count_visible_keys_exactly(variant):
     wl = W.make_workload("q0", [1000, 77], [16, 5], 24, 4, 256, 0, seed=12, q_mode="zero")
-    dw = run_and_check(wl, trace=False)
+    dw = run_and_check(wl, variant, trace=False)
     lse = dw.lse.cpu().numpy().astype(np.float64)
     for r, (c, w) in enumerate(zip([1000, 77], [16, 5])):
         row0 = int(wl.q_indptr[r])
@@ -194,9 +210,10 @@ def test_zero_queries_count_visible_keys_exactly():
 
 
 @pytest.mark.parametrize("kv", [W.KV_BF16])
-def test_constant_values_come_back_bit_exactly(kv):
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_constant_values_come_back_bit_exactly(kv, variant):
     wl = W.make_workload("vconst", [2100, 9], [16, 3], 24, 4, 256, 0, seed=13, v_mode="const")
-    dw = sa.DeviceWorkload(wl, "cuda")
+    dw = make_dw(wl, variant)
     dw.run()
     torch.cuda.synchronize()
     v = wl.v_pool[int(wl.block_table[0, 0]), :, 0, :]  # [Hkv, d], same for every key
@@ -209,9 +226,10 @@ def test_constant_values_come_back_bit_exactly(kv):
 # --------------------------------------------------------------------------- #
 # Device-side checks: bad inputs become a status bit, never a fault
 # --------------------------------------------------------------------------- #
-def test_bad_page_id_sets_status_and_keeps_going():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_bad_page_id_sets_status_and_keeps_going(variant):
     wl = W.make_workload("badpage", [200], [4], 8, 2, 128, 0, seed=14)
-    dw = sa.DeviceWorkload(wl, "cuda")
+    dw = make_dw(wl, variant)
     dw.block_table[0, 3] = wl.num_pages + 1000
     dw.run()
     torch.cuda.synchronize()
@@ -222,10 +240,11 @@ def test_bad_page_id_sets_status_and_keeps_going():
     assert dw.device_status() == 0
 
 
-def test_seq_len_above_plan_sets_status():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_seq_len_above_plan_sets_status(variant):
     wl = W.make_workload("badlen", [200, 50], [4, 4], 8, 2, 128, 0, seed=15, pool_slack=1.0,
                          bt_stride=40)
-    dw = sa.DeviceWorkload(wl, "cuda")
+    dw = make_dw(wl, variant)
     dw.seq_lens[1] = wl.max_seq_len + 100     # above the plan's max_seq_len
     dw.run()
     torch.cuda.synchronize()
@@ -236,9 +255,10 @@ def test_seq_len_above_plan_sets_status():
     assert dw.device_status() & sa.SPEC_ATTN_DEV_BAD_SEQ_LEN
 
 
-def test_window_wider_than_plan_sets_status():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_window_wider_than_plan_sets_status(variant):
     wl = W.make_workload("badw", [100, 100], [4, 4], 8, 2, 128, 0, seed=16)
-    dw = sa.DeviceWorkload(wl, "cuda")
+    dw = make_dw(wl, variant)
     dw.q_indptr.copy_(torch.tensor([0, 1, 8], dtype=torch.int32))  # W = 1 and 7 > max_w 4
     dw.run()
     torch.cuda.synchronize()
@@ -247,7 +267,7 @@ def test_window_wider_than_plan_sets_status():
 
 def test_run_rejects_small_workspace_and_misalignment():
     wl = W.make_workload("ws", [3000], [8], 24, 4, 256, 0, seed=17)
-    dw = sa.DeviceWorkload(wl, "cuda")
+    dw = make_dw(wl, variant)
     assert dw.plan.workspace_bytes > 256
     small = torch.zeros(256, dtype=torch.uint8, device="cuda")
     with pytest.raises(sa.SpecAttnError) as ei:
@@ -264,9 +284,10 @@ def test_run_rejects_small_workspace_and_misalignment():
 # --------------------------------------------------------------------------- #
 # CUDA graph capture and replay
 # --------------------------------------------------------------------------- #
-def test_graph_capture_replay_matches_eager():
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_graph_capture_replay_matches_eager(variant):
     wl = W.make_workload("graph", [1800, 900, 60], [9, 9, 9], 32, 8, 128, 1, seed=18, pool_slack=0.1)
-    dw = sa.DeviceWorkload(wl, "cuda")
+    dw = make_dw(wl, variant)
     dw.run()
     torch.cuda.synchronize()
     o_eager = dw.o.clone()
@@ -319,7 +340,8 @@ FULL = [
 ]
 
 
+@pytest.mark.parametrize("variant", VARIANTS[1:])
 @pytest.mark.parametrize("name,make", FULL, ids=[n for n, _ in FULL])
-def test_full_size_sampled(name, make):
+def test_full_size_sampled(name, make, variant):
     wl = make()
-    run_and_check(wl, trace=True, sel=_sample(wl))
+    run_and_check(wl, variant, trace=True, sel=_sample(wl))
