@@ -230,6 +230,31 @@ int spec_attn_last_cuda_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int spec_attn_version(void);
 
+/*
+ * spec_attn_run without a workspace argument, for callers that cannot
+ * allocate device memory (code running where cudaMalloc is not allowed, such
+ * as inside an allocator hook or a host callback, or a plugin handed only its
+ * input and output buffers).  No counterpart on the pages this library
+ * restates: it is a convenience of this library.
+ *
+ * Scratch comes from one array of SPEC_ATTN_NOALLOC_SCRATCH_BYTES (32 MiB) in
+ * the library's own device memory; every GPU that loads the library holds it
+ * until the process exits.  A plan whose workspace_bytes exceeds that size is
+ * rejected with SPEC_ATTN_E_WORKSPACE_TOO_SMALL.  Every call on a device
+ * shares the array, so calls that may overlap on the GPU race and must be
+ * serialised by the caller; each call clears the device-status word at the
+ * head of the array and does not report device-side checks.  The first call
+ * on each device looks up the array's device address (with that device
+ * current) and caches it; make that first call before any stream capture.
+ * Allocates nothing; other arguments and errors as spec_attn_run.
+ */
+#define SPEC_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int spec_attn_run_noalloc(const spec_attn_plan* plan, const void* q, const void* k_pool,
+                          const void* v_pool, const void* k_scales, const void* v_scales,
+                          float k_gscale, float v_gscale, const int32_t* block_table,
+                          const int32_t* seq_lens, const int32_t* q_indptr, void* o, float* lse,
+                          spec_attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

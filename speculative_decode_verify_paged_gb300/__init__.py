@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "spec_attn_run", "spec_attn_run_traced", "spec_attn_plan_set_timing_events",
     "spec_attn_reset_device_status", "spec_attn_check_device_status",
     "spec_attn_status_string", "spec_attn_last_cuda_error", "spec_attn_version",
+    "spec_attn_run_noalloc",
 )
 
 
@@ -121,6 +122,8 @@ def load_library(path: Optional[str] = None):
         lib.spec_attn_last_cuda_error.argtypes = []
         lib.spec_attn_version.restype = i32
         lib.spec_attn_version.argtypes = []
+        lib.spec_attn_run_noalloc.restype = i32
+        lib.spec_attn_run_noalloc.argtypes = run_args + [vp]
         if path is None:
             _lib = lib
         return lib
@@ -249,6 +252,17 @@ def spec_attn_run_traced(plan: Plan, q, k_pool, v_pool, block_table, seq_lens, q
     _check(lib.spec_attn_run_traced(*args, _dptr(trace, "trace", torch.int64), _dptr(workspace, "workspace"),
                                     ctypes.c_size_t(ws_bytes), _stream_handle(stream)),
            "spec_attn_run_traced")
+
+
+def spec_attn_run_noalloc(plan: Plan, q, k_pool, v_pool, block_table, seq_lens, q_indptr, o, lse,
+                          k_scales=None, v_scales=None, k_gscale=1.0, v_gscale=1.0, stream=None):
+    """spec_attn_run for callers that cannot allocate device memory: the
+    library's built-in scratch array stands in for the workspace (calls that
+    may overlap on the GPU must be serialised by the caller)."""
+    lib = load_library()
+    args = _run_args(plan, q, k_pool, v_pool, block_table, seq_lens, q_indptr, o, lse, k_scales,
+                     v_scales, k_gscale, v_gscale)
+    _check(lib.spec_attn_run_noalloc(*args, _stream_handle(stream)), "spec_attn_run_noalloc")
 
 
 def spec_attn_reset_device_status(workspace, stream=None):

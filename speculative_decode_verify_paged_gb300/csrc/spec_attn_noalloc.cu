@@ -1,0 +1,73 @@
+// spec_attn_run_noalloc: the same attention call as spec_attn_run, for
+// callers that cannot allocate device memory.
+//
+// spec_attn_run needs a caller-provided workspace for the split-KV partials
+// (and the device-status word).  Some callers have no way to provide one:
+// code that runs where cudaMalloc is off limits (inside a host callback or
+// a custom allocator's own hook, under a memory pool that is already full or
+// locked by a framework, or in a plugin that is handed only its input and
+// output buffers).  For them this entry point takes its scratch from a
+// fixed-size array that lives in the library's own device memory.
+//
+// The array is a file-scope __device__ variable: every GPU that loads the
+// library holds its 32 MiB until the process exits, and every call on a
+// device shares the same array.  Calls that may overlap on the GPU (two
+// streams, or two host threads) race on it and must be serialised by the
+// caller.  The array keeps whatever the last call left; the only part that
+// must start at zero (the device-status word) is cleared by every call.
+// Plans that need more scratch than the array holds are rejected with
+// SPEC_ATTN_E_WORKSPACE_TOO_SMALL.
+//
+// Host code can not use the array's name as a device address, so the first
+// call on each device looks the address up (cudaGetSymbolAddress, with that
+// device current) and caches it; make that first call before any stream
+// capture begins.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/spec_attn.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = SPEC_ATTN_NOALLOC_SCRATCH_BYTES;  // 32 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" int spec_attn_run_noalloc(const spec_attn_plan* plan, const void* q, const void* k_pool,
+                                     const void* v_pool, const void* k_scales, const void* v_scales,
+                                     float k_gscale, float v_gscale, const int32_t* block_table,
+                                     const int32_t* seq_lens, const int32_t* q_indptr, void* o,
+                                     float* lse, spec_attn_stream_t stream) {
+    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    spec_attn_plan_info info;
+    int st = spec_attn_plan_get_info(plan, &info);
+    if (st != SPEC_ATTN_OK) return st;
+    if (info.workspace_bytes > kNoAllocScratchBytes) return SPEC_ATTN_E_WORKSPACE_TOO_SMALL;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ATTN_E_CUDA;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        if (!g_scratch_addr[dev]) {
+            void* ptr = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess || !ptr) return SPEC_ATTN_E_CUDA;
+            g_scratch_addr[dev] = ptr;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    // the device-status word at the head of the scratch must start at zero
+    st = spec_attn_reset_device_status(scratch, stream);
+    if (st != SPEC_ATTN_OK) return st;
+    return spec_attn_run(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
+                         seq_lens, q_indptr, o, lse, scratch, kNoAllocScratchBytes, stream);
+}
