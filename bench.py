@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--quick", action="store_true", help="main workload only (no table)")
     ap.add_argument("--variant", type=int, default=0, help="kernel variant (0 auto, 1 cuda-core, 2 tcgen05)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="profiling mode: run this named workload (see workloads.NAMED) --calls times, untimed")
+    ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args()
 
 
@@ -285,7 +288,12 @@ def run_ours(args, rank, world, local_rank):
     if not args.quick:
         for name, make in table_workloads():
             wl = make()
-            dw = sa.DeviceWorkload(wl, dev, kernel_variant=args.variant)
+            try:
+                dw = sa.DeviceWorkload(wl, dev, kernel_variant=args.variant)
+            except sa.SpecAttnError as e:  # forced variant not available for this shape
+                if e.status != sa.SPEC_ATTN_E_UNSUPPORTED:
+                    raise
+                dw = sa.DeviceWorkload(wl, dev, kernel_variant=sa.SPEC_ATTN_VARIANT_AUTO)
             ts, _ = time_calls([dw], flush, max(10, args.steps), 3, stream)
             us = statistics.median(ts) * 1e3
             gbs = wl.kv_bytes / (us * 1e-6) / 1e9
@@ -357,8 +365,29 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def run_only(args):
+    """Profiling driver: plan once, then `--calls` layer calls of one named workload."""
+    import torch
+    import speculative_decode_verify_paged_gb300 as sa
+    from speculative_decode_verify_paged_gb300 import build as libbuild
+    from speculative_decode_verify_paged_gb300 import workloads as W
+
+    libbuild.build()
+    wl = W.NAMED[args.only]()
+    dw = sa.DeviceWorkload(wl, "cuda", kernel_variant=args.variant)
+    for _ in range(args.calls):
+        dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() == 0
+    print(json.dumps({"workload": args.only, "calls": args.calls, "kv_bytes": wl.kv_bytes,
+                      "plan": dw.plan.info}))
+
+
 def main():
     args = parse()
+    if args.only:
+        run_only(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

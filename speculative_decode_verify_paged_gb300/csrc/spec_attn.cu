@@ -197,8 +197,9 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         delete plan;
         return SPEC_ATTN_E_UNSUPPORTED;
     }
-    // AUTO keeps the CUDA-core kernel until the tensor-core kernel is qualified.
-    const bool use_tc = p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05;
+    // AUTO takes the tensor-core kernel wherever it applies (W x G <= 128, bf16 KV).
+    const bool use_tc = p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05 ||
+                        (p.kernel_variant == SPEC_ATTN_VARIANT_AUTO && tc_ok);
     if (use_tc) {
         plan->variant = SPEC_ATTN_VARIANT_TCGEN05;
         plan->rows_per_cta = 128;

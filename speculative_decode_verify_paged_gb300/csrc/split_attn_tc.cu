@@ -318,7 +318,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     const float p0 = (c <= lim) ? fast_exp2(sv[c] - ref) : 0.f;
                     const float p1 = (c + 1 <= lim) ? fast_exp2(sv[c + 1] - ref) : 0.f;
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    psum += __low2float(h2) + __high2float(h2);
+                    // the normaliser sums the fp32 weights: rounding P to bf16 for
+                    // the PV MMA must not leak into l (and so into LSE) on rows
+                    // that see only a few keys
+                    psum += p0 + p1;
                     pk[c >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 l_sum = l_sum * alpha + psum;

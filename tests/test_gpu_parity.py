@@ -267,7 +267,7 @@ def test_window_wider_than_plan_sets_status(variant):
 
 def test_run_rejects_small_workspace_and_misalignment():
     wl = W.make_workload("ws", [3000], [8], 24, 4, 256, 0, seed=17)
-    dw = make_dw(wl, variant)
+    dw = make_dw(wl, 0)
     assert dw.plan.workspace_bytes > 256
     small = torch.zeros(256, dtype=torch.uint8, device="cuda")
     with pytest.raises(sa.SpecAttnError) as ei:
