@@ -51,8 +51,28 @@ __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(const MergePar
     // Wait for the split kernel's partials (no-op without a programmatic edge).
     pdl_wait_primary();
 
+    // max and sum of the split weights: every thread reads a strided subset of
+    // the split LSEs (independent loads), then a block reduction
+    __shared__ float red[kMergeThreads / 32];
     float mx = -INFINITY;
-    for (int s = 0; s < n; ++s) mx = fmaxf(mx, p.ws_lse[s * split_stride + oi]);
+    for (int s = tid; s < n; s += kMergeThreads) mx = fmaxf(mx, p.ws_lse[s * split_stride + oi]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
+    if ((tid & 31) == 0) red[tid >> 5] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int k = 1; k < kMergeThreads / 32; ++k) mx = fmaxf(mx, red[k]);
+    __syncthreads();
+    float wl = 0.f;
+    for (int s = tid; s < n; s += kMergeThreads) {
+        const float ls = p.ws_lse[s * split_stride + oi];
+        wl += (ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFullMask, wl, off);
+    if ((tid & 31) == 0) red[tid >> 5] = wl;
+
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
     for (int s = g; s < n; s += SG) {
@@ -68,10 +88,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(const MergePar
     __syncthreads();
     if (g != 0) return;
     float wsum = 0.f;
-    for (int s = 0; s < n; ++s) {
-        const float ls = p.ws_lse[s * split_stride + oi];
-        wsum += (ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
-    }
+#pragma unroll
+    for (int k = 0; k < kMergeThreads / 32; ++k) wsum += red[k];
 #pragma unroll
     for (int k = 1; k < SG; ++k) {
         acc.x += part[k][v].x;
