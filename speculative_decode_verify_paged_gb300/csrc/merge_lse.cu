@@ -10,12 +10,14 @@
 // written as bf16 O (round to nearest even) and natural-log LSE (lse * ln 2).
 //
 // One CTA per (window row, query head).  Its 256 threads are split into
-// split groups x head_dim vectors: thread (g, v) accumulates float4 v of the
-// partials of splits g, g + SG, g + 2 SG, ... (many independent 16-byte loads
-// in flight per thread), then the groups are summed in shared memory.
-// Requests with a single split were finished by the split kernel and are
-// skipped here.  The kernel may be launched as a programmatic dependent of
-// the split kernel: it waits on griddepcontrol before touching partials.
+// split groups x head_dim vectors: thread (g, v) owns float4 v of the splits
+// g, g + SG, g + 2 SG, ...  It issues the loads of up to kBatch of its splits
+// (LSE and partial row) at once -- one memory round trip for the usual split
+// counts -- and folds them with a running maximum (online LSE combination).
+// The groups are then combined once through shared memory.  Requests with a
+// single split were finished by the split kernel and are skipped here.  The
+// kernel may be launched as a programmatic dependent of the split kernel: it
+// waits on griddepcontrol before touching partials.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,12 +27,14 @@ namespace spec_attn {
 namespace {
 
 constexpr int kMergeThreads = 256;
+constexpr int kBatch = 8;
 
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const MergeParams p) {
     constexpr int VEC = D / 4;                 // float4 vectors per row
     constexpr int SG = kMergeThreads / VEC;    // split groups
     __shared__ float4 part[SG][VEC];
+    __shared__ float part_m[SG], part_l[SG];
     const int tid = threadIdx.x;
     const int v = tid % VEC, g = tid / VEC;
     const int pair = blockIdx.x;
@@ -51,55 +55,64 @@ __global__ void __launch_bounds__(kMergeThreads) merge_lse_kernel(const MergePar
     // Wait for the split kernel's partials (no-op without a programmatic edge).
     pdl_wait_primary();
 
-    // max and sum of the split weights: every thread reads a strided subset of
-    // the split LSEs (independent loads), then a block reduction
-    __shared__ float red[kMergeThreads / 32];
-    float mx = -INFINITY;
-    for (int s = tid; s < n; s += kMergeThreads) mx = fmaxf(mx, p.ws_lse[s * split_stride + oi]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
-    if ((tid & 31) == 0) red[tid >> 5] = mx;
-    __syncthreads();
-    mx = red[0];
-#pragma unroll
-    for (int k = 1; k < kMergeThreads / 32; ++k) mx = fmaxf(mx, red[k]);
-    __syncthreads();
-    float wl = 0.f;
-    for (int s = tid; s < n; s += kMergeThreads) {
-        const float ls = p.ws_lse[s * split_stride + oi];
-        wl += (ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFullMask, wl, off);
-    if ((tid & 31) == 0) red[tid >> 5] = wl;
-
+    float m_run = -INFINITY, l_run = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = g; s < n; s += SG) {
-        const float ls = p.ws_lse[s * split_stride + oi];
-        const float w = (ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
-        const float4 o = *reinterpret_cast<const float4*>(p.ws_o + (s * split_stride + oi) * D + v * 4);
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
+    for (int s0 = g; s0 < n; s0 += SG * kBatch) {
+        float ls[kBatch];
+        float4 o[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int s = s0 + k * SG;
+            if (s < n) {
+                ls[k] = p.ws_lse[s * split_stride + oi];
+                o[k] = *reinterpret_cast<const float4*>(p.ws_o + (s * split_stride + oi) * D + v * 4);
+            } else {
+                ls[k] = -INFINITY;
+                o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            if (ls[k] == -INFINITY) continue;
+            if (ls[k] > m_run) {
+                const float a = fast_exp2(m_run - ls[k]);   // 0 when m_run is -inf
+                acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+                l_run *= a;
+                m_run = ls[k];
+            }
+            const float w = fast_exp2(ls[k] - m_run);
+            acc.x = fmaf(w, o[k].x, acc.x);
+            acc.y = fmaf(w, o[k].y, acc.y);
+            acc.z = fmaf(w, o[k].z, acc.z);
+            acc.w = fmaf(w, o[k].w, acc.w);
+            l_run += w;
+        }
     }
     part[g][v] = acc;
+    if (v == 0) {
+        part_m[g] = m_run;
+        part_l[g] = l_run;
+    }
     __syncthreads();
     if (g != 0) return;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < SG; ++k) mx = fmaxf(mx, part_m[k]);
+    float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
 #pragma unroll
-    for (int k = 0; k < kMergeThreads / 32; ++k) wsum += red[k];
-#pragma unroll
-    for (int k = 1; k < SG; ++k) {
-        acc.x += part[k][v].x;
-        acc.y += part[k][v].y;
-        acc.z += part[k][v].z;
-        acc.w += part[k][v].w;
+    for (int k = 0; k < SG; ++k) {
+        if (part_m[k] == -INFINITY) continue;
+        const float a = fast_exp2(part_m[k] - mx);
+        tot.x = fmaf(a, part[k][v].x, tot.x);
+        tot.y = fmaf(a, part[k][v].y, tot.y);
+        tot.z = fmaf(a, part[k][v].z, tot.z);
+        tot.w = fmaf(a, part[k][v].w, tot.w);
+        wsum = fmaf(a, part_l[k], wsum);
     }
     const float inv = 1.f / wsum;
-    const uint32_t lo = float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
-    const uint32_t hi = float_to_bf16_bits(acc.z * inv) | ((uint32_t)float_to_bf16_bits(acc.w * inv) << 16);
+    const uint32_t lo = float_to_bf16_bits(tot.x * inv) | ((uint32_t)float_to_bf16_bits(tot.y * inv) << 16);
+    const uint32_t hi = float_to_bf16_bits(tot.z * inv) | ((uint32_t)float_to_bf16_bits(tot.w * inv) << 16);
     *reinterpret_cast<uint2*>(p.o + oi * D + v * 4) = make_uint2(lo, hi);
     if (p.lse && v == 0) p.lse[oi] = (mx + log2f(wsum)) * kLn2;
 }

@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -43,6 +44,11 @@ struct spec_attn_plan {
     float sm_scale;
     cudaEvent_t ev_begin;
     cudaEvent_t ev_end;
+    // TMA descriptors of the last (Q, K pool, V pool) pointers a run used: a
+    // decode loop re-running a plan on the same buffers encodes them once.
+    std::mutex maps_mutex;
+    TcMaps maps;
+    const void* maps_key[3] = {nullptr, nullptr, nullptr};
 };
 
 namespace {
@@ -382,13 +388,28 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.score_scale_log2 = plan->sm_scale * log2e * (fp4 ? k_gscale : 1.0f);
     sp.out_scale = fp4 ? v_gscale : 1.0f;
 
+    spec_attn_plan* mp = const_cast<spec_attn_plan*>(plan);
+    std::unique_lock<std::mutex> maps_lock(mp->maps_mutex, std::defer_lock);
+    if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
+        maps_lock.lock();
+        if (mp->maps_key[0] != q || mp->maps_key[1] != k_pool || mp->maps_key[2] != v_pool) {
+            if (!tc_encode_maps(sp, &mp->maps)) {
+                mp->maps_key[0] = mp->maps_key[1] = mp->maps_key[2] = nullptr;
+                return SPEC_ATTN_E_INVALID_ARG;
+            }
+            mp->maps_key[0] = q;
+            mp->maps_key[1] = k_pool;
+            mp->maps_key[2] = v_pool;
+        }
+    }
     if (plan->ev_begin) {
         e = cudaEventRecord(plan->ev_begin, stream);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05)
-        e = tc_launch(sp, trace != nullptr, plan->grid, stream);
-    else
+    if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
+        e = tc_launch(sp, mp->maps, trace != nullptr, plan->grid, stream);
+        maps_lock.unlock();
+    } else
         e = cc_launch(sp, p.kv_dtype, plan->cc, trace != nullptr, plan->grid, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (plan->ev_end) {

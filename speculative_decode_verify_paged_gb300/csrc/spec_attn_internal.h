@@ -82,11 +82,18 @@ cudaError_t cc_launch(const SplitParams& p, int kv_dtype, const CcConfig& cfg, b
                       dim3 grid, cudaStream_t stream);
 
 // ---- tcgen05 split-KV kernel (split_attn_tc.cu) ----
+// TMA descriptors of one (Q, K pool, V pool) triple; opaque CUtensorMap storage.
+struct TcMaps {
+    alignas(64) unsigned char q[128];
+    alignas(64) unsigned char k[128];
+    alignas(64) unsigned char v[128];
+};
 bool tc_supported(int head_dim, int kv_dtype, int max_rows);
 int tc_smem_bytes(int head_dim);
 int tc_threads();
 cudaError_t tc_prepare(int head_dim);
-cudaError_t tc_launch(const SplitParams& p, bool traced, dim3 grid, cudaStream_t stream);
+bool tc_encode_maps(const SplitParams& p, TcMaps* maps);
+cudaError_t tc_launch(const SplitParams& p, const TcMaps& maps, bool traced, dim3 grid, cudaStream_t stream);
 
 // ---- LSE merge (merge_lse.cu) ----
 cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic);

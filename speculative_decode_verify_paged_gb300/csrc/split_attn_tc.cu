@@ -49,7 +49,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kBN = 32;        // keys per tile (two 16-key pages)
+constexpr int kBN = 64;        // keys per tile (a multiple of the 16-key page; 32 or 64)
+constexpr int kPPT = kBN / 16;  // pages per tile
+static_assert(kBN == 32 || kBN == 64, "tile");
 constexpr int kM = 128;        // MMA rows (query tile, padded)
 constexpr int kTcThreads = 256;
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM cycles
@@ -63,18 +65,23 @@ template <int D>
 struct TcLayout {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along head_dim
     static constexpr int kQBytes = kM * D * 2;
-    static constexpr int kPBytes = kM * 128;               // two 32-key halves of a 64-key swizzle atom row
+    // P: two tiles (double buffer).  32-key tiles share each 128-byte swizzle row
+    // (one half each); 64-key tiles fill a row, so the buffers are separate.
+    static constexpr int kPBytes = kM * 128 * (kBN == 64 ? 2 : 1);
     static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile
+    static constexpr int kPageBytes = 16 * D * 2;          // one page-head of V
     static constexpr int kAuxBytes = 1536;
     static constexpr int kMaxDyn = 232448;                  // 227 KB opt-in limit
     static constexpr int kRing = (kMaxDyn - 1024 - kQBytes - kPBytes - kAuxBytes) / kTileBytes;
     // K tiles are released as soon as their S = Q K^T is done, V tiles only after
     // P V: give V the larger share of the ring.
-    static constexpr int kNK = (kRing / 3) > kMaxNK ? kMaxNK : (kRing / 3);
+    static constexpr int kNK = (kRing / 3) > kMaxNK ? kMaxNK : ((kRing / 3) < 2 ? 2 : (kRing / 3));
     static constexpr int kNV = (kRing - kNK) > kMaxNV ? kMaxNV : (kRing - kNK);
     static constexpr int kSmem = 1024 + kQBytes + kPBytes + (kNK + kNV) * kTileBytes + kAuxBytes;
     static constexpr uint32_t kTmemCols = (D + 2 * kBN) <= 128 ? 128u : ((D + 2 * kBN) <= 256 ? 256u : 512u);
     static_assert(kNK >= 2 && kNV >= 2, "ring too small");
+    // the epilogue stages kM rows of fp32 O (+16 B padding) over query/P/ring buffers
+    static_assert(kM * (D * 4 + 16) <= kQBytes + kPBytes + (kNK + kNV) * kTileBytes, "epilogue staging");
 };
 
 struct TcAux {
@@ -90,13 +97,19 @@ struct TcAux {
     uint64_t o_final;    // one phase after the last P V (the epilogue's wait)
     uint64_t q_full;
     uint64_t drain;
-    int32_t pages_v[kMaxNV][2];            // physical pages of each V slot (index trace)
+    int32_t pages_v[kMaxNV][kPPT];         // physical pages of each V slot (index trace)
     uint32_t tmem_base;
     int abort;
     int32_t list_k[kPageListCap];          // the split's page ids, one list per producer
     int32_t list_v[kPageListCap];
 };
 static_assert(sizeof(TcAux) <= 1536, "aux region");
+
+// Byte offset of P buffer b as seen by the MMA descriptor (32-key tiles: the
+// second half of each 128-byte row; 64-key tiles: a separate 16 KB buffer).
+__device__ __forceinline__ uint32_t p_tile_offset(int b) {
+    return kBN == 32 ? static_cast<uint32_t>(b * 64) : static_cast<uint32_t>(b * kM * 128);
+}
 
 // Warp-uniform bounded wait (all 32 lanes leave together).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -139,21 +152,27 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
     for (int t = 0; t < T; ++t) {
         const int slot = t % NSLOT;
         if (t >= NSLOT && !warp_wait(&empty[slot], ((t / NSLOT) - 1) & 1, abort)) break;
-        const int rel = t * 2;  // first page of the tile, relative to the split
+        const int rel = t * kPPT;  // first page of the tile, relative to the split
         if (rel >= list_base + kPageListCap) {
             __syncwarp();
             list_base = rel;
             fill_list(list_base);
         }
         if (lane == 0) {
-            const int np = min(2, (key_hi - (key_lo + t * kBN) + 15) / 16);
+            const int np = min(kPPT, (key_hi - (key_lo + t * kBN) + 15) / 16);
             unsigned char* dst = ring + slot * L::kTileBytes;
             mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(np * L::kChunks * 2048));
             for (int pp = 0; pp < np; ++pp) {
                 const int pg = list[rel - list_base + pp];
                 if (TRACE && IS_V) aux->pages_v[slot][pp] = pg;
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_4d(dst + c * (kBN * 128) + pp * 2048, tm, c * 64, 0, kvh, pg, &full[slot]);
+                if (IS_V) {
+                    // whole page-head in one copy: [chunk][16 slots][128 B], page after page
+                    tma_load_5d(dst + pp * L::kPageBytes, tm, 0, 0, 0, kvh, pg, &full[slot]);
+                } else {
+                    // chunk-major across the tile's pages, so S = Q K^T spans the tile in one MMA
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_4d(dst + c * (kBN * 128) + pp * 2048, tm, c * 64, 0, kvh, pg, &full[slot]);
+                }
             }
         }
         __syncwarp();
@@ -262,7 +281,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Issues S_t = Q K_t^T and O += P_t V_t in whichever order their inputs
-        // become ready (polling), so a late K tile never holds back a P V.
+        // become ready (non-blocking polls), so a late K tile never holds back
+        // a P V and vice versa.
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kBN, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kM, D, 0, 1);
@@ -276,8 +296,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 bool progressed = false;
                 if (ns < T) {
                     const int ks = ns % NK, b = ns & 1;
-                    if (mbar_try_wait(&aux->k_full[ks], (ns / NK) & 1) &&
-                        (ns < 2 || mbar_try_wait(&aux->s_empty[b], ((ns >> 1) - 1) & 1))) {
+                    if (mbar_test_wait(&aux->k_full[ks], (ns / NK) & 1) &&
+                        (ns < 2 || mbar_test_wait(&aux->s_empty[b], ((ns >> 1) - 1) & 1))) {
                         tc_fence_after();
                         const uint32_t k_addr = smem_addr(sK + ks * L::kTileBytes);
                         const uint32_t d_tmem = tmem + D + b * kBN;
@@ -296,14 +316,16 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 }
                 if (npv < ns) {
                     const int vs = npv % NV, b = npv & 1;
-                    if (mbar_try_wait(&aux->p_full[b], (npv >> 1) & 1) &&
-                        mbar_try_wait(&aux->v_full[vs], (npv / NV) & 1)) {
+                    if (mbar_test_wait(&aux->p_full[b], (npv >> 1) & 1) &&
+                        mbar_test_wait(&aux->v_full[vs], (npv / NV) & 1)) {
                         tc_fence_after();
-                        const int np = min(2, (key_hi - (key_lo + npv * kBN) + 15) / 16);
+                        const int np = min(kPPT, (key_hi - (key_lo + npv * kBN) + 15) / 16);
                         const uint32_t v_addr = smem_addr(sV + vs * L::kTileBytes);
                         for (int kk = 0; kk < np; ++kk) {
-                            const uint64_t a = smem_desc_sw128(p_addr + b * 64 + kk * 32, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(v_addr + kk * 2048, kBN * 128, 1024);
+                            const uint64_t a = smem_desc_sw128(p_addr + p_tile_offset(b) + kk * 32, 16, 1024);
+                            // V page kk: [chunk][16 keys][128 B]; MN atoms (64 head_dim
+                            // elements) 2 KB apart, 8-key groups 1 KB apart
+                            const uint64_t bd = smem_desc_sw128(v_addr + kk * L::kPageBytes, 2048, 1024);
                             mma_bf16_ss(tmem, a, bd, idesc_o, (npv > 0 || kk > 0) ? 1u : 0u);
                         }
                         mma_commit(&aux->v_empty[vs]);
@@ -350,8 +372,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             const int b = t & 1;
             if (!(ok = warp_wait(&aux->s_full[b], (t >> 1) & 1, abort))) break;
             tc_fence_after();
-            float sv[32];
-            tmem_ld32(lane_tmem + D + b * kBN, sv);
+            float sv[kBN];
+#pragma unroll
+            for (int h = 0; h < kBN / 32; ++h)
+                tmem_ld32(lane_tmem + D + b * kBN + h * 32, *reinterpret_cast<float(*)[32]>(sv + h * 32));
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -411,7 +435,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 if (!(ok = warp_wait(&aux->v_full[vs], (t / NV) & 1, abort))) break;
             }
             if (ragged_tail) {
-                const int np = min(2, (key_hi - key0 + 15) / 16);
+                const int np = min(kPPT, (key_hi - key0 + 15) / 16);
                 const int row_first = ri.len - key0, row_end = np * 16;
                 unsigned char* vt = sV + vs * L::kTileBytes;
                 const int pieces = (row_end - row_first) * L::kChunks * 8;
@@ -419,7 +443,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     const int rr = row_first + u / (L::kChunks * 8);
                     const int rem = u % (L::kChunks * 8);
                     const int c = rem >> 3, j = rem & 7;
-                    *reinterpret_cast<uint4*>(vt + c * (kBN * 128) + rr * 128 + (j << 4)) =
+                    *reinterpret_cast<uint4*>(vt + (rr >> 4) * L::kPageBytes + c * 2048 + (rr & 15) * 128 + (j << 4)) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
             }
@@ -430,11 +454,11 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     tr_sum += (long long)aux->pages_v[vs][c >> 4] * 16 + (key & 15);
                 }
             }
-            // P row m into half b of the 128-byte-swizzled K-major A tile
+            // P row m into buffer b of the 128-byte-swizzled K-major A tile
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int chunk = b * 4 + j;
-                *reinterpret_cast<uint4*>(sP + m * 128 + ((chunk ^ (m & 7)) << 4)) =
+            for (int j = 0; j < kBN / 8; ++j) {
+                const int chunk = (kBN == 32 ? b * 4 : 0) + j;
+                *reinterpret_cast<uint4*>(sP + (kBN == 64 ? b * (kM * 128) : 0) + m * 128 + ((chunk ^ (m & 7)) << 4)) =
                     make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
             }
             fence_proxy_async_smem();
@@ -446,18 +470,24 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         if (ok) ok = warp_wait(&aux->o_final, 0, abort);
         tc_fence_after();
         if (ok) {
+            // Epilogue.  Every MMA and copy has completed (o_final), so the query,
+            // P and ring buffers are free: each warp stages its 32 rows of O / l
+            // there (row stride padded by 16 bytes: conflict-free 16-byte stores),
+            // then copies them out row by row with coalesced 512-byte stores.
             const float inv = (valid && l_sum > 0.f) ? (p.out_scale / l_sum) : 0.f;
             const float lse2 = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) : -INFINITY;
             const size_t oi = (size_t)qrow * p.num_q_heads + hq;
             const bool final_out = (ri.nsplits == 1);
+            const int row_bytes = final_out ? D * 2 : D * 4;
+            const int rs = row_bytes + 16;
+            unsigned char* stg = smem;
+            unsigned char* myrow = stg + m * rs;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
                 float ov[32];
                 tmem_ld32(lane_tmem + ch * 32, ov);
                 tmem_wait_ld();
-                if (!valid) continue;
                 if (final_out) {
-                    uint16_t* op = p.o + oi * D + ch * 32;
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t w[4];
@@ -467,16 +497,27 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                                 __floats2bfloat162_rn(ov[q4 * 8 + 2 * e] * inv, ov[q4 * 8 + 2 * e + 1] * inv);
                             w[e] = *reinterpret_cast<const uint32_t*>(&h2);
                         }
-                        *reinterpret_cast<uint4*>(op + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(myrow + ch * 64 + q4 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 } else {
-                    float* wp = p.ws_o + ((size_t)split * p.total_rows * p.num_q_heads + oi) * D + ch * 32;
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
-                        *reinterpret_cast<float4*>(wp + q4 * 4) =
+                        *reinterpret_cast<float4*>(myrow + ch * 128 + q4 * 16) =
                             make_float4(ov[q4 * 4] * inv, ov[q4 * 4 + 1] * inv, ov[q4 * 4 + 2] * inv,
                                         ov[q4 * 4 + 3] * inv);
                 }
+            }
+            __syncwarp();
+            for (int rr = 0; rr < 32; ++rr) {
+                const int mm = wq * 32 + rr;
+                if (mm >= R) break;
+                const size_t oi2 = (size_t)(ri.row0 + mm / G) * p.num_q_heads + kvh * G + (mm % G);
+                unsigned char* dst = final_out
+                    ? reinterpret_cast<unsigned char*>(p.o + oi2 * D)
+                    : reinterpret_cast<unsigned char*>(p.ws_o + ((size_t)split * p.total_rows * p.num_q_heads + oi2) * D);
+                const unsigned char* src = stg + mm * rs;
+                for (int off = lane * 16; off < row_bytes; off += 512)
+                    *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(src + off);
             }
             if (valid) {
                 if (final_out) {
@@ -540,6 +581,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Pool [num_pages, Hkv, 16, d] bf16 viewed as a 4-D tensor (d, slot, kv head, page);
 // box = 64 head_dim elements x 16 slots of one page and head, 128-byte swizzle.
+// The same pool as a 5-D tensor (64 elements, slot, 64-element chunk, kv head,
+// page); box = one whole page-head, landing chunk-major: [chunk][16 slots][128 B].
+bool encode_pool_map_pages(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[5] = {64, 16, (cuuint64_t)d / 64, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)d * 2, 128, (cuuint64_t)d * 2 * 16, (cuuint64_t)d * 2 * 16 * hkv};
+    cuuint32_t box[5] = {64, 16, (cuuint32_t)d / 64, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
 bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -587,15 +643,22 @@ cudaError_t tc_prepare(int head_dim) {
     return encode_fn() ? cudaSuccess : cudaErrorNotSupported;
 }
 
-cudaError_t tc_launch(const SplitParams& p, bool traced, dim3 grid, cudaStream_t stream) {
+bool tc_encode_maps(const SplitParams& p, TcMaps* maps) {
+    static_assert(sizeof(CUtensorMap) == sizeof(maps->q), "tensor map size");
+    return encode_q_map(reinterpret_cast<CUtensorMap*>(maps->q), p.q, p.total_rows, p.num_q_heads, p.head_dim,
+                        p.group, p.max_w) &&
+           encode_pool_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
+                           p.head_dim) &&
+           encode_pool_map_pages(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,
+                                 p.head_dim);
+}
+
+cudaError_t tc_launch(const SplitParams& p, const TcMaps& maps, bool traced, dim3 grid, cudaStream_t stream) {
     TcKernel k = pick(p.head_dim, traced);
     if (!k) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv;
-    if (!encode_q_map(&mq, p.q, p.total_rows, p.num_q_heads, p.head_dim, p.group, p.max_w) ||
-        !encode_pool_map(&mk, p.k_pool, p.num_pages, p.num_kv_heads, p.head_dim) ||
-        !encode_pool_map(&mv, p.v_pool, p.num_pages, p.num_kv_heads, p.head_dim))
-        return cudaErrorInvalidValue;
-    k<<<grid, kTcThreads, smem_for(p.head_dim), stream>>>(p, mq, mk, mv);
+    k<<<grid, kTcThreads, smem_for(p.head_dim), stream>>>(p, *reinterpret_cast<const CUtensorMap*>(maps.q),
+                                                           *reinterpret_cast<const CUtensorMap*>(maps.k),
+                                                           *reinterpret_cast<const CUtensorMap*>(maps.v));
     return cudaGetLastError();
 }
 
