@@ -9,15 +9,17 @@
 //   lse = log2 sum_s 2^(lse_s),  O = sum_s 2^(lse_s - lse) O_s,
 // written as bf16 O (round to nearest even) and natural-log LSE (lse * ln 2).
 //
-// One CTA per (window row, query head).  Its 256 threads are split into
-// split groups x head_dim vectors: thread (g, v) owns float4 v of the splits
-// g, g + SG, g + 2 SG, ...  It issues the loads of up to kBatch of its splits
-// (LSE and partial row) at once -- one memory round trip for the usual split
-// counts -- and folds them with a running maximum (online LSE combination).
-// The groups are then combined once through shared memory.  Requests with a
-// single split were finished by the split kernel and are skipped here.  The
-// kernel may be launched as a programmatic dependent of the split kernel: it
-// waits on griddepcontrol before touching partials.
+// Work layout.  A thread owns 8 consecutive output elements (two float4) of one
+// (window row, query head) pair and the splits g, g + SG, g + 2 SG, ... of it,
+// where SG (split groups) is chosen at launch so that a thread has at most
+// kBatch splits: all its loads (LSE and partial rows) are issued at once, one
+// memory round trip, and folded with a running maximum (online LSE
+// combination).  A 256-thread CTA covers 256 / (D/8 * SG) pairs, so short
+// split counts pack many pairs per CTA.  Groups are combined once through
+// shared memory.  Requests with a single split were finished by the split
+// kernel and are skipped.  The kernel may be launched as a programmatic
+// dependent of the split kernel: it waits on griddepcontrol before touching
+// partials.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,102 +29,113 @@ namespace spec_attn {
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kBatch = 8;
+constexpr int kBatch = 5;
 
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const MergeParams p) {
-    constexpr int VEC = D / 4;                 // float4 vectors per row
-    constexpr int SG = kMergeThreads / VEC;    // split groups
-    __shared__ float4 part[SG][VEC];
-    __shared__ float part_m[SG], part_l[SG];
+__global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const MergeParams p, const int sg) {
+    constexpr int VEC = D / 8;                  // 8-float slices per row
+    __shared__ float4 part[kMergeThreads][2];
+    __shared__ float part_m[kMergeThreads], part_l[kMergeThreads];
     const int tid = threadIdx.x;
-    const int v = tid % VEC, g = tid / VEC;
-    const int pair = blockIdx.x;
+    const int tpp = VEC * sg;                    // threads per pair
+    const int ppc = kMergeThreads / tpp;         // pairs per CTA
+    const int lp = tid / tpp, within = tid % tpp;
+    const int g = within / VEC, v = within % VEC;
+    const int pair = blockIdx.x * ppc + lp;
     const int r = blockIdx.y;
     const int i = pair / p.num_q_heads;
     const int h = pair % p.num_q_heads;
 
     ReqInfo ri;
-    const bool ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
-                                 p.bt_capacity_keys, p.keys_per_split, nullptr, ri);
-    if (!ok || i >= ri.w || ri.nsplits <= 1) {
-        pdl_wait_primary();
-        return;
-    }
-    const size_t oi = (size_t)(ri.row0 + i) * p.num_q_heads + h;
-    const size_t split_stride = (size_t)p.total_rows * p.num_q_heads;
-    const int n = ri.nsplits;
+    const bool req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
+                                     p.bt_capacity_keys, p.keys_per_split, nullptr, ri);
+    const bool active = lp < ppc && req_ok && i < ri.w && ri.nsplits > 1;
     // Wait for the split kernel's partials (no-op without a programmatic edge).
     pdl_wait_primary();
 
     float m_run = -INFINITY, l_run = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = g; s0 < n; s0 += SG * kBatch) {
-        float ls[kBatch];
-        float4 o[kBatch];
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    size_t oi = 0;
+    if (active) {
+        oi = (size_t)(ri.row0 + i) * p.num_q_heads + h;
+        const size_t split_stride = (size_t)p.total_rows * p.num_q_heads;
+        const int n = ri.nsplits;
+        for (int s0 = g; s0 < n; s0 += sg * kBatch) {
+            float ls[kBatch];
+            float4 o0[kBatch], o1[kBatch];
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int s = s0 + k * SG;
-            if (s < n) {
-                ls[k] = p.ws_lse[s * split_stride + oi];
-                o[k] = *reinterpret_cast<const float4*>(p.ws_o + (s * split_stride + oi) * D + v * 4);
-            } else {
-                ls[k] = -INFINITY;
-                o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < kBatch; ++k) {
+                const int s = s0 + k * sg;
+                if (s < n) {
+                    ls[k] = p.ws_lse[s * split_stride + oi];
+                    const float* src = p.ws_o + (s * split_stride + oi) * D + v * 8;
+                    o0[k] = *reinterpret_cast<const float4*>(src);
+                    o1[k] = *reinterpret_cast<const float4*>(src + 4);
+                } else {
+                    ls[k] = -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (ls[k] == -INFINITY) continue;
+                if (ls[k] > m_run) {
+                    const float a = fast_exp2(m_run - ls[k]);   // 0 while m_run is -inf
+                    a0.x *= a; a0.y *= a; a0.z *= a; a0.w *= a;
+                    a1.x *= a; a1.y *= a; a1.z *= a; a1.w *= a;
+                    l_run *= a;
+                    m_run = ls[k];
+                }
+                const float w = fast_exp2(ls[k] - m_run);
+                a0.x = fmaf(w, o0[k].x, a0.x); a0.y = fmaf(w, o0[k].y, a0.y);
+                a0.z = fmaf(w, o0[k].z, a0.z); a0.w = fmaf(w, o0[k].w, a0.w);
+                a1.x = fmaf(w, o1[k].x, a1.x); a1.y = fmaf(w, o1[k].y, a1.y);
+                a1.z = fmaf(w, o1[k].z, a1.z); a1.w = fmaf(w, o1[k].w, a1.w);
+                l_run += w;
             }
         }
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            if (ls[k] == -INFINITY) continue;
-            if (ls[k] > m_run) {
-                const float a = fast_exp2(m_run - ls[k]);   // 0 when m_run is -inf
-                acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
-                l_run *= a;
-                m_run = ls[k];
-            }
-            const float w = fast_exp2(ls[k] - m_run);
-            acc.x = fmaf(w, o[k].x, acc.x);
-            acc.y = fmaf(w, o[k].y, acc.y);
-            acc.z = fmaf(w, o[k].z, acc.z);
-            acc.w = fmaf(w, o[k].w, acc.w);
-            l_run += w;
-        }
     }
-    part[g][v] = acc;
-    if (v == 0) {
-        part_m[g] = m_run;
-        part_l[g] = l_run;
-    }
+    part[tid][0] = a0;
+    part[tid][1] = a1;
+    part_m[tid] = m_run;
+    part_l[tid] = l_run;
     __syncthreads();
-    if (g != 0) return;
+    if (!active || g != 0) return;
+    const int base = lp * tpp + v;               // thread of group k: base + k * VEC
     float mx = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < SG; ++k) mx = fmaxf(mx, part_m[k]);
-    float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < sg; ++k) mx = fmaxf(mx, part_m[base + k * VEC]);
+    float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0;
     float wsum = 0.f;
-#pragma unroll
-    for (int k = 0; k < SG; ++k) {
-        if (part_m[k] == -INFINITY) continue;
-        const float a = fast_exp2(part_m[k] - mx);
-        tot.x = fmaf(a, part[k][v].x, tot.x);
-        tot.y = fmaf(a, part[k][v].y, tot.y);
-        tot.z = fmaf(a, part[k][v].z, tot.z);
-        tot.w = fmaf(a, part[k][v].w, tot.w);
-        wsum = fmaf(a, part_l[k], wsum);
+    for (int k = 0; k < sg; ++k) {
+        const int j = base + k * VEC;
+        if (part_m[j] == -INFINITY) continue;
+        const float a = fast_exp2(part_m[j] - mx);
+        const float4 q0 = part[j][0], q1 = part[j][1];
+        t0.x = fmaf(a, q0.x, t0.x); t0.y = fmaf(a, q0.y, t0.y); t0.z = fmaf(a, q0.z, t0.z); t0.w = fmaf(a, q0.w, t0.w);
+        t1.x = fmaf(a, q1.x, t1.x); t1.y = fmaf(a, q1.y, t1.y); t1.z = fmaf(a, q1.z, t1.z); t1.w = fmaf(a, q1.w, t1.w);
+        wsum = fmaf(a, part_l[j], wsum);
     }
     const float inv = 1.f / wsum;
-    const uint32_t lo = float_to_bf16_bits(tot.x * inv) | ((uint32_t)float_to_bf16_bits(tot.y * inv) << 16);
-    const uint32_t hi = float_to_bf16_bits(tot.z * inv) | ((uint32_t)float_to_bf16_bits(tot.w * inv) << 16);
-    *reinterpret_cast<uint2*>(p.o + oi * D + v * 4) = make_uint2(lo, hi);
+    uint4 out;
+    out.x = float_to_bf16_bits(t0.x * inv) | ((uint32_t)float_to_bf16_bits(t0.y * inv) << 16);
+    out.y = float_to_bf16_bits(t0.z * inv) | ((uint32_t)float_to_bf16_bits(t0.w * inv) << 16);
+    out.z = float_to_bf16_bits(t1.x * inv) | ((uint32_t)float_to_bf16_bits(t1.y * inv) << 16);
+    out.w = float_to_bf16_bits(t1.z * inv) | ((uint32_t)float_to_bf16_bits(t1.w * inv) << 16);
+    *reinterpret_cast<uint4*>(p.o + oi * D + v * 8) = out;
     if (p.lse && v == 0) p.lse[oi] = (mx + log2f(wsum)) * kLn2;
 }
 
 }  // namespace
 
 cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic) {
-    dim3 grid(p.max_w * p.num_q_heads, p.num_reqs, 1);
+    const int vec = p.head_dim / 8;
+    int sg = (p.max_splits + kBatch - 1) / kBatch;
+    if (sg < 1) sg = 1;
+    if (sg > kMergeThreads / vec) sg = kMergeThreads / vec;
+    const int ppc = kMergeThreads / (vec * sg);
+    const int pairs = p.max_w * p.num_q_heads;
+    dim3 grid((pairs + ppc - 1) / ppc, p.num_reqs, 1);
     dim3 block(kMergeThreads, 1, 1);
-    void (*k)(const MergeParams) = nullptr;
+    void (*k)(const MergeParams, const int) = nullptr;
     switch (p.head_dim) {
         case 64: k = &merge_lse_kernel<64>; break;
         case 128: k = &merge_lse_kernel<128>; break;
@@ -139,7 +152,7 @@ cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool program
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k, p);
+    return cudaLaunchKernelEx(&cfg, k, p, sg);
 }
 
 }  // namespace spec_attn
