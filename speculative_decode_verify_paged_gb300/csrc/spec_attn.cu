@@ -210,9 +210,9 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         plan->variant = SPEC_ATTN_VARIANT_TCGEN05;
         plan->rows_per_cta = 128;
         plan->row_groups = 1;
-        plan->threads = tc_threads();
-        plan->smem = tc_smem_bytes(p.head_dim);
-        e = tc_prepare(p.head_dim);
+        plan->threads = tc_threads(p.kv_dtype);
+        plan->smem = tc_smem_bytes(p.head_dim, p.kv_dtype);
+        e = tc_prepare(p.head_dim, p.kv_dtype);
     } else {
         plan->variant = SPEC_ATTN_VARIANT_CUDA_CORE;
         plan->cc = cc_config(p.head_dim, p.kv_dtype, max_rows);
@@ -393,7 +393,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
         maps_lock.lock();
         if (mp->maps_key[0] != q || mp->maps_key[1] != k_pool || mp->maps_key[2] != v_pool) {
-            if (!tc_encode_maps(sp, &mp->maps)) {
+            if (!tc_encode_maps(sp, p.kv_dtype, &mp->maps)) {
                 mp->maps_key[0] = mp->maps_key[1] = mp->maps_key[2] = nullptr;
                 return SPEC_ATTN_E_INVALID_ARG;
             }
@@ -407,7 +407,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
-        e = tc_launch(sp, mp->maps, trace != nullptr, plan->grid, stream);
+        e = tc_launch(sp, p.kv_dtype, mp->maps, trace != nullptr, plan->grid, stream);
         maps_lock.unlock();
     } else
         e = cc_launch(sp, p.kv_dtype, plan->cc, trace != nullptr, plan->grid, stream);

@@ -89,11 +89,12 @@ struct TcMaps {
     alignas(64) unsigned char v[128];
 };
 bool tc_supported(int head_dim, int kv_dtype, int max_rows);
-int tc_smem_bytes(int head_dim);
-int tc_threads();
-cudaError_t tc_prepare(int head_dim);
-bool tc_encode_maps(const SplitParams& p, TcMaps* maps);
-cudaError_t tc_launch(const SplitParams& p, const TcMaps& maps, bool traced, dim3 grid, cudaStream_t stream);
+int tc_smem_bytes(int head_dim, int kv_dtype);
+int tc_threads(int kv_dtype);
+cudaError_t tc_prepare(int head_dim, int kv_dtype);
+bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps);
+cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bool traced, dim3 grid,
+                      cudaStream_t stream);
 
 // ---- LSE merge (merge_lse.cu) ----
 cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic);

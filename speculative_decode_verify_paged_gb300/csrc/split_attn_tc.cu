@@ -39,6 +39,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -53,33 +54,50 @@ constexpr int kBN = 64;        // keys per tile (a multiple of the 16-key page; 
 constexpr int kPPT = kBN / 16;  // pages per tile
 static_assert(kBN == 32 || kBN == 64, "tile");
 constexpr int kM = 128;        // MMA rows (query tile, padded)
-constexpr int kTcThreads = 256;
+constexpr int kTcThreadsBf16 = 256;   // warps 0-7
+constexpr int kTcThreadsFp4 = 512;    // + warps 8-11 (K dequant) and 12-15 (V dequant)
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM cycles
 constexpr long long kDrainLimit = 200000000LL;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units: rescale when max grows by > 2^8
-constexpr int kPageListCap = 96;                 // page ids staged in shared memory at a time
+constexpr int kPageListCap = 64;                 // page ids staged in shared memory at a time
+constexpr int kMaxNR = 8;                        // NVFP4 raw (codes + scales) ring slots
 constexpr int kMaxNK = 8, kMaxNV = 16;
 
-// Shared memory: query tile | P tile | K ring | V ring | barriers and page lists.
-template <int D>
+// Shared memory: query tile | P tile | K ring | V ring | [NVFP4 raw ring] | barriers.
+// bf16 KV: K and V tiles arrive by TMA into rings of kNK / kNV slots.
+// NVFP4 KV: codes and scales arrive by cp.async into a ring of kNR raw slots and
+// are decoded into one bf16 K tile and one bf16 V tile (kNK = kNV = 1).
+template <int D, int KV>
 struct TcLayout {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along head_dim
     static constexpr int kQBytes = kM * D * 2;
     // P: two tiles (double buffer).  32-key tiles share each 128-byte swizzle row
     // (one half each); 64-key tiles fill a row, so the buffers are separate.
     static constexpr int kPBytes = kM * 128 * (kBN == 64 ? 2 : 1);
-    static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile
-    static constexpr int kPageBytes = 16 * D * 2;          // one page-head of V
+    static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile (bf16)
+    static constexpr int kPageBytes = 16 * D * 2;          // one page-head of V (bf16)
+    static constexpr int kRawCodePage = 16 * D / 2;        // NVFP4 codes of one page-head
+    static constexpr int kRawScalePage = 16 * D / 16;      // NVFP4 scales of one page-head
+    static constexpr int kRawKS = kPPT * kRawCodePage;     // offsets inside a raw slot
+    static constexpr int kRawVC = kRawKS + kPPT * kRawScalePage;
+    static constexpr int kRawVS = kRawVC + kPPT * kRawCodePage;
+    static constexpr int kRawTile = 2 * kPPT * (kRawCodePage + kRawScalePage);
     static constexpr int kAuxBytes = 1536;
     static constexpr int kMaxDyn = 232448;                  // 227 KB opt-in limit
-    static constexpr int kRing = (kMaxDyn - 1024 - kQBytes - kPBytes - kAuxBytes) / kTileBytes;
-    // K tiles are released as soon as their S = Q K^T is done, V tiles only after
-    // P V: give V the larger share of the ring.
-    static constexpr int kNK = (kRing / 3) > kMaxNK ? kMaxNK : ((kRing / 3) < 2 ? 2 : (kRing / 3));
-    static constexpr int kNV = (kRing - kNK) > kMaxNV ? kMaxNV : (kRing - kNK);
-    static constexpr int kSmem = 1024 + kQBytes + kPBytes + (kNK + kNV) * kTileBytes + kAuxBytes;
+    static constexpr int kFixed = 1024 + kQBytes + kPBytes + kAuxBytes;
+    static constexpr int kRing = (kMaxDyn - kFixed) / kTileBytes;
+    // bf16: K tiles are released as soon as their S = Q K^T is done, V tiles only
+    // after P V, so V gets the larger share of the ring.
+    static constexpr int kNK = KV ? 1 : ((kRing / 3) > kMaxNK ? kMaxNK : ((kRing / 3) < 2 ? 2 : (kRing / 3)));
+    static constexpr int kNV = KV ? 1 : ((kRing - kNK) > kMaxNV ? kMaxNV : (kRing - kNK));
+    static constexpr int kRawFit = (kMaxDyn - kFixed - 2 * kTileBytes - 512) / kRawTile;
+    static constexpr int kNR = KV ? (kRawFit > kMaxNR ? kMaxNR : kRawFit) : 0;
+    static constexpr int kLutBytes = KV ? 512 : 0;         // NVFP4: e4m3 -> bf16 scale table
+    static constexpr int kSmem = kFixed + (kNK + kNV) * kTileBytes + kNR * kRawTile + kLutBytes;
+    static constexpr int kThreads = KV ? kTcThreadsFp4 : kTcThreadsBf16;
     static constexpr uint32_t kTmemCols = (D + 2 * kBN) <= 128 ? 128u : ((D + 2 * kBN) <= 256 ? 256u : 512u);
-    static_assert(kNK >= 2 && kNV >= 2, "ring too small");
+    static_assert(KV ? (kNR >= 2) : (kNK >= 2 && kNV >= 2), "ring too small");
+    static_assert(kSmem <= kMaxDyn, "shared memory");
     // the epilogue stages kM rows of fp32 O (+16 B padding) over query/P/ring buffers
     static_assert(kM * (D * 4 + 16) <= kQBytes + kPBytes + (kNK + kNV) * kTileBytes, "epilogue staging");
 };
@@ -97,7 +115,10 @@ struct TcAux {
     uint64_t o_final;    // one phase after the last P V (the epilogue's wait)
     uint64_t q_full;
     uint64_t drain;
+    uint64_t raw_full[kMaxNR];             // NVFP4: codes/scales of a tile landed (32 lane arrivals)
+    uint64_t raw_empty[kMaxNR];            // NVFP4: both dequant warpgroups are done with a raw slot
     int32_t pages_v[kMaxNV][kPPT];         // physical pages of each V slot (index trace)
+    int32_t raw_pages[kMaxNR][kPPT];       // NVFP4: physical pages of each raw slot
     uint32_t tmem_base;
     int abort;
     int32_t list_k[kPageListCap];          // the split's page ids, one list per producer
@@ -132,7 +153,7 @@ template <int D, int NSLOT, bool IS_V, bool TRACE>
 __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
                                        unsigned char* ring, uint64_t* full, uint64_t* empty, int32_t* list,
                                        TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane) {
-    using L = TcLayout<D>;
+    using L = TcLayout<D, 0>;
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride + key_lo / 16;
     const int n_pages = (key_hi - key_lo + 15) / 16;
     int list_base = 0;
@@ -181,6 +202,151 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
     return issued;
 }
 
+// NVFP4: one warp copies each tile's e2m1 codes and e4m3 scales (K then V; a
+// page-head's codes and scales are contiguous in their pools) with 16-byte
+// cp.async into a raw ring slot; every lane then arrives on the slot's
+// barrier when its copies have landed.
+__device__ __forceinline__ void cp_async16_raw(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int D>
+__device__ __forceinline__ void produce_raw(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
+                                            unsigned char* raw, TcAux* aux, volatile int* abort, int lane) {
+    using L = TcLayout<D, 1>;
+    constexpr int NR = L::kNR;
+    const int32_t* bt = p.block_table + (size_t)r * p.bt_stride + key_lo / 16;
+    const int n_pages = (key_hi - key_lo + 15) / 16;
+    int32_t* list = aux->list_k;
+    int list_base = 0;
+    auto fill_list = [&](int base) {
+        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) {
+            int pg = bt[base + i];
+            if (pg < 0 || pg >= p.num_pages) {
+                atomicOr(p.status, kDevBadPage);
+                pg = 0;
+            }
+            list[i] = pg;
+        }
+        __syncwarp();
+    };
+    fill_list(0);
+    const unsigned char* kc_pool = static_cast<const unsigned char*>(p.k_pool);
+    const unsigned char* vc_pool = static_cast<const unsigned char*>(p.v_pool);
+    for (int t = 0; t < T; ++t) {
+        const int slot = t % NR;
+        if (t >= NR && !warp_wait(&aux->raw_empty[slot], ((t / NR) - 1) & 1, abort)) break;
+        const int rel = t * kPPT;
+        if (rel >= list_base + kPageListCap) {
+            __syncwarp();
+            list_base = rel;
+            fill_list(list_base);
+        }
+        const int np = min(kPPT, (key_hi - (key_lo + t * kBN) + 15) / 16);
+        unsigned char* dst = raw + slot * L::kRawTile;
+        for (int pp = 0; pp < np; ++pp) {
+            const int pg = list[rel - list_base + pp];
+            if (lane == 0) aux->raw_pages[slot][pp] = pg;
+            const size_t tok = ((size_t)pg * p.num_kv_heads + kvh) * 16;
+            const unsigned char* kc = kc_pool + tok * (D / 2);
+            const unsigned char* vc = vc_pool + tok * (D / 2);
+            const unsigned char* ks = p.k_scales + tok * (D / 16);
+            const unsigned char* vs = p.v_scales + tok * (D / 16);
+            for (int c = lane; c < L::kRawCodePage / 16; c += 32) {
+                cp_async16_raw(dst + pp * L::kRawCodePage + c * 16, kc + c * 16);
+                cp_async16_raw(dst + L::kRawVC + pp * L::kRawCodePage + c * 16, vc + c * 16);
+            }
+            for (int c = lane; c < L::kRawScalePage / 16; c += 32) {
+                cp_async16_raw(dst + L::kRawKS + pp * L::kRawScalePage + c * 16, ks + c * 16);
+                cp_async16_raw(dst + L::kRawVS + pp * L::kRawScalePage + c * 16, vs + c * 16);
+            }
+        }
+        cp_async_arrive_noinc(&aux->raw_full[slot]);
+    }
+    cp_async_wait_all();   // nothing may still be landing when the CTA exits
+}
+
+// 16 NVFP4 elements (8 code bytes, low nibble first) times their e4m3 block
+// scale, as 16 bf16 values.  An e2m1 magnitude's bf16 bit pattern is looked up
+// with byte permutes (high and low bytes of the eight possible magnitudes
+// 0, .5, 1, 1.5, 2, 3, 4, 6), the sign is the code's bit 3, and the product with
+// the scale (at most 6 significant bits) is exact in bf16.
+__device__ __forceinline__ void e2m1x4_bf16(uint32_t hw, __nv_bfloat162 s2, uint32_t& p01, uint32_t& p23) {
+    const uint32_t sel = hw & 0x7777u;
+    const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);
+    const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);
+    const uint32_t sg = hw & 0x8888u;
+    uint32_t a = __byte_perm(lo, hi, 0x5140u) | ((sg << 12) & 0x8000u) | ((sg << 24) & 0x80000000u);
+    uint32_t b = __byte_perm(lo, hi, 0x7362u) | ((sg << 4) & 0x8000u) | ((sg << 16) & 0x80000000u);
+    __nv_bfloat162 xa = *reinterpret_cast<const __nv_bfloat162*>(&a);
+    __nv_bfloat162 xb = *reinterpret_cast<const __nv_bfloat162*>(&b);
+    xa = __hmul2(xa, s2);
+    xb = __hmul2(xb, s2);
+    p01 = *reinterpret_cast<const uint32_t*>(&xa);
+    p23 = *reinterpret_cast<const uint32_t*>(&xb);
+}
+// scale_bf16: bf16 bit pattern of the block's e4m3 scale (from the table).
+__device__ __forceinline__ void decode16(uint2 codes, uint32_t scale_bf16, uint4& lo8, uint4& hi8) {
+    const uint32_t s2u = scale_bf16 | (scale_bf16 << 16);
+    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
+    e2m1x4_bf16(codes.x & 0xFFFFu, s2, lo8.x, lo8.y);
+    e2m1x4_bf16(codes.x >> 16, s2, lo8.z, lo8.w);
+    e2m1x4_bf16(codes.y & 0xFFFFu, s2, hi8.x, hi8.y);
+    e2m1x4_bf16(codes.y >> 16, s2, hi8.z, hi8.w);
+}
+
+// One dequant warpgroup (128 threads) decodes the K (IS_V false) or V codes of
+// each tile from the raw ring into the bf16 operand tile the MMA reads: K
+// chunk-major across the tile's keys, V page by page, 128-byte swizzled like
+// the TMA-loaded bf16 tiles.  Keys at or past key_hi are written as zeros.
+template <int D, bool IS_V, bool TRACE>
+__device__ __forceinline__ void dequant(const SplitParams& p, int key_lo, int key_hi, int T, const unsigned char* raw,
+                                        unsigned char* tile, const uint16_t* scale_lut, TcAux* aux,
+                                        volatile int* abort, int dt) {
+    using L = TcLayout<D, 1>;
+    constexpr int NR = L::kNR;
+    constexpr int kPieces = kBN * (D / 16);   // 16-element pieces per tile
+    const int lane = dt & 31;
+    uint64_t* full = IS_V ? aux->v_full : aux->k_full;
+    uint64_t* empty = IS_V ? aux->v_empty : aux->k_empty;
+    for (int t = 0; t < T; ++t) {
+        const int slot = t % NR;
+        if (!warp_wait(&aux->raw_full[slot], (t / NR) & 1, abort)) break;
+        if (t >= 1 && !warp_wait(&empty[0], (t - 1) & 1, abort)) break;
+        const int nvalid = key_hi - (key_lo + t * kBN);
+        const unsigned char* src = raw + slot * L::kRawTile;
+        const unsigned char* codes = src + (IS_V ? L::kRawVC : 0);
+        const unsigned char* scales = src + (IS_V ? L::kRawVS : L::kRawKS);
+#pragma unroll 2
+        for (int u = dt; u < kPieces; u += 128) {
+            const int j = u / (D / 16);           // key within the tile
+            const int e0 = (u % (D / 16)) * 16;   // first head_dim element
+            const int pg = j >> 4, sl = j & 15;
+            uint4 lo8 = make_uint4(0u, 0u, 0u, 0u), hi8 = lo8;
+            if (j < nvalid) {
+                const uint2 cw = *reinterpret_cast<const uint2*>(codes + pg * L::kRawCodePage + sl * (D / 2) + e0 / 2);
+                decode16(cw, scale_lut[scales[pg * L::kRawScalePage + sl * (D / 16) + e0 / 16]], lo8, hi8);
+            }
+            const int c = e0 >> 6, q = (e0 & 63) >> 3;   // 64-element chunk, 16-byte piece
+            unsigned char* row = IS_V ? tile + pg * L::kPageBytes + c * 2048 + sl * 128
+                                      : tile + c * (kBN * 128) + j * 128;
+            *reinterpret_cast<uint4*>(row + ((q ^ (j & 7)) << 4)) = lo8;
+            *reinterpret_cast<uint4*>(row + (((q + 1) ^ (j & 7)) << 4)) = hi8;
+        }
+        if (TRACE && IS_V && dt < kPPT) aux->pages_v[0][dt] = aux->raw_pages[slot][dt];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&full[0]);
+            mbar_arrive(&aux->raw_empty[slot]);
+        }
+    }
+}
+
 template <int NSLOT>
 __device__ __forceinline__ void drain_copies(uint64_t* full, int issued) {
     // let every copy still in flight land before the CTA's shared memory goes away
@@ -190,11 +356,11 @@ __device__ __forceinline__ void drain_copies(uint64_t* full, int issued) {
     }
 }
 
-template <int D, bool TRACE>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int D, int KV, bool TRACE>
+__global__ void __launch_bounds__(KV ? kTcThreadsFp4 : kTcThreadsBf16, 1)
 split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-    using L = TcLayout<D>;
+    using L = TcLayout<D, KV>;
     constexpr int NK = L::kNK, NV = L::kNV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
@@ -218,17 +384,25 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     unsigned char* sP = sQ + L::kQBytes;
     unsigned char* sK = sP + L::kPBytes;
     unsigned char* sV = sK + NK * L::kTileBytes;
-    TcAux* aux = reinterpret_cast<TcAux*>(sV + NV * L::kTileBytes);
+    unsigned char* sRaw = sV + NV * L::kTileBytes;   // NVFP4 only
+    uint16_t* sLut = reinterpret_cast<uint16_t*>(sRaw + L::kNR * L::kRawTile);   // NVFP4 only
+    TcAux* aux = reinterpret_cast<TcAux*>(sRaw + L::kNR * L::kRawTile + L::kLutBytes);
     volatile int* abort = &aux->abort;
 
     if (tid == 0) {
+        // bf16: a full barrier completes on its TMA bytes (one expect_tx arrival);
+        // NVFP4: on the four warps of the dequant warpgroup
         for (int s = 0; s < NK; ++s) {
-            mbar_init(&aux->k_full[s], 1);
+            mbar_init(&aux->k_full[s], KV ? 4 : 1);
             mbar_init(&aux->k_empty[s], 1);
         }
         for (int s = 0; s < NV; ++s) {
-            mbar_init(&aux->v_full[s], 1);
+            mbar_init(&aux->v_full[s], KV ? 4 : 1);
             mbar_init(&aux->v_empty[s], 1);
+        }
+        for (int s = 0; s < L::kNR; ++s) {
+            mbar_init(&aux->raw_full[s], 32);
+            mbar_init(&aux->raw_empty[s], 8);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&aux->s_full[b], 1);
@@ -244,8 +418,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         fence_mbarrier_init();
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmq);
-        tma_prefetch_desc(&tmk);
-        tma_prefetch_desc(&tmv);
+        if (!KV) {
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+        }
     }
     if (warp == 1) tmem_alloc(&aux->tmem_base, L::kTmemCols);
     tc_fence_before();
@@ -265,19 +441,35 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 tma_load_3d(sQ + c * (kM * 128), &tmq, c * 64, kvh * G, ri.row0, &aux->q_full);
         }
         __syncwarp();
-        const int issued = produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK, aux->k_full,
-                                                        aux->k_empty, aux->list_k, aux, &tmk, abort, lane);
-        if (*abort && lane == 0) {
-            drain_copies<NK>(aux->k_full, issued);
-            atomicOr(p.status, kDevWaitTimeout);
+        if constexpr (KV) {
+            produce_raw<D>(p, r, kvh, key_lo, key_hi, T, sRaw, aux, abort, lane);
+            if (*abort && lane == 0) atomicOr(p.status, kDevWaitTimeout);
+        } else {
+            const int issued = produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK, aux->k_full,
+                                                            aux->k_empty, aux->list_k, aux, &tmk, abort, lane);
+            if (*abort && lane == 0) {
+                drain_copies<NK>(aux->k_full, issued);
+                atomicOr(p.status, kDevWaitTimeout);
+            }
         }
         __syncwarp();
     } else if (warp == 2) {
-        // ------------------------------------------------------------ V producer
-        const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
-                                                       aux->v_empty, aux->list_v, aux, &tmv, abort, lane);
-        if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
+        // ------------------------------------------------------------ V producer (bf16)
+        if constexpr (!KV) {
+            const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
+                                                           aux->v_empty, aux->list_v, aux, &tmv, abort, lane);
+            if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
+        }
         __syncwarp();
+    } else if (KV && warp >= 8) {
+        // ------------------------------------------------------------ NVFP4 dequant (K: 8-11, V: 12-15)
+        // e4m3 -> bf16 table for the block scales, from the format definition
+        sLut[tid - 256] = __bfloat16_as_ushort(__float2bfloat16_rn(e4m3_to_float(static_cast<uint32_t>(tid - 256))));
+        asm volatile("bar.sync 1, 256;" ::: "memory");   // the two dequant warpgroups only
+        if (warp < 12)
+            dequant<D, false, TRACE>(p, key_lo, key_hi, T, sRaw, sK, sLut, aux, abort, tid - 256);
+        else
+            dequant<D, true, TRACE>(p, key_lo, key_hi, T, sRaw, sV, sLut, aux, abort, tid - 384);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // Issues S_t = Q K_t^T and O += P_t V_t in whichever order their inputs
@@ -383,23 +575,32 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
 
             const int key0 = key_lo + t * kBN;
             const int lim = valid ? (min(key_hi - 1, hi) - key0) : -1;  // visible iff c <= lim
-            float mx = -INFINITY;
+            // Scores stay unscaled: the maximum is taken on raw scores (sc > 0) and
+            // the scale is folded into one FFMA per exponent.  Tiles whose keys
+            // are all visible to every row of the warp skip the mask.
+            float mraw = -INFINITY;
+            if (__all_sync(kFullMask, lim >= kBN - 1)) {
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                const float x = (c <= lim) ? sv[c] * sc : -INFINITY;
-                sv[c] = x;
-                mx = fmaxf(mx, x);
+                for (int c = 0; c < kBN; ++c) mraw = fmaxf(mraw, sv[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    if (c > lim) sv[c] = -INFINITY;
+                    mraw = fmaxf(mraw, sv[c]);
+                }
             }
+            const float mx = mraw * sc;
             const bool need = (m_ref != -INFINITY) && (mx > m_ref + kRescaleThreshold);
             const bool first = (m_ref == -INFINITY) && (mx != -INFINITY);
             const float ref = (need || first) ? mx : m_ref;
             const float alpha = need ? fast_exp2(m_ref - ref) : 1.f;
             uint32_t pk[kBN / 2];
             float psum = 0.f;
+            const float nref = (ref == -INFINITY) ? 0.f : -ref;   // masked scores are -inf -> p = 0
 #pragma unroll
             for (int c = 0; c < kBN; c += 2) {
-                const float p0 = (c <= lim) ? fast_exp2(sv[c] - ref) : 0.f;
-                const float p1 = (c + 1 <= lim) ? fast_exp2(sv[c + 1] - ref) : 0.f;
+                const float p0 = fast_exp2(fmaf(sv[c], sc, nref));
+                const float p1 = fast_exp2(fmaf(sv[c + 1], sc, nref));
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                 // the normaliser sums the fp32 weights: rounding P to bf16 for
                 // the PV MMA must not leak into l (and so into LSE) on rows
@@ -430,7 +631,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             const int vs = t % NV;
             // The request's last page may end mid-page: its stale slots hold
             // arbitrary (even non-finite) values and 0 * NaN is NaN, so zero them.
-            const bool ragged_tail = key_hi == ri.len && t == T - 1 && (ri.len & 15) != 0;
+            // (NVFP4 tiles come out of the dequant already zeroed past key_hi)
+            const bool ragged_tail = !KV && key_hi == ri.len && t == T - 1 && (ri.len & 15) != 0;
             if (ragged_tail || TRACE) {
                 if (!(ok = warp_wait(&aux->v_full[vs], (t / NV) & 1, abort))) break;
             }
@@ -543,28 +745,34 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
 
 using TcKernel = void (*)(const SplitParams, const CUtensorMap, const CUtensorMap, const CUtensorMap);
 
-template <int D>
+template <int D, int KV>
 TcKernel pick_trace(bool traced) {
-    return traced ? &split_attn_tc_kernel<D, true> : &split_attn_tc_kernel<D, false>;
+    return traced ? &split_attn_tc_kernel<D, KV, true> : &split_attn_tc_kernel<D, KV, false>;
 }
 
-TcKernel pick(int d, bool traced) {
+template <int KV>
+TcKernel pick_d(int d, bool traced) {
     switch (d) {
-        case 64: return pick_trace<64>(traced);
-        case 128: return pick_trace<128>(traced);
-        case 256: return pick_trace<256>(traced);
+        case 64: return pick_trace<64, KV>(traced);
+        case 128: return pick_trace<128, KV>(traced);
+        case 256: return pick_trace<256, KV>(traced);
         default: return nullptr;
     }
 }
 
-int smem_for(int d) {
+TcKernel pick(int d, int kv, bool traced) { return kv ? pick_d<1>(d, traced) : pick_d<0>(d, traced); }
+
+template <int KV>
+int smem_d(int d) {
     switch (d) {
-        case 64: return TcLayout<64>::kSmem;
-        case 128: return TcLayout<128>::kSmem;
-        case 256: return TcLayout<256>::kSmem;
+        case 64: return TcLayout<64, KV>::kSmem;
+        case 128: return TcLayout<128, KV>::kSmem;
+        case 256: return TcLayout<256, KV>::kSmem;
         default: return 0;
     }
 }
+
+int smem_for(int d, int kv) { return kv ? smem_d<1>(d) : smem_d<0>(d); }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -627,38 +835,46 @@ bool encode_q_map(CUtensorMap* map, const void* q, int total_rows, int hq, int d
 }  // namespace
 
 bool tc_supported(int head_dim, int kv_dtype, int max_rows) {
-    return kv_dtype == 0 && max_rows <= kM && (head_dim == 64 || head_dim == 128 || head_dim == 256);
+    return (kv_dtype == 0 || kv_dtype == 1) && max_rows <= kM && (head_dim == 64 || head_dim == 128 || head_dim == 256);
 }
 
-int tc_smem_bytes(int head_dim) { return smem_for(head_dim); }
-int tc_threads() { return kTcThreads; }
+int tc_smem_bytes(int head_dim, int kv_dtype) { return smem_for(head_dim, kv_dtype); }
+int tc_threads(int kv_dtype) { return kv_dtype ? kTcThreadsFp4 : kTcThreadsBf16; }
 
-cudaError_t tc_prepare(int head_dim) {
+cudaError_t tc_prepare(int head_dim, int kv_dtype) {
     for (int traced = 0; traced < 2; ++traced) {
-        TcKernel k = pick(head_dim, traced != 0);
+        TcKernel k = pick(head_dim, kv_dtype, traced != 0);
         if (!k) return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_for(head_dim));
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem_for(head_dim, kv_dtype));
         if (e != cudaSuccess) return e;
     }
     return encode_fn() ? cudaSuccess : cudaErrorNotSupported;
 }
 
-bool tc_encode_maps(const SplitParams& p, TcMaps* maps) {
+bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
     static_assert(sizeof(CUtensorMap) == sizeof(maps->q), "tensor map size");
-    return encode_q_map(reinterpret_cast<CUtensorMap*>(maps->q), p.q, p.total_rows, p.num_q_heads, p.head_dim,
-                        p.group, p.max_w) &&
-           encode_pool_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
+    if (!encode_q_map(reinterpret_cast<CUtensorMap*>(maps->q), p.q, p.total_rows, p.num_q_heads, p.head_dim,
+                      p.group, p.max_w))
+        return false;
+    if (kv_dtype != 0) {   // NVFP4 pools are read with cp.async, not TMA
+        memset(maps->k, 0, sizeof(maps->k));
+        memset(maps->v, 0, sizeof(maps->v));
+        return true;
+    }
+    return encode_pool_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
                            p.head_dim) &&
            encode_pool_map_pages(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,
                                  p.head_dim);
 }
 
-cudaError_t tc_launch(const SplitParams& p, const TcMaps& maps, bool traced, dim3 grid, cudaStream_t stream) {
-    TcKernel k = pick(p.head_dim, traced);
+cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bool traced, dim3 grid,
+                      cudaStream_t stream) {
+    TcKernel k = pick(p.head_dim, kv_dtype, traced);
     if (!k) return cudaErrorInvalidValue;
-    k<<<grid, kTcThreads, smem_for(p.head_dim), stream>>>(p, *reinterpret_cast<const CUtensorMap*>(maps.q),
-                                                           *reinterpret_cast<const CUtensorMap*>(maps.k),
-                                                           *reinterpret_cast<const CUtensorMap*>(maps.v));
+    k<<<grid, tc_threads(kv_dtype), smem_for(p.head_dim, kv_dtype), stream>>>(
+        p, *reinterpret_cast<const CUtensorMap*>(maps.q), *reinterpret_cast<const CUtensorMap*>(maps.k),
+        *reinterpret_cast<const CUtensorMap*>(maps.v));
     return cudaGetLastError();
 }
 
