@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--only", default=None,
                     help="profiling mode: run this named workload (see workloads.NAMED) --calls times, untimed")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--write-traffic", default=None, metavar="NCU_CSV",
+                    help="write profiles/split_attn_traffic.json from an ncu --csv log of "
+                         "dram__bytes_read.sum/dram__bytes_write.sum over split_attn launches")
     return ap.parse_args()
 
 
@@ -271,6 +274,24 @@ def e2e_step(dws, host, stream):
         h["lse"].copy_(dw.lse, non_blocking=True)
 
 
+def max_over_ranks(values, world, device):
+    """Max of each per-rank time over all ranks (every rank gets the result);
+    the replicas' job time is the slowest replica's."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return [float(v) for v in t.tolist()]
+
+
+def job_gbs(bytes_per_rank, ms, world):
+    """Whole-job KV GB/s: every replica reads bytes_per_rank in `ms` (the max over ranks)."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import speculative_decode_verify_paged_gb300 as sa
@@ -300,12 +321,8 @@ def run_ours(args, rank, world, local_rank):
     step_ms = statistics.mean(per_step)
     dirty_step, _ = time_calls(dws, flush, max(5, args.steps // 2), 3, stream, clean=False)
     dirty_ms = statistics.mean(dirty_step)
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-        torch.distributed.barrier()
-    value = world * sum(kv_bytes) / (step_ms * 1e-3) / 1e9
+    step_ms, dirty_ms = max_over_ranks([step_ms, dirty_ms], world, dev)
+    value = job_gbs(sum(kv_bytes), step_ms, world)
 
     # per-call medians (graph replay and eager) and the split kernel alone
     # (timing events captured around its launch)
@@ -377,8 +394,8 @@ def run_ours(args, rank, world, local_rank):
         s1.synchronize()
         if it >= 3:
             e2e_times.append(s0.elapsed_time(s1))
-    e2e_ms = statistics.mean(e2e_times)
-    e2e = {"value": round(world * sum(kv_bytes) / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    e2e_ms, = max_over_ranks([statistics.mean(e2e_times)], world, dev)
+    e2e = {"value": round(job_gbs(sum(kv_bytes), e2e_ms, world), 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     cpu = None
@@ -403,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
                        "us_per_call": {c["workload"]: c["us"] for c in per_call},
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_peak": round(100 * value / world / peak, 1),
-            "value_dirty_l2_flush": round(world * sum(kv_bytes) / (dirty_ms * 1e-3) / 1e9, 1),
+            "value_dirty_l2_flush": round(job_gbs(sum(kv_bytes), dirty_ms, world), 1),
             "per_call": per_call,
             "table": table,
             "roofline": roofline,
@@ -416,25 +433,58 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_only(args):
-    """Profiling driver: plan once, then `--calls` layer calls of one named workload."""
+    """Profiling driver: plan once, then `--calls` layer calls of one named
+    workload ("main" = the three calls of the main step, in step order)."""
     import torch
     import speculative_decode_verify_paged_gb300 as sa
     from speculative_decode_verify_paged_gb300 import build as libbuild
     from speculative_decode_verify_paged_gb300 import workloads as W
 
     libbuild.build()
-    wl = W.NAMED[args.only]()
-    dw = sa.DeviceWorkload(wl, "cuda", kernel_variant=args.variant)
+    names = ["verify_sweep_w1", "verify_sweep_w8", "verify_sweep_w16"] if args.only == "main" else [args.only]
+    wls = [W.NAMED[n]() for n in names]
+    dws = [sa.DeviceWorkload(wl, "cuda", kernel_variant=args.variant) for wl in wls]
     for _ in range(args.calls):
-        dw.run()
+        for dw in dws:
+            dw.run()
     torch.cuda.synchronize()
-    assert dw.device_status() == 0
-    print(json.dumps({"workload": args.only, "calls": args.calls, "kv_bytes": wl.kv_bytes,
-                      "plan": dw.plan.info}))
+    for dw in dws:
+        assert dw.device_status() == 0
+    print(json.dumps({"workload": args.only, "calls": args.calls,
+                      "kv_bytes": [wl.kv_bytes for wl in wls], "plan": [dw.plan.info for dw in dws]}))
+
+
+def write_traffic(csv_path, out_path=None):
+    """Per-launch DRAM bytes (read + write) of the split kernel, averaged over
+    the launches an ncu --csv capture holds, stamped with the kernel-source hash
+    so that bench.py reports it only while the kernel is unchanged."""
+    import csv
+    per = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(l for l in f if l.startswith('"'))]
+    hdr = rows[0]
+    ki, mi, vi, ii = (hdr.index(k) for k in ("Kernel Name", "Metric Name", "Metric Value", "ID"))
+    for r in rows[1:]:
+        if "split_attn" not in r[ki] or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        per[r[ii]] = per.get(r[ii], 0) + float(r[vi].replace(",", ""))
+    if not per:
+        raise SystemExit(f"no split_attn dram byte counts in {csv_path}")
+    out = {"kernel_source_hash": kernel_source_hash(),
+           "dram_bytes_per_launch": round(sum(per.values()) / len(per)),
+           "launches": len(per), "per_launch": [round(v) for v in per.values()],
+           "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none "
+                     "-k regex:split_attn -c 6 --csv python bench.py --only main --calls 2"}
+    with open(out_path or os.path.join(ROOT, "profiles", "split_attn_traffic.json"), "w") as f:
+        json.dump(out, f, indent=1)
+    print(json.dumps(out))
 
 
 def main():
     args = parse()
+    if args.write_traffic:
+        write_traffic(args.write_traffic)
+        return
     if args.only:
         run_only(args)
         return
