@@ -193,17 +193,22 @@ def committed_traffic():
 
 
 class Captured:
-    """One DeviceWorkload's spec_attn_run captured in a CUDA graph."""
+    """Layer calls (spec_attn_run of several DeviceWorkloads, in order)
+    captured in one CUDA graph, as a model's decode step captures its layers:
+    inside it each call's kernels follow the previous call's as programmatic
+    dependents."""
 
-    def __init__(self, dw, stream):
+    def __init__(self, dws, stream):
         import torch
-        self.dw = dw
-        dw.run(stream)                       # warm: TMA descriptors cached in the plan
+        self.dws = dws
+        for dw in dws:
+            dw.run(stream)                   # warm: TMA descriptors cached in the plan
         torch.cuda.synchronize()
         cap = torch.cuda.Stream()            # capture needs a non-default stream
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, stream=cap):
-            dw.run(cap)
+            for dw in dws:
+                dw.run(cap)
         torch.cuda.synchronize()
 
     def replay(self):
@@ -223,8 +228,9 @@ def flush_l2(flush, clean=True):
 def time_calls(dws, flush, steps, warmup, stream, timing_events=False, graphs=True, clean=True):
     """Per-step device time (ms) of one call per DeviceWorkload, L2 flushed (a
     2 x L2 write) before each step, outside the timed events.  With graphs=True
-    each call is a CUDA-graph replay, so the host never starves the GPU inside
-    the timed region; returns (per-step ms list, mean split-kernel ms per call)."""
+    the step's calls are one CUDA-graph replay, so the host never starves the
+    GPU inside the timed region; returns (per-step ms list, mean split-kernel
+    ms per call)."""
     import torch
     if timing_events:
         graphs = False   # events recorded inside a graph can not be timed; run eagerly
@@ -235,7 +241,7 @@ def time_calls(dws, flush, steps, warmup, stream, timing_events=False, graphs=Tr
             e.record(stream)
             dw._timing = (b, e)
             dw.plan.set_timing_events(b, e)
-    caps = [Captured(dw, stream) for dw in dws] if graphs else None
+    cap = Captured(dws, stream) if graphs else None
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     per_step, split_ms = [], [0.0] * len(dws)
@@ -245,10 +251,10 @@ def time_calls(dws, flush, steps, warmup, stream, timing_events=False, graphs=Tr
         # falls inside the timed events (outside the timed region)
         torch.cuda._sleep(200000)
         start.record(stream)
-        for k, dw in enumerate(dws):
-            if graphs:
-                caps[k].replay()
-            else:
+        if graphs:
+            cap.replay()
+        else:
+            for dw in dws:
                 dw.run(stream)
         end.record(stream)
         if it >= warmup:
@@ -416,7 +422,7 @@ def run_ours(args, rank, world, local_rank):
             "data": "synthetic (seeded N(0,1), bf16)",
             "config": {"workload": MAIN_WORKLOAD, "calls_per_step": len(dws),
                        "kv_bytes_per_step": sum(kv_bytes), "l2": "flushed before every step, untimed: write of a 2 x L2 buffer, then read of a second one (clean L2); value_dirty_l2_flush = write only",
-                       "timing": "CUDA events around CUDA-graph replays of spec_attn_run (device time); us_eager in per_call",
+                       "timing": "CUDA events around one CUDA-graph replay of the step's three spec_attn_run calls (device time); per_call: each call alone in its own graph, and us_eager",
                        "us_per_call": {c["workload"]: c["us"] for c in per_call},
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_peak": round(100 * value / world / peak, 1),

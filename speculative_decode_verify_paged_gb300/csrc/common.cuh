@@ -65,15 +65,16 @@ __device__ __forceinline__ bool load_request(const int32_t* seq_lens, const int3
                                              long long max_seq_len, int cap_keys,
                                              int keys_per_split, unsigned int* status,
                                              ReqInfo& ri) {
+    // three independent loads: one memory round trip
     const int row0 = q_indptr[r];
     const int row1 = q_indptr[r + 1];
+    const int len = seq_lens[r];
     const int w = row1 - row0;
     if (w < 0 || w > max_w || row0 < 0 || row1 > total_rows) {
         if (status) atomicOr(status, kDevBadWindow);
         return false;
     }
     if (w == 0) return false;
-    const int len = seq_lens[r];
     if (len < w || (long long)len > max_seq_len || len > cap_keys) {
         if (status) atomicOr(status, kDevBadSeqLen);
         return false;

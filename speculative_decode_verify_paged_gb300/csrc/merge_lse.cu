@@ -19,7 +19,8 @@
 // shared memory.  Requests with a single split were finished by the split
 // kernel and are skipped.  The kernel may be launched as a programmatic
 // dependent of the split kernel: it waits on griddepcontrol before touching
-// partials.
+// partials, and it lets the next kernel in the stream launch early (that
+// kernel waits for this grid's completion before reading its outputs).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,6 +38,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
     __shared__ float4 part[kMergeThreads][2];
     __shared__ float part_m[kMergeThreads], part_l[kMergeThreads];
     const int tid = threadIdx.x;
+    pdl_launch_dependents();
     const int tpp = VEC * sg;                    // threads per pair
     const int ppc = kMergeThreads / tpp;         // pairs per CTA
     const int lp = tid / tpp, within = tid % tpp;
@@ -59,6 +61,8 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
     if (active) {
         oi = (size_t)(ri.row0 + i) * p.num_q_heads + h;
         const size_t split_stride = (size_t)p.total_rows * p.num_q_heads;
+        const size_t pair0 = partial_pair(0, p.total_rows, p.num_q_heads, p.group, h / p.group, ri.row0 + i,
+                                          h % p.group);
         const int n = ri.nsplits;
         for (int s0 = g; s0 < n; s0 += sg * kBatch) {
             float ls[kBatch];
@@ -67,8 +71,8 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
             for (int k = 0; k < kBatch; ++k) {
                 const int s = s0 + k * sg;
                 if (s < n) {
-                    ls[k] = p.ws_lse[s * split_stride + oi];
-                    const float* src = p.ws_o + (s * split_stride + oi) * D + v * 8;
+                    ls[k] = p.ws_lse[s * split_stride + pair0];
+                    const float* src = p.ws_o + (s * split_stride + pair0) * D + v * 8;
                     o0[k] = *reinterpret_cast<const float4*>(src);
                     o1[k] = *reinterpret_cast<const float4*>(src + 4);
                 } else {

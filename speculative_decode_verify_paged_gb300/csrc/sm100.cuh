@@ -119,6 +119,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// 16-byte shared load by 32-bit shared address (no generic-address aliasing
+// with the global stores that follow, so loads can run ahead of them).
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+__device__ __forceinline__ void st_global_v4(void* gaddr, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Allocate `ncols` (power of two >= 32) TMEM columns; the base address is
 // written to shared memory at `dst`.  Whole warp.

@@ -407,10 +407,10 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
-        e = tc_launch(sp, p.kv_dtype, mp->maps, trace != nullptr, plan->grid, stream);
+        e = tc_launch(sp, p.kv_dtype, mp->maps, trace != nullptr, plan->grid, stream, plan->ev_begin == nullptr);
         maps_lock.unlock();
     } else
-        e = cc_launch(sp, p.kv_dtype, plan->cc, trace != nullptr, plan->grid, stream);
+        e = cc_launch(sp, p.kv_dtype, plan->cc, trace != nullptr, plan->grid, stream, plan->ev_begin == nullptr);
     if (e != cudaSuccess) return cuda_fail(e);
     if (plan->ev_end) {
         e = cudaEventRecord(plan->ev_end, stream);
@@ -429,6 +429,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         mp.total_rows = p.total_q_rows;
         mp.max_w = p.max_w;
         mp.num_q_heads = p.num_q_heads;
+        mp.group = p.num_q_heads / p.num_kv_heads;
         mp.head_dim = p.head_dim;
         mp.keys_per_split = plan->keys_per_split;
         mp.max_splits = plan->max_splits;

@@ -21,8 +21,8 @@ struct SplitParams {
     uint16_t* o;                // [total_rows, Hq, d] bf16 bits
     float* lse;                 // [total_rows, Hq] or nullptr
     long long* trace;           // [total_rows, Hq, 2] or nullptr
-    float* ws_o;                // [max_splits, total_rows, Hq, d] fp32 partials
-    float* ws_lse;              // [max_splits, total_rows, Hq] fp32 partial LSE (log2 units)
+    float* ws_o;                // fp32 partials, (row, head) pairs ordered by partial_pair()
+    float* ws_lse;              // fp32 partial LSE (log2 units), same pair order
     unsigned int* status;       // sticky device-status word
     int num_reqs;
     int total_rows;
@@ -55,12 +55,22 @@ struct MergeParams {
     int total_rows;
     int max_w;
     int num_q_heads;
+    int group;                  // Hq / Hkv
     int head_dim;
     int keys_per_split;
     int max_splits;
     long long max_seq_len;
     int bt_capacity_keys;       // bt_stride * page_size
 };
+
+// Order of the (window row, query head) pairs in the split partials: split-major,
+// then KV head, then window row, then the G query heads of that KV head.  The
+// pairs one split CTA produces (one KV head, consecutive window rows) are one
+// contiguous block, so its epilogue writes a single dense run of memory.
+__host__ __device__ __forceinline__ size_t partial_pair(int split, int total_rows, int num_q_heads, int group,
+                                                        int kvh, int row, int g) {
+    return (size_t)split * total_rows * num_q_heads + ((size_t)kvh * total_rows + row) * group + g;
+}
 
 // Device-status bits (mirror the public SPEC_ATTN_DEV_* values).
 constexpr unsigned int kDevBadPage = 0x1u;
@@ -78,8 +88,10 @@ struct CcConfig {
 CcConfig cc_config(int head_dim, int kv_dtype, int max_rows);
 // Prepare (max dynamic smem attribute) the instance a config uses; returns a CUDA error code.
 cudaError_t cc_prepare(int head_dim, int kv_dtype, const CcConfig& cfg);
+// programmatic: launch as a programmatic dependent of the previous kernel in the
+// stream (the kernel waits on griddepcontrol before its first global access).
 cudaError_t cc_launch(const SplitParams& p, int kv_dtype, const CcConfig& cfg, bool traced,
-                      dim3 grid, cudaStream_t stream);
+                      dim3 grid, cudaStream_t stream, bool programmatic);
 
 // ---- tcgen05 split-KV kernel (split_attn_tc.cu) ----
 // TMA descriptors of one (Q, K pool, V pool) triple; opaque CUtensorMap storage.
@@ -94,7 +106,7 @@ int tc_threads(int kv_dtype);
 cudaError_t tc_prepare(int head_dim, int kv_dtype);
 bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps);
 cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bool traced, dim3 grid,
-                      cudaStream_t stream);
+                      cudaStream_t stream, bool programmatic);
 
 // ---- LSE merge (merge_lse.cu) ----
 cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic);

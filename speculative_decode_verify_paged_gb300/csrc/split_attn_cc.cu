@@ -146,6 +146,9 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
     const int kvh = blockIdx.y;
     const int r = blockIdx.z;
 
+    // launched as a programmatic dependent: nothing global is touched before
+    // the previous kernel in the stream has completed
+    pdl_wait_primary();
     ReqInfo ri;
     const bool reporter = (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0);
     if (!load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
@@ -327,11 +330,12 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
             }
             if (p.lse && lane == 0) p.lse[oi] = lse2 * kLn2;
         } else {
-            float* wp = p.ws_o + ((size_t)split * p.total_rows * p.num_q_heads + oi) * D + lane * DPL;
+            const size_t pi = partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, qrow[t], hq[t] - kvh * G);
+            float* wp = p.ws_o + pi * D + lane * DPL;
 #pragma unroll
             for (int e = 0; e < DPL; e += 2)
                 *reinterpret_cast<float2*>(wp + e) = make_float2(o_acc[t][e] * inv_l, o_acc[t][e + 1] * inv_l);
-            if (lane == 0) p.ws_lse[(size_t)split * p.total_rows * p.num_q_heads + oi] = lse2;
+            if (lane == 0) p.ws_lse[pi] = lse2;
         }
     }
 }
@@ -398,11 +402,20 @@ cudaError_t cc_prepare(int head_dim, int kv_dtype, const CcConfig& cfg) {
 }
 
 cudaError_t cc_launch(const SplitParams& p, int kv_dtype, const CcConfig& cfg, bool traced,
-                      dim3 grid, cudaStream_t stream) {
+                      dim3 grid, cudaStream_t stream, bool programmatic) {
     CcKernel k = pick(p.head_dim, kv_dtype, cfg.rows_per_warp, traced);
     if (!k) return cudaErrorInvalidValue;
-    k<<<grid, cfg.threads, cfg.smem_bytes, stream>>>(p, cfg.stages);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(cfg.threads, 1, 1);
+    lc.dynamicSmemBytes = cfg.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, k, p, cfg.stages);
 }
 
 }  // namespace spec_attn

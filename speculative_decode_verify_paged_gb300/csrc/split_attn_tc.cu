@@ -59,7 +59,7 @@ constexpr int kTcThreadsFp4 = 512;    // + warps 8-11 (K dequant) and 12-15 (V d
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM cycles
 constexpr long long kDrainLimit = 200000000LL;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units: rescale when max grows by > 2^8
-constexpr int kPageListCap = 64;                 // page ids staged in shared memory at a time
+constexpr int kPageListCap = 64;                 // page ids staged in shared memory at a time (2 per lane)
 constexpr int kMaxNR = 8;                        // NVFP4 raw (codes + scales) ring slots
 constexpr int kMaxNK = 8, kMaxNV = 16;
 
@@ -152,23 +152,27 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <int D, int NSLOT, bool IS_V, bool TRACE>
 __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
                                        unsigned char* ring, uint64_t* full, uint64_t* empty, int32_t* list,
-                                       TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane) {
+                                       TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane,
+                                       int pre0, int pre1) {
     using L = TcLayout<D, 0>;
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride + key_lo / 16;
     const int n_pages = (key_hi - key_lo + 15) / 16;
     int list_base = 0;
-    auto fill_list = [&](int base) {
-        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) {
-            int pg = bt[base + i];
-            if (pg < 0 || pg >= p.num_pages) {
-                if (!IS_V) atomicOr(p.status, kDevBadPage);
-                pg = 0;
-            }
-            list[i] = pg;
+    auto checked = [&](int pg) {
+        if (pg < 0 || pg >= p.num_pages) {
+            if (!IS_V) atomicOr(p.status, kDevBadPage);
+            pg = 0;
         }
+        return pg;
+    };
+    auto fill_list = [&](int base) {
+        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) list[i] = checked(bt[base + i]);
         __syncwarp();
     };
-    fill_list(0);
+    // the first 64 entries were fetched at kernel start
+    if (lane < n_pages) list[lane] = checked(pre0);
+    if (lane + 32 < n_pages) list[lane + 32] = checked(pre1);
+    __syncwarp();
     int issued = 0;
     for (int t = 0; t < T; ++t) {
         const int slot = t % NSLOT;
@@ -179,22 +183,26 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
             list_base = rel;
             fill_list(list_base);
         }
-        if (lane == 0) {
-            const int np = min(kPPT, (key_hi - (key_lo + t * kBN) + 15) / 16);
-            unsigned char* dst = ring + slot * L::kTileBytes;
-            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(np * L::kChunks * 2048));
-            for (int pp = 0; pp < np; ++pp) {
-                const int pg = list[rel - list_base + pp];
-                if (TRACE && IS_V) aux->pages_v[slot][pp] = pg;
-                if (IS_V) {
-                    // whole page-head in one copy: [chunk][16 slots][128 B], page after page
-                    tma_load_5d(dst + pp * L::kPageBytes, tm, 0, 0, 0, kvh, pg, &full[slot]);
-                } else {
-                    // chunk-major across the tile's pages, so S = Q K^T spans the tile in one MMA
-                    for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_4d(dst + c * (kBN * 128) + pp * 2048, tm, c * 64, 0, kvh, pg, &full[slot]);
-                }
+        // The copies of a tile are issued by several lanes at once (a copy's
+        // issue takes a while; one lane issuing them all in turn would add
+        // that time to every tile's latency).
+        const int np = min(kPPT, (key_hi - (key_lo + t * kBN) + 15) / 16);
+        unsigned char* dst = ring + slot * L::kTileBytes;
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(np * L::kChunks * 2048));
+        __syncwarp();
+        if (IS_V) {
+            // lane pp: the whole page-head pp in one copy, [chunk][16 slots][128 B]
+            if (lane < np) {
+                const int pg = list[rel - list_base + lane];
+                if (TRACE) aux->pages_v[slot][lane] = pg;
+                tma_load_5d(dst + lane * L::kPageBytes, tm, 0, 0, 0, kvh, pg, &full[slot]);
             }
+        } else if (lane < np * L::kChunks) {
+            // lane (pp, c): chunk c of page pp, chunk-major across the tile's
+            // pages so that S = Q K^T spans the tile in one MMA
+            const int pp = lane / L::kChunks, c = lane % L::kChunks;
+            const int pg = list[rel - list_base + pp];
+            tma_load_4d(dst + c * (kBN * 128) + pp * 2048, tm, c * 64, 0, kvh, pg, &full[slot]);
         }
         __syncwarp();
         issued = t + 1;
@@ -216,25 +224,29 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 template <int D>
 __device__ __forceinline__ void produce_raw(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
-                                            unsigned char* raw, TcAux* aux, volatile int* abort, int lane) {
+                                            unsigned char* raw, TcAux* aux, volatile int* abort, int lane,
+                                            int pre0, int pre1) {
     using L = TcLayout<D, 1>;
     constexpr int NR = L::kNR;
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride + key_lo / 16;
     const int n_pages = (key_hi - key_lo + 15) / 16;
     int32_t* list = aux->list_k;
     int list_base = 0;
-    auto fill_list = [&](int base) {
-        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) {
-            int pg = bt[base + i];
-            if (pg < 0 || pg >= p.num_pages) {
-                atomicOr(p.status, kDevBadPage);
-                pg = 0;
-            }
-            list[i] = pg;
+    auto checked = [&](int pg) {
+        if (pg < 0 || pg >= p.num_pages) {
+            atomicOr(p.status, kDevBadPage);
+            pg = 0;
         }
+        return pg;
+    };
+    auto fill_list = [&](int base) {
+        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) list[i] = checked(bt[base + i]);
         __syncwarp();
     };
-    fill_list(0);
+    // the first 64 entries were fetched at kernel start
+    if (lane < n_pages) list[lane] = checked(pre0);
+    if (lane + 32 < n_pages) list[lane + 32] = checked(pre1);
+    __syncwarp();
     const unsigned char* kc_pool = static_cast<const unsigned char*>(p.k_pool);
     const unsigned char* vc_pool = static_cast<const unsigned char*>(p.v_pool);
     for (int t = 0; t < T; ++t) {
@@ -365,18 +377,6 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
 
-    ReqInfo ri;
-    const bool reporter = (tid == 0 && split == 0 && kvh == 0);
-    if (!load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
-                      p.bt_stride * 16, p.keys_per_split, reporter ? p.status : nullptr, ri))
-        return;
-    if (split >= ri.nsplits) return;
-    const int G = p.group;
-    const int R = ri.w * G;  // <= 128: the plan admits this kernel only when max_w * G <= 128
-    const int key_lo = split * p.keys_per_split;
-    const int key_hi = min(key_lo + p.keys_per_split, ri.len);
-    const int T = (key_hi - key_lo + kBN - 1) / kBN;
-
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -429,6 +429,35 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     tc_fence_after();
     const uint32_t tmem = aux->tmem_base;
 
+    // Up to here the CTA touched only its own resources (and the kernel
+    // parameters), which lets it start while the previous kernel in the stream
+    // drains; from here on it reads what that kernel may have written.
+    pdl_wait_primary();
+    const int key_lo = split * p.keys_per_split;
+    // The split's first block-table entries sit at a fixed place, so the
+    // producers fetch them in the same memory round trip as the request's
+    // window and length (entries past the request's pages are never used).
+    int pre0 = -1, pre1 = -1;
+    if ((warp == 0 || (!KV && warp == 2)) && r < p.num_reqs) {
+        const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
+        const int i0 = key_lo / 16 + lane;
+        if (i0 < p.bt_stride) pre0 = bt[i0];
+        if (i0 + 32 < p.bt_stride) pre1 = bt[i0 + 32];
+    }
+    ReqInfo ri;
+    const bool reporter = (tid == 0 && split == 0 && kvh == 0);
+    const bool active = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
+                                     p.bt_stride * 16, p.keys_per_split, reporter ? p.status : nullptr, ri) &&
+                        split < ri.nsplits;
+    if (!active) {   // uniform across the CTA
+        if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
+        return;
+    }
+    const int G = p.group;
+    const int R = ri.w * G;  // <= 128: the plan admits this kernel only when max_w * G <= 128
+    const int key_hi = min(key_lo + p.keys_per_split, ri.len);
+    const int T = (key_hi - key_lo + kBN - 1) / kBN;
+
     if (warp == 0) {
         // ------------------------------------------------------------ query tile + K producer
         if (lane == 0) {
@@ -442,11 +471,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         }
         __syncwarp();
         if constexpr (KV) {
-            produce_raw<D>(p, r, kvh, key_lo, key_hi, T, sRaw, aux, abort, lane);
+            produce_raw<D>(p, r, kvh, key_lo, key_hi, T, sRaw, aux, abort, lane, pre0, pre1);
             if (*abort && lane == 0) atomicOr(p.status, kDevWaitTimeout);
         } else {
             const int issued = produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK, aux->k_full,
-                                                            aux->k_empty, aux->list_k, aux, &tmk, abort, lane);
+                                                            aux->k_empty, aux->list_k, aux, &tmk, abort, lane,
+                                                            pre0, pre1);
             if (*abort && lane == 0) {
                 drain_copies<NK>(aux->k_full, issued);
                 atomicOr(p.status, kDevWaitTimeout);
@@ -457,7 +487,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         // ------------------------------------------------------------ V producer (bf16)
         if constexpr (!KV) {
             const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
-                                                           aux->v_empty, aux->list_v, aux, &tmv, abort, lane);
+                                                           aux->v_empty, aux->list_v, aux, &tmv, abort, lane,
+                                                           pre0, pre1);
             if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
         }
         __syncwarp();
@@ -672,63 +703,56 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         if (ok) ok = warp_wait(&aux->o_final, 0, abort);
         tc_fence_after();
         if (ok) {
-            // Epilogue.  Every MMA and copy has completed (o_final), so the query,
-            // P and ring buffers are free: each warp stages its 32 rows of O / l
-            // there (row stride padded by 16 bytes: conflict-free 16-byte stores),
-            // then copies them out row by row with coalesced 512-byte stores.
+            // Every MMA and copy has completed (o_final), so the query, P and
+            // ring buffers are free: each thread stages its row of the
+            // normalised O there (bf16 output, or the fp32 partial), row stride
+            // padded by 16 bytes so the 16-byte stores of a warp hit distinct
+            // banks.  All warps copy the rows out below.
             const float inv = (valid && l_sum > 0.f) ? (p.out_scale / l_sum) : 0.f;
             const float lse2 = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) : -INFINITY;
-            const size_t oi = (size_t)qrow * p.num_q_heads + hq;
             const bool final_out = (ri.nsplits == 1);
-            const int row_bytes = final_out ? D * 2 : D * 4;
-            const int rs = row_bytes + 16;
-            unsigned char* stg = smem;
-            unsigned char* myrow = stg + m * rs;
+            const int rs = (final_out ? D * 2 : D * 4) + 16;
+            unsigned char* myrow = smem + m * rs;
+            // two 32-column TMEM loads in flight per wait
 #pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-                float ov[32];
-                tmem_ld32(lane_tmem + ch * 32, ov);
+            for (int ch0 = 0; ch0 < D / 32; ch0 += 2) {
+                float ov[2][32];
+                tmem_ld32(lane_tmem + ch0 * 32, ov[0]);
+                tmem_ld32(lane_tmem + (ch0 + 1) * 32, ov[1]);
                 tmem_wait_ld();
-                if (final_out) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t w[4];
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int ch = ch0 + hh;
+                    if (final_out) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 h2 =
-                                __floats2bfloat162_rn(ov[q4 * 8 + 2 * e] * inv, ov[q4 * 8 + 2 * e + 1] * inv);
-                            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[hh][q4 * 8 + 2 * e] * inv,
+                                                                                ov[hh][q4 * 8 + 2 * e + 1] * inv);
+                                w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                            }
+                            *reinterpret_cast<uint4*>(myrow + ch * 64 + q4 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        *reinterpret_cast<uint4*>(myrow + ch * 64 + q4 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                } else {
+                    } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        *reinterpret_cast<float4*>(myrow + ch * 128 + q4 * 16) =
-                            make_float4(ov[q4 * 4] * inv, ov[q4 * 4 + 1] * inv, ov[q4 * 4 + 2] * inv,
-                                        ov[q4 * 4 + 3] * inv);
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            *reinterpret_cast<float4*>(myrow + ch * 128 + q4 * 16) =
+                                make_float4(ov[hh][q4 * 4] * inv, ov[hh][q4 * 4 + 1] * inv,
+                                            ov[hh][q4 * 4 + 2] * inv, ov[hh][q4 * 4 + 3] * inv);
+                    }
                 }
-            }
-            __syncwarp();
-            for (int rr = 0; rr < 32; ++rr) {
-                const int mm = wq * 32 + rr;
-                if (mm >= R) break;
-                const size_t oi2 = (size_t)(ri.row0 + mm / G) * p.num_q_heads + kvh * G + (mm % G);
-                unsigned char* dst = final_out
-                    ? reinterpret_cast<unsigned char*>(p.o + oi2 * D)
-                    : reinterpret_cast<unsigned char*>(p.ws_o + ((size_t)split * p.total_rows * p.num_q_heads + oi2) * D);
-                const unsigned char* src = stg + mm * rs;
-                for (int off = lane * 16; off < row_bytes; off += 512)
-                    *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(src + off);
             }
             if (valid) {
                 if (final_out) {
-                    if (p.lse) p.lse[oi] = lse2 * kLn2;
+                    if (p.lse) p.lse[(size_t)qrow * p.num_q_heads + hq] = lse2 * kLn2;
                 } else {
-                    p.ws_lse[(size_t)split * p.total_rows * p.num_q_heads + oi] = lse2;
+                    p.ws_lse[partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, qrow, m % G)] = lse2;
                 }
                 if (TRACE && p.trace) {
-                    unsigned long long* tp = reinterpret_cast<unsigned long long*>(p.trace + oi * 2);
+                    unsigned long long* tp =
+                        reinterpret_cast<unsigned long long*>(p.trace + ((size_t)qrow * p.num_q_heads + hq) * 2);
                     atomicAdd(tp, (unsigned long long)tr_cnt);
                     atomicAdd(tp + 1, (unsigned long long)tr_sum);
                 }
@@ -740,6 +764,49 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
+    }
+    // ------------------------------------------------------------ copy-out (every thread)
+    // The staged rows leave in coalesced 16-byte pieces, several loads in
+    // flight per thread before their stores.  Split partials of this CTA are one
+    // dense block (rows m = window row * G + head, see partial_pair); bf16
+    // output rows go to [row][head] with the G heads of a window row adjacent.
+    // Nothing was staged if any role gave up (abort).
+    if (*abort == 0) {
+        const bool final_out = (ri.nsplits == 1);
+        const int lg_pieces = final_out ? (D == 64 ? 3 : D == 128 ? 4 : 5) : (D == 64 ? 4 : D == 128 ? 5 : 6);
+        const int rs = (final_out ? D * 2 : D * 4) + 16;
+        const int total = R << lg_pieces;
+        const uint32_t sbase = smem_addr(smem);
+        unsigned char* blk = reinterpret_cast<unsigned char*>(
+            p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0, 0) * D);
+        constexpr int kBatchPieces = 8;
+        const int nt = blockDim.x;
+        for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
+            uint4 v[kBatchPieces];
+#pragma unroll
+            for (int k = 0; k < kBatchPieces; ++k) {
+                const int u = u0 + k * nt;
+                if (u < total) {
+                    const int mm = u >> lg_pieces, c = u & ((1 << lg_pieces) - 1);
+                    v[k] = ld_shared_v4(sbase + mm * rs + c * 16);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatchPieces; ++k) {
+                const int u = u0 + k * nt;
+                if (u < total) {
+                    unsigned char* dst;
+                    if (final_out) {
+                        const int mm = u >> lg_pieces, c = u & ((1 << lg_pieces) - 1);
+                        dst = reinterpret_cast<unsigned char*>(p.o) +
+                              (((size_t)(ri.row0 + mm / G) * p.num_q_heads + kvh * G + mm % G) * D) * 2 + c * 16;
+                    } else {
+                        dst = blk + (size_t)u * 16;
+                    }
+                    st_global_v4(dst, v[k]);
+                }
+            }
+        }
     }
 }
 
@@ -869,13 +936,22 @@ bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
 }
 
 cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bool traced, dim3 grid,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool programmatic) {
     TcKernel k = pick(p.head_dim, kv_dtype, traced);
     if (!k) return cudaErrorInvalidValue;
-    k<<<grid, tc_threads(kv_dtype), smem_for(p.head_dim, kv_dtype), stream>>>(
-        p, *reinterpret_cast<const CUtensorMap*>(maps.q), *reinterpret_cast<const CUtensorMap*>(maps.k),
-        *reinterpret_cast<const CUtensorMap*>(maps.v));
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(tc_threads(kv_dtype), 1, 1);
+    lc.dynamicSmemBytes = smem_for(p.head_dim, kv_dtype);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, k, p, *reinterpret_cast<const CUtensorMap*>(maps.q),
+                              *reinterpret_cast<const CUtensorMap*>(maps.k),
+                              *reinterpret_cast<const CUtensorMap*>(maps.v));
 }
 
 }  // namespace spec_attn
