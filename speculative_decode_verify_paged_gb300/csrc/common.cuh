@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "spec_attn_internal.h"
@@ -17,6 +18,15 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Two floats as fp16 (round to nearest even), low half first.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_half2(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 // Hardware base-2 exponential (MUFU.EX2), flush-to-zero; ex2(-inf) = 0.

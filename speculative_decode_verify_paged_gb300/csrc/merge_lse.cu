@@ -3,9 +3,9 @@
 // (DFlash K>=8 verify at long context)", section "Finding").
 //
 // Split s of a request leaves, per (row, head), the normalised partial
-// O_s = (sum_j 2^(s_j - m_s) v_j) / l_s in fp32 and lse_s = m_s + log2 l_s
-// (base 2, scores pre-scaled by log2 e; -inf when the split saw no key of
-// that row).  The merge is
+// O_s = (sum_j 2^(s_j - m_s) v_j) / l_s, stored as fp16 of O_s / scale_s with
+// scale_s = max |O_s|, and lse_s = m_s + log2 l_s (base 2, scores pre-scaled
+// by log2 e; -inf when the split saw no key of that row).  The merge is
 //   lse = log2 sum_s 2^(lse_s),  O = sum_s 2^(lse_s - lse) O_s,
 // written as bf16 O (round to nearest even) and natural-log LSE (lse * ln 2).
 //
@@ -65,16 +65,16 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
                                           h % p.group);
         const int n = ri.nsplits;
         for (int s0 = g; s0 < n; s0 += sg * kBatch) {
-            float ls[kBatch];
-            float4 o0[kBatch], o1[kBatch];
+            float ls[kBatch], sc[kBatch];
+            uint4 hv[kBatch];
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) {
                 const int s = s0 + k * sg;
                 if (s < n) {
-                    ls[k] = p.ws_lse[s * split_stride + pair0];
-                    const float* src = p.ws_o + (s * split_stride + pair0) * D + v * 8;
-                    o0[k] = *reinterpret_cast<const float4*>(src);
-                    o1[k] = *reinterpret_cast<const float4*>(src + 4);
+                    const float2 lsc = p.ws_ls[s * split_stride + pair0];
+                    ls[k] = lsc.x;
+                    sc[k] = lsc.y;
+                    hv[k] = *reinterpret_cast<const uint4*>(p.ws_o + (s * split_stride + pair0) * D + v * 8);
                 } else {
                     ls[k] = -INFINITY;
                 }
@@ -82,6 +82,13 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) {
                 if (ls[k] == -INFINITY) continue;
+                float4 o0, o1;
+                {
+                    const float2 a = unpack_half2(hv[k].x), b = unpack_half2(hv[k].y);
+                    const float2 c = unpack_half2(hv[k].z), d = unpack_half2(hv[k].w);
+                    o0 = make_float4(a.x * sc[k], a.y * sc[k], b.x * sc[k], b.y * sc[k]);
+                    o1 = make_float4(c.x * sc[k], c.y * sc[k], d.x * sc[k], d.y * sc[k]);
+                }
                 if (ls[k] > m_run) {
                     const float a = fast_exp2(m_run - ls[k]);   // 0 while m_run is -inf
                     a0.x *= a; a0.y *= a; a0.z *= a; a0.w *= a;
@@ -90,10 +97,10 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
                     m_run = ls[k];
                 }
                 const float w = fast_exp2(ls[k] - m_run);
-                a0.x = fmaf(w, o0[k].x, a0.x); a0.y = fmaf(w, o0[k].y, a0.y);
-                a0.z = fmaf(w, o0[k].z, a0.z); a0.w = fmaf(w, o0[k].w, a0.w);
-                a1.x = fmaf(w, o1[k].x, a1.x); a1.y = fmaf(w, o1[k].y, a1.y);
-                a1.z = fmaf(w, o1[k].z, a1.z); a1.w = fmaf(w, o1[k].w, a1.w);
+                a0.x = fmaf(w, o0.x, a0.x); a0.y = fmaf(w, o0.y, a0.y);
+                a0.z = fmaf(w, o0.z, a0.z); a0.w = fmaf(w, o0.w, a0.w);
+                a1.x = fmaf(w, o1.x, a1.x); a1.y = fmaf(w, o1.y, a1.y);
+                a1.z = fmaf(w, o1.z, a1.z); a1.w = fmaf(w, o1.w, a1.w);
                 l_run += w;
             }
         }

@@ -39,7 +39,7 @@ struct spec_attn_plan {
     int smem;
     bool uses_merge;
     size_t ws_bytes;
-    size_t ws_lse_off;
+    size_t ws_ls_off;
     size_t ws_o_off;
     float sm_scale;
     cudaEvent_t ev_begin;
@@ -261,7 +261,8 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         const double t_stream = 2.0 * bkh / (6.5e6 / (plan->num_sms * occ));
         cm.key_us = std::max(t_compute, t_stream);
     }
-    const double partial_bytes = static_cast<double>(p.total_q_rows) * p.num_q_heads * (p.head_dim + 1) * 4.0 * 2.0;
+    // per split: fp16 partial rows + (lse, scale), written once and read once
+    const double partial_bytes = static_cast<double>(p.total_q_rows) * p.num_q_heads * (p.head_dim * 2.0 + 8.0) * 2.0;
     if (p.force_splits > 0) {
         int64_t c = (max_seq + p.force_splits - 1) / p.force_splits;
         c = (c + kSplitUnit - 1) / kSplitUnit * kSplitUnit;
@@ -272,17 +273,18 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     }
     plan->max_splits = static_cast<int>((max_seq + plan->keys_per_split - 1) / plan->keys_per_split);
     plan->uses_merge = plan->max_splits > 1;
+
     plan->grid = dim3(static_cast<unsigned>(plan->max_splits * plan->row_groups),
                       static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(std::max(1, p.num_reqs)));
 
-    // ---- workspace layout: [status 256 B][lse partials][O partials] ----
-    plan->ws_lse_off = kStatusBytes;
+    // ---- workspace layout: [status 256 B][(lse, scale) partials][fp16 O partials] ----
+    plan->ws_ls_off = kStatusBytes;
     size_t ws = kStatusBytes;
     if (plan->uses_merge) {
         const size_t pairs = static_cast<size_t>(p.total_q_rows) * p.num_q_heads;
-        ws = align_up(plan->ws_lse_off + static_cast<size_t>(plan->max_splits) * pairs * sizeof(float), 256);
+        ws = align_up(plan->ws_ls_off + static_cast<size_t>(plan->max_splits) * pairs * 2 * sizeof(float), 256);
         plan->ws_o_off = ws;
-        ws += static_cast<size_t>(plan->max_splits) * pairs * p.head_dim * sizeof(float);
+        ws += static_cast<size_t>(plan->max_splits) * pairs * p.head_dim * sizeof(uint16_t);
     } else {
         plan->ws_o_off = kStatusBytes;
     }
@@ -365,8 +367,8 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.lse = lse;
     sp.trace = reinterpret_cast<long long*>(trace);
     sp.status = reinterpret_cast<unsigned int*>(ws);
-    sp.ws_lse = reinterpret_cast<float*>(ws + plan->ws_lse_off);
-    sp.ws_o = reinterpret_cast<float*>(ws + plan->ws_o_off);
+    sp.ws_ls = reinterpret_cast<float2*>(ws + plan->ws_ls_off);
+    sp.ws_o = reinterpret_cast<uint16_t*>(ws + plan->ws_o_off);
     sp.num_reqs = p.num_reqs;
     sp.total_rows = p.total_q_rows;
     sp.max_w = p.max_w;
@@ -422,7 +424,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         mp.seq_lens = seq_lens;
         mp.q_indptr = q_indptr;
         mp.ws_o = sp.ws_o;
-        mp.ws_lse = sp.ws_lse;
+        mp.ws_ls = sp.ws_ls;
         mp.o = sp.o;
         mp.lse = lse;
         mp.num_reqs = p.num_reqs;

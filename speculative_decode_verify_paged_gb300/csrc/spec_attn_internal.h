@@ -21,8 +21,8 @@ struct SplitParams {
     uint16_t* o;                // [total_rows, Hq, d] bf16 bits
     float* lse;                 // [total_rows, Hq] or nullptr
     long long* trace;           // [total_rows, Hq, 2] or nullptr
-    float* ws_o;                // fp32 partials, (row, head) pairs ordered by partial_pair()
-    float* ws_lse;              // fp32 partial LSE (log2 units), same pair order
+    uint16_t* ws_o;             // split partials: per (row, head) pair, d fp16 values of O_s / scale_s
+    float2* ws_ls;              // per pair: (lse_s in log2 units, scale_s = max |O_s|), same order
     unsigned int* status;       // sticky device-status word
     int num_reqs;
     int total_rows;
@@ -47,8 +47,8 @@ struct SplitParams {
 struct MergeParams {
     const int32_t* seq_lens;
     const int32_t* q_indptr;
-    const float* ws_o;
-    const float* ws_lse;
+    const uint16_t* ws_o;
+    const float2* ws_ls;
     uint16_t* o;
     float* lse;
     int num_reqs;
@@ -63,6 +63,12 @@ struct MergeParams {
     int bt_capacity_keys;       // bt_stride * page_size
 };
 
+// Split partials.  A split leaves, per (window row, query head) pair, its
+// normalised partial output O_s (d values), lse_s and scale_s = max_e |O_s[e]|;
+// O_s is stored as d fp16 values of O_s / scale_s (in [-1, 1]), so a stored
+// value is off by at most scale_s * 2^-12, and the partials take half the bytes
+// of fp32 for the split kernel to write and the merge to read.
+//
 // Order of the (window row, query head) pairs in the split partials: split-major,
 // then KV head, then window row, then the G query heads of that KV head.  The
 // pairs one split CTA produces (one KV head, consecutive window rows) are one

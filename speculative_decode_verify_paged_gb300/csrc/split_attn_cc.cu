@@ -330,12 +330,18 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
             }
             if (p.lse && lane == 0) p.lse[oi] = lse2 * kLn2;
         } else {
+            // fp16 of value / scale, scale = the row's largest magnitude
             const size_t pi = partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, qrow[t], hq[t] - kvh * G);
-            float* wp = p.ws_o + pi * D + lane * DPL;
+            float amax = 0.f;
 #pragma unroll
-            for (int e = 0; e < DPL; e += 2)
-                *reinterpret_cast<float2*>(wp + e) = make_float2(o_acc[t][e] * inv_l, o_acc[t][e + 1] * inv_l);
-            if (lane == 0) p.ws_lse[pi] = lse2;
+            for (int e = 0; e < DPL; ++e) amax = fmaxf(amax, fabsf(o_acc[t][e] * inv_l));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
+            const float sc = amax > 0.f ? inv_l / amax : 0.f;
+            uint32_t* wp = reinterpret_cast<uint32_t*>(p.ws_o + pi * D + lane * DPL);
+#pragma unroll
+            for (int e = 0; e < DPL; e += 2) wp[e / 2] = pack_half2(o_acc[t][e] * sc, o_acc[t][e + 1] * sc);
+            if (lane == 0) p.ws_ls[pi] = make_float2(lse2, amax);
         }
     }
 }

@@ -98,8 +98,9 @@ struct TcLayout {
     static constexpr uint32_t kTmemCols = (D + 2 * kBN) <= 128 ? 128u : ((D + 2 * kBN) <= 256 ? 256u : 512u);
     static_assert(KV ? (kNR >= 2) : (kNK >= 2 && kNV >= 2), "ring too small");
     static_assert(kSmem <= kMaxDyn, "shared memory");
-    // the epilogue stages kM rows of fp32 O (+16 B padding) over query/P/ring buffers
-    static_assert(kM * (D * 4 + 16) <= kQBytes + kPBytes + (kNK + kNV) * kTileBytes, "epilogue staging");
+    // the epilogue stages kM rows of fp32 O (+16 B padding) and kM row scales
+    // over the query/P/ring buffers
+    static_assert(kM * (D * 4 + 16) + kM * 4 <= kQBytes + kPBytes + (kNK + kNV) * kTileBytes, "epilogue staging");
 };
 
 struct TcAux {
@@ -705,14 +706,16 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         if (ok) {
             // Every MMA and copy has completed (o_final), so the query, P and
             // ring buffers are free: each thread stages its row of the
-            // normalised O there (bf16 output, or the fp32 partial), row stride
-            // padded by 16 bytes so the 16-byte stores of a warp hit distinct
-            // banks.  All warps copy the rows out below.
+            // normalised O there (bf16 output, or fp32 for a split partial,
+            // with the row's largest magnitude), row stride padded by 16 bytes
+            // so the 16-byte stores of a warp hit distinct banks.  All warps
+            // copy the rows out below.
             const float inv = (valid && l_sum > 0.f) ? (p.out_scale / l_sum) : 0.f;
             const float lse2 = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) : -INFINITY;
             const bool final_out = (ri.nsplits == 1);
             const int rs = (final_out ? D * 2 : D * 4) + 16;
             unsigned char* myrow = smem + m * rs;
+            float amax = 0.f;
             // two 32-column TMEM loads in flight per wait
 #pragma unroll 1
             for (int ch0 = 0; ch0 < D / 32; ch0 += 2) {
@@ -737,18 +740,23 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                         }
                     } else {
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            *reinterpret_cast<float4*>(myrow + ch * 128 + q4 * 16) =
-                                make_float4(ov[hh][q4 * 4] * inv, ov[hh][q4 * 4 + 1] * inv,
-                                            ov[hh][q4 * 4 + 2] * inv, ov[hh][q4 * 4 + 3] * inv);
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            const float4 f = make_float4(ov[hh][q4 * 4] * inv, ov[hh][q4 * 4 + 1] * inv,
+                                                         ov[hh][q4 * 4 + 2] * inv, ov[hh][q4 * 4 + 3] * inv);
+                            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+                            *reinterpret_cast<float4*>(myrow + ch * 128 + q4 * 16) = f;
+                        }
                     }
                 }
             }
+            if (!final_out)   // 1 / scale of each staged row, after the rows
+                reinterpret_cast<float*>(smem + kM * rs)[m] = amax > 0.f ? 1.f / amax : 0.f;
             if (valid) {
                 if (final_out) {
                     if (p.lse) p.lse[(size_t)qrow * p.num_q_heads + hq] = lse2 * kLn2;
                 } else {
-                    p.ws_lse[partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, qrow, m % G)] = lse2;
+                    p.ws_ls[partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, qrow, m % G)] =
+                        make_float2(lse2, amax);
                 }
                 if (TRACE && p.trace) {
                     unsigned long long* tp =
@@ -768,42 +776,68 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     // ------------------------------------------------------------ copy-out (every thread)
     // The staged rows leave in coalesced 16-byte pieces, several loads in
     // flight per thread before their stores.  Split partials of this CTA are one
-    // dense block (rows m = window row * G + head, see partial_pair); bf16
-    // output rows go to [row][head] with the G heads of a window row adjacent.
-    // Nothing was staged if any role gave up (abort).
+    // dense block (rows m = window row * G + head, see partial_pair), written as
+    // fp16 of value / scale; bf16 output rows go to [row][head] with the G
+    // heads of a window row adjacent.  Nothing was staged if any role gave up
+    // (abort).
     if (*abort == 0) {
-        const bool final_out = (ri.nsplits == 1);
-        const int lg_pieces = final_out ? (D == 64 ? 3 : D == 128 ? 4 : 5) : (D == 64 ? 4 : D == 128 ? 5 : 6);
-        const int rs = (final_out ? D * 2 : D * 4) + 16;
-        const int total = R << lg_pieces;
-        const uint32_t sbase = smem_addr(smem);
-        unsigned char* blk = reinterpret_cast<unsigned char*>(
-            p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0, 0) * D);
         constexpr int kBatchPieces = 8;
         const int nt = blockDim.x;
-        for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
-            uint4 v[kBatchPieces];
+        const uint32_t sbase = smem_addr(smem);
+        if (ri.nsplits == 1) {
+            constexpr int lg = (D == 64 ? 3 : D == 128 ? 4 : 5);   // 16-byte pieces per bf16 row
+            constexpr int rs = D * 2 + 16;
+            const int total = R << lg;
+            for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
+                uint4 v[kBatchPieces];
 #pragma unroll
-            for (int k = 0; k < kBatchPieces; ++k) {
-                const int u = u0 + k * nt;
-                if (u < total) {
-                    const int mm = u >> lg_pieces, c = u & ((1 << lg_pieces) - 1);
-                    v[k] = ld_shared_v4(sbase + mm * rs + c * 16);
+                for (int k = 0; k < kBatchPieces; ++k) {
+                    const int u = u0 + k * nt;
+                    if (u < total) v[k] = ld_shared_v4(sbase + (u >> lg) * rs + (u & ((1 << lg) - 1)) * 16);
+                }
+#pragma unroll
+                for (int k = 0; k < kBatchPieces; ++k) {
+                    const int u = u0 + k * nt;
+                    if (u < total) {
+                        const int mm = u >> lg, c = u & ((1 << lg) - 1);
+                        unsigned char* dst = reinterpret_cast<unsigned char*>(p.o) +
+                                             (((size_t)(ri.row0 + mm / G) * p.num_q_heads + kvh * G + mm % G) * D) * 2 +
+                                             c * 16;
+                        st_global_v4(dst, v[k]);
+                    }
                 }
             }
+        } else {
+            constexpr int lg = (D == 64 ? 3 : D == 128 ? 4 : 5);   // 8-value pieces per row
+            constexpr int rs = D * 4 + 16;
+            const int total = R << lg;
+            const float* rinv = reinterpret_cast<const float*>(smem + kM * rs);
+            unsigned char* blk = reinterpret_cast<unsigned char*>(
+                p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0, 0) * D);
+            for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
+                uint4 a[kBatchPieces], b[kBatchPieces];
+                float sc[kBatchPieces];
 #pragma unroll
-            for (int k = 0; k < kBatchPieces; ++k) {
-                const int u = u0 + k * nt;
-                if (u < total) {
-                    unsigned char* dst;
-                    if (final_out) {
-                        const int mm = u >> lg_pieces, c = u & ((1 << lg_pieces) - 1);
-                        dst = reinterpret_cast<unsigned char*>(p.o) +
-                              (((size_t)(ri.row0 + mm / G) * p.num_q_heads + kvh * G + mm % G) * D) * 2 + c * 16;
-                    } else {
-                        dst = blk + (size_t)u * 16;
+                for (int k = 0; k < kBatchPieces; ++k) {
+                    const int u = u0 + k * nt;
+                    if (u < total) {
+                        const uint32_t src = sbase + (u >> lg) * rs + (u & ((1 << lg) - 1)) * 32;
+                        a[k] = ld_shared_v4(src);
+                        b[k] = ld_shared_v4(src + 16);
+                        sc[k] = rinv[u >> lg];
                     }
-                    st_global_v4(dst, v[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < kBatchPieces; ++k) {
+                    const int u = u0 + k * nt;
+                    if (u < total) {
+                        uint4 h;
+                        h.x = pack_half2(__uint_as_float(a[k].x) * sc[k], __uint_as_float(a[k].y) * sc[k]);
+                        h.y = pack_half2(__uint_as_float(a[k].z) * sc[k], __uint_as_float(a[k].w) * sc[k]);
+                        h.z = pack_half2(__uint_as_float(b[k].x) * sc[k], __uint_as_float(b[k].y) * sc[k]);
+                        h.w = pack_half2(__uint_as_float(b[k].z) * sc[k], __uint_as_float(b[k].w) * sc[k]);
+                        st_global_v4(blk + (size_t)u * 16, h);
+                    }
                 }
             }
         }

@@ -66,7 +66,7 @@ def test_noalloc_matches_run_on_two_calls(lib, variant):
 
 
 def test_noalloc_rejects_plans_larger_than_its_scratch(lib):
-    # 257 splits x 16 rows x 32 heads x 256 dims x 4 B = 134 MB of partials > 32 MiB
+    # 513 splits x 16 rows x 32 heads x (256 fp16 values + lse + scale) = 68 MB of partials > 32 MiB
     wl = W.make_workload("big", [32768], [16], 32, 2, 256, W.MASK_NON_CAUSAL, seed=32)
     dw = sa.DeviceWorkload(wl, "cuda", force_splits=512)
     assert dw.plan.workspace_bytes > (32 << 20)
