@@ -29,6 +29,14 @@ __device__ __forceinline__ float2 unpack_half2(uint32_t w) {
     return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
+// A bf16 pair as an fp16 pair (round to nearest even, saturating to +-65504).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t w) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));   // first operand -> upper half
+    return d;
+}
+
 // Hardware base-2 exponential (MUFU.EX2), flush-to-zero; ex2(-inf) = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

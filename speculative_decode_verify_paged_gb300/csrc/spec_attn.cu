@@ -48,7 +48,7 @@ struct spec_attn_plan {
     // decode loop re-running a plan on the same buffers encodes them once.
     std::mutex maps_mutex;
     TcMaps maps;
-    const void* maps_key[3] = {nullptr, nullptr, nullptr};
+    const void* maps_key[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
 };
 
 namespace {
@@ -394,14 +394,17 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     std::unique_lock<std::mutex> maps_lock(mp->maps_mutex, std::defer_lock);
     if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
         maps_lock.lock();
-        if (mp->maps_key[0] != q || mp->maps_key[1] != k_pool || mp->maps_key[2] != v_pool) {
+        if (mp->maps_key[0] != q || mp->maps_key[1] != k_pool || mp->maps_key[2] != v_pool ||
+            mp->maps_key[3] != k_scales || mp->maps_key[4] != v_scales) {
             if (!tc_encode_maps(sp, p.kv_dtype, &mp->maps)) {
-                mp->maps_key[0] = mp->maps_key[1] = mp->maps_key[2] = nullptr;
+                for (auto& k : mp->maps_key) k = nullptr;
                 return SPEC_ATTN_E_INVALID_ARG;
             }
             mp->maps_key[0] = q;
             mp->maps_key[1] = k_pool;
             mp->maps_key[2] = v_pool;
+            mp->maps_key[3] = k_scales;
+            mp->maps_key[4] = v_scales;
         }
     }
     if (plan->ev_begin) {

@@ -101,10 +101,13 @@ cudaError_t cc_launch(const SplitParams& p, int kv_dtype, const CcConfig& cfg, b
 
 // ---- tcgen05 split-KV kernel (split_attn_tc.cu) ----
 // TMA descriptors of one (Q, K pool, V pool) triple; opaque CUtensorMap storage.
+// bf16 KV: K and V pools; NVFP4: K and V code pools, plus their scale pools.
 struct TcMaps {
     alignas(64) unsigned char q[128];
     alignas(64) unsigned char k[128];
     alignas(64) unsigned char v[128];
+    alignas(64) unsigned char ks[128];
+    alignas(64) unsigned char vs[128];
 };
 bool tc_supported(int head_dim, int kv_dtype, int max_rows);
 int tc_smem_bytes(int head_dim, int kv_dtype);

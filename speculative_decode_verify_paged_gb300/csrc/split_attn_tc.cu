@@ -1,5 +1,5 @@
 // Split-KV block attention on 5th-generation tensor cores (tcgen05 + TMEM),
-// bf16 KV, for sm_103a.
+// bf16 or NVFP4 KV, for sm_103a.
 //
 // One CTA = (split s of request r's keys) x (KV head kvh).  Its query tile is
 // all W x G rows of the request that read KV head kvh (row m = window row
@@ -11,26 +11,31 @@
 // rows (page "DFlash2 leaves the paged graph fast path at every c>1 ...",
 // section "The cost").
 //
-// Warp roles (256 threads):
+// Warp roles, bf16 KV (256 threads):
 //   warp 0      loads the query tile once (TMA, one box per 64 head_dim
 //               elements covering G heads x max_w window rows), then streams
-//               the K tiles: 32 keys (two 16-key pages, one 2 KB box per 64
-//               head_dim elements), 128-byte swizzled, into a ring of slots.
-//   warp 2      streams the V tiles the same way into a second, deeper ring
+//               the K tiles: 64 keys (four 16-key pages, one 2 KB box per page
+//               and 64 head_dim elements, issued from 16 lanes), 128-byte
+//               swizzled, chunk-major, into a ring of slots.
+//   warp 2      streams the V tiles into a second ring, one box per page-head
 //               (a K slot frees as soon as its S is computed, a V slot only
-//               after P V, so the two rings keep more bytes in flight).
+//               after P V).
 //   warp 1      allocates TMEM; one lane issues the MMAs as their inputs land:
-//                 S_t = Q K_t^T   (M 128, N 32, bf16 -> fp32 in TMEM, double-buffered)
-//                 O  += P_t V_t   (M 128, N head_dim, P from shared memory, V MN-major)
+//                 S_t = Q K_t^T   (M 128, N 64, -> fp32 in TMEM, double-buffered)
+//                 O  += P_t V_t   (M 128, N head_dim, one MMA per page, V MN-major)
 //   warp 3      idle.
 //   warps 4-7   softmax: thread m owns row m (TMEM lane m).  Per tile it reads
-//               its 32 scores, applies the causal-in-block / non-causal mask by
+//               its 64 scores, applies the causal-in-block / non-causal mask by
 //               key index, updates a base-2 online softmax whose reference
 //               maximum moves only when a score exceeds it by more than 2^8
-//               (then the row of O in TMEM is rescaled), writes P as bf16 into
-//               one half of a double-buffered swizzled A-operand tile, and at
-//               the end normalises O and
-//               writes the output (or an fp32 partial for the LSE merge).
+//               (then the row of O in TMEM is rescaled), and writes P into
+//               one half of a double buffer; at the end it normalises O and
+//               stages the row for the output (or a split partial), which
+//               every warp then copies out.
+// NVFP4 KV (512 threads): warp 0 copies the tiles' codes and scales with
+// cp.async into a raw ring instead of TMA; warps 8-11 decode K and 12-15 decode
+// V into fp16 operand tiles; the softmax warps first convert the query tile to
+// fp16 in place, and P (fp16) goes to TMEM, where the P V MMA reads it.
 //
 // Every wait on an mbarrier is bounded: on time-out the CTA raises the
 // device-status bit, stops issuing, drains its in-flight copies and MMAs,
@@ -63,19 +68,26 @@ constexpr int kPageListCap = 64;                 // page ids staged in shared me
 constexpr int kMaxNR = 8;                        // NVFP4 raw (codes + scales) ring slots
 constexpr int kMaxNK = 8, kMaxNV = 16;
 
-// Shared memory: query tile | P tile | K ring | V ring | [NVFP4 raw ring] | barriers.
-// bf16 KV: K and V tiles arrive by TMA into rings of kNK / kNV slots.
-// NVFP4 KV: codes and scales arrive by cp.async into a ring of kNR raw slots and
-// are decoded into one bf16 K tile and one bf16 V tile (kNK = kNV = 1).
+// Shared memory: [query tile] | P tile | K ring | V ring | [NVFP4 raw ring] | barriers.
+// bf16 KV: the query tile, P (bf16) and the K and V tiles are MMA operands in
+// shared memory; K and V arrive by TMA into rings of kNK / kNV slots.
+// NVFP4 KV: codes and scales arrive by TMA into a ring of kNR raw slots and are
+// decoded into fp16 K and V operand tiles (two slots each).  The query tile
+// lands (bf16, by TMA) in the V slots, which it exactly fills, and the softmax
+// warps move it, converted to fp16, into TMEM; P (fp16) is written to TMEM too.
+// Both MMAs then take their A operand from TMEM: that keeps the 128-row tiles
+// out of shared memory, whose bandwidth the decode needs, and an MMA with its
+// A operand in TMEM issues at about twice the rate.
 template <int D, int KV>
 struct TcLayout {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along head_dim
-    static constexpr int kQBytes = kM * D * 2;
+    static constexpr int kQBytes = kM * D * 2;             // the query tile (16-bit elements)
+    static constexpr int kQSmem = KV ? 0 : kQBytes;        // its own region in the shared-memory layout
     // P: two tiles (double buffer).  32-key tiles share each 128-byte swizzle row
     // (one half each); 64-key tiles fill a row, so the buffers are separate.
-    static constexpr int kPBytes = kM * 128 * (kBN == 64 ? 2 : 1);
-    static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile (bf16)
-    static constexpr int kPageBytes = 16 * D * 2;          // one page-head of V (bf16)
+    static constexpr int kPBytes = KV ? 0 : kM * 128 * (kBN == 64 ? 2 : 1);
+    static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile (16-bit elements)
+    static constexpr int kPageBytes = 16 * D * 2;          // one page-head of V (16-bit elements)
     static constexpr int kRawCodePage = 16 * D / 2;        // NVFP4 codes of one page-head
     static constexpr int kRawScalePage = 16 * D / 16;      // NVFP4 scales of one page-head
     static constexpr int kRawKS = kPPT * kRawCodePage;     // offsets inside a raw slot
@@ -84,23 +96,31 @@ struct TcLayout {
     static constexpr int kRawTile = 2 * kPPT * (kRawCodePage + kRawScalePage);
     static constexpr int kAuxBytes = 1536;
     static constexpr int kMaxDyn = 232448;                  // 227 KB opt-in limit
-    static constexpr int kFixed = 1024 + kQBytes + kPBytes + kAuxBytes;
+    static constexpr int kFixed = 1024 + kQSmem + kPBytes + kAuxBytes;
     static constexpr int kRing = (kMaxDyn - kFixed) / kTileBytes;
     // bf16: K tiles are released as soon as their S = Q K^T is done, V tiles only
     // after P V, so V gets the larger share of the ring.
-    static constexpr int kNK = KV ? 1 : ((kRing / 3) > kMaxNK ? kMaxNK : ((kRing / 3) < 2 ? 2 : (kRing / 3)));
-    static constexpr int kNV = KV ? 1 : ((kRing - kNK) > kMaxNV ? kMaxNV : (kRing - kNK));
-    static constexpr int kRawFit = (kMaxDyn - kFixed - 2 * kTileBytes - 512) / kRawTile;
+    static constexpr int kNK = KV ? 2 : ((kRing / 3) > kMaxNK ? kMaxNK : ((kRing / 3) < 2 ? 2 : (kRing / 3)));
+    static constexpr int kNV = KV ? 2 : ((kRing - kNK) > kMaxNV ? kMaxNV : (kRing - kNK));
+    static constexpr int kRawFit = (kMaxDyn - kFixed - (kNK + kNV) * kTileBytes) / kRawTile;
     static constexpr int kNR = KV ? (kRawFit > kMaxNR ? kMaxNR : kRawFit) : 0;
-    static constexpr int kLutBytes = KV ? 512 : 0;         // NVFP4: e4m3 -> bf16 scale table
-    static constexpr int kSmem = kFixed + (kNK + kNV) * kTileBytes + kNR * kRawTile + kLutBytes;
-    static constexpr int kThreads = KV ? kTcThreadsFp4 : kTcThreadsBf16;
-    static constexpr uint32_t kTmemCols = (D + 2 * kBN) <= 128 ? 128u : ((D + 2 * kBN) <= 256 ? 256u : 512u);
+    static constexpr int kSmem = kFixed + (kNK + kNV) * kTileBytes + kNR * kRawTile;
+    // TMEM columns.  bf16: O [0, D), S double buffer [D, D + 2 BN).  NVFP4: O
+    // [0, D), S single buffer [D, D + BN), P double buffer (fp16 pairs)
+    // [D + BN, D + 2 BN), query tile (fp16 pairs) [D + 2 BN, D + 2 BN + D / 2).
+    static constexpr int kSBufs = KV ? 1 : 2;
+    static constexpr int kPCol = D + kBN;
+    static constexpr int kQCol = D + 2 * kBN;
+    static constexpr int kTmemNeed = D + 2 * kBN + (KV ? D / 2 : 0);
+    static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128u : (kTmemNeed <= 256 ? 256u : 512u);
     static_assert(KV ? (kNR >= 2) : (kNK >= 2 && kNV >= 2), "ring too small");
     static_assert(kSmem <= kMaxDyn, "shared memory");
+    static_assert(kTmemNeed <= 512, "tensor memory");
+    static_assert(!KV || kQBytes == kNV * kTileBytes, "NVFP4: the query tile lands in the V slots");
     // the epilogue stages kM rows of fp32 O (+16 B padding) and kM row scales
-    // over the query/P/ring buffers
-    static_assert(kM * (D * 4 + 16) + kM * 4 <= kQBytes + kPBytes + (kNK + kNV) * kTileBytes, "epilogue staging");
+    // over the query/P/operand/raw buffers (all idle by then)
+    static_assert(kM * (D * 4 + 16) + kM * 4 <= kQSmem + kPBytes + (kNK + kNV) * kTileBytes + kNR * kRawTile,
+                  "epilogue staging");
 };
 
 struct TcAux {
@@ -115,7 +135,9 @@ struct TcAux {
     uint64_t o_done;     // one phase per P V (rescale waits: at most one phase behind)
     uint64_t o_final;    // one phase after the last P V (the epilogue's wait)
     uint64_t q_full;
+    uint64_t q_ready;    // NVFP4: the query tile converted to fp16 (one arrival per softmax warp)
     uint64_t drain;
+    uint64_t drain_pv;   // NVFP4: the P V issuer's own MMAs
     uint64_t raw_full[kMaxNR];             // NVFP4: codes/scales of a tile landed (32 lane arrivals)
     uint64_t raw_empty[kMaxNR];            // NVFP4: both dequant warpgroups are done with a raw slot
     int32_t pages_v[kMaxNV][kPPT];         // physical pages of each V slot (index trace)
@@ -211,22 +233,23 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
     return issued;
 }
 
-// NVFP4: one warp copies each tile's e2m1 codes and e4m3 scales (K then V; a
-// page-head's codes and scales are contiguous in their pools) with 16-byte
-// cp.async into a raw ring slot; every lane then arrives on the slot's
-// barrier when its copies have landed.
-__device__ __forceinline__ void cp_async16_raw(void* smem_dst, const void* gmem_src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
+// Position of 16-byte code chunk ch (of D / 32) within key sl's row of a page's
+// codes in the raw ring.  The TMA copies them with the 128/64/32-byte swizzle
+// of d = 256/128/64 (16-byte chunk index XOR address bits 7..9), which places
+// one chunk of 8 consecutive keys in 8 different 16-byte bank groups.
 template <int D>
-__device__ __forceinline__ void produce_raw(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
-                                            unsigned char* raw, TcAux* aux, volatile int* abort, int lane,
-                                            int pre0, int pre1) {
+__device__ __forceinline__ int raw_code_chunk(int sl, int ch) {
+    return D == 256 ? (ch ^ (sl & 7)) : D == 128 ? (ch ^ ((sl >> 1) & 3)) : (ch ^ ((sl >> 2) & 1));
+}
+
+// NVFP4: one warp streams each tile's e2m1 codes and e4m3 scales, K and V, into
+// a raw ring slot by TMA: per page-head one box of codes (16 keys x d/2 bytes,
+// swizzled) and one of scales (d bytes), issued from 4 lanes per page.
+template <int D>
+__device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
+                                           unsigned char* raw, TcAux* aux, const CUtensorMap* tkc,
+                                           const CUtensorMap* tvc, const CUtensorMap* tks, const CUtensorMap* tvs,
+                                           volatile int* abort, int lane, int pre0, int pre1) {
     using L = TcLayout<D, 1>;
     constexpr int NR = L::kNR;
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride + key_lo / 16;
@@ -248,8 +271,7 @@ __device__ __forceinline__ void produce_raw(const SplitParams& p, int r, int kvh
     if (lane < n_pages) list[lane] = checked(pre0);
     if (lane + 32 < n_pages) list[lane + 32] = checked(pre1);
     __syncwarp();
-    const unsigned char* kc_pool = static_cast<const unsigned char*>(p.k_pool);
-    const unsigned char* vc_pool = static_cast<const unsigned char*>(p.v_pool);
+    int issued = 0;
     for (int t = 0; t < T; ++t) {
         const int slot = t % NR;
         if (t >= NR && !warp_wait(&aux->raw_empty[slot], ((t / NR) - 1) & 1, abort)) break;
@@ -261,100 +283,117 @@ __device__ __forceinline__ void produce_raw(const SplitParams& p, int r, int kvh
         }
         const int np = min(kPPT, (key_hi - (key_lo + t * kBN) + 15) / 16);
         unsigned char* dst = raw + slot * L::kRawTile;
-        for (int pp = 0; pp < np; ++pp) {
+        // the slot's page ids (index trace) are published by the arrival below
+        if (lane < np) aux->raw_pages[slot][lane] = list[rel - list_base + lane];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_expect_tx(&aux->raw_full[slot],
+                                  static_cast<uint32_t>(np * 2 * (L::kRawCodePage + L::kRawScalePage)));
+        __syncwarp();
+        if (lane < 4 * np) {
+            const int pp = lane >> 2, kind = lane & 3;
             const int pg = list[rel - list_base + pp];
-            if (lane == 0) aux->raw_pages[slot][pp] = pg;
-            const size_t tok = ((size_t)pg * p.num_kv_heads + kvh) * 16;
-            const unsigned char* kc = kc_pool + tok * (D / 2);
-            const unsigned char* vc = vc_pool + tok * (D / 2);
-            const unsigned char* ks = p.k_scales + tok * (D / 16);
-            const unsigned char* vs = p.v_scales + tok * (D / 16);
-            for (int c = lane; c < L::kRawCodePage / 16; c += 32) {
-                cp_async16_raw(dst + pp * L::kRawCodePage + c * 16, kc + c * 16);
-                cp_async16_raw(dst + L::kRawVC + pp * L::kRawCodePage + c * 16, vc + c * 16);
-            }
-            for (int c = lane; c < L::kRawScalePage / 16; c += 32) {
-                cp_async16_raw(dst + L::kRawKS + pp * L::kRawScalePage + c * 16, ks + c * 16);
-                cp_async16_raw(dst + L::kRawVS + pp * L::kRawScalePage + c * 16, vs + c * 16);
-            }
+            const int z = pg * p.num_kv_heads + kvh;   // page-head index
+            uint64_t* bar = &aux->raw_full[slot];
+            if (kind == 0) tma_load_3d(dst + pp * L::kRawCodePage, tkc, 0, 0, z, bar);
+            else if (kind == 1) tma_load_3d(dst + L::kRawVC + pp * L::kRawCodePage, tvc, 0, 0, z, bar);
+            else if (kind == 2) tma_load_2d(dst + L::kRawKS + pp * L::kRawScalePage, tks, 0, z, bar);
+            else tma_load_2d(dst + L::kRawVS + pp * L::kRawScalePage, tvs, 0, z, bar);
         }
-        cp_async_arrive_noinc(&aux->raw_full[slot]);
+        __syncwarp();
+        issued = t + 1;
     }
-    cp_async_wait_all();   // nothing may still be landing when the CTA exits
+    return issued;
 }
 
-// 16 NVFP4 elements (8 code bytes, low nibble first) times their e4m3 block
-// scale, as 16 bf16 values.  An e2m1 magnitude's bf16 bit pattern is looked up
-// with byte permutes (high and low bytes of the eight possible magnitudes
-// 0, .5, 1, 1.5, 2, 3, 4, 6), the sign is the code's bit 3, and the product with
-// the scale (at most 6 significant bits) is exact in bf16.
-__device__ __forceinline__ void e2m1x4_bf16(uint32_t hw, __nv_bfloat162 s2, uint32_t& p01, uint32_t& p23) {
-    const uint32_t sel = hw & 0x7777u;
-    const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);
-    const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);
-    const uint32_t sg = hw & 0x8888u;
-    uint32_t a = __byte_perm(lo, hi, 0x5140u) | ((sg << 12) & 0x8000u) | ((sg << 24) & 0x80000000u);
-    uint32_t b = __byte_perm(lo, hi, 0x7362u) | ((sg << 4) & 0x8000u) | ((sg << 16) & 0x80000000u);
-    __nv_bfloat162 xa = *reinterpret_cast<const __nv_bfloat162*>(&a);
-    __nv_bfloat162 xb = *reinterpret_cast<const __nv_bfloat162*>(&b);
-    xa = __hmul2(xa, s2);
-    xb = __hmul2(xb, s2);
-    p01 = *reinterpret_cast<const uint32_t*>(&xa);
-    p23 = *reinterpret_cast<const uint32_t*>(&xb);
+// Decode of NVFP4 K/V into fp16 MMA operands.  cvt.rn.f16x2.e2m1x2 turns one
+// code byte (two e2m1 values, the low nibble into the low half) into an fp16
+// pair and cvt.rn.f16x2.e4m3x2 one scale byte into (s, s); the products (at most
+// 5 significant bits, magnitudes 2^-10 .. 2688) are exact in fp16.
+__device__ __forceinline__ uint32_t e4m3_pair_f16x2(uint32_t byte) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(byte * 0x0101u)));
+    return d;
 }
-// scale_bf16: bf16 bit pattern of the block's e4m3 scale (from the table).
-__device__ __forceinline__ void decode16(uint2 codes, uint32_t scale_bf16, uint4& lo8, uint4& hi8) {
-    const uint32_t s2u = scale_bf16 | (scale_bf16 << 16);
-    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
-    e2m1x4_bf16(codes.x & 0xFFFFu, s2, lo8.x, lo8.y);
-    e2m1x4_bf16(codes.x >> 16, s2, lo8.z, lo8.w);
-    e2m1x4_bf16(codes.y & 0xFFFFu, s2, hi8.x, hi8.y);
-    e2m1x4_bf16(codes.y >> 16, s2, hi8.z, hi8.w);
+// 8 e2m1 codes (one 32-bit word) times the fp16 scale pair s2, as 4 fp16 pairs.
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t s2, uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                           uint32_t& o3) {
+    uint32_t a0, a1, a2, a3;
+    asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4; "
+        "cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1; "
+        "cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+        : "r"(w));
+    const __half2 s = *reinterpret_cast<const __half2*>(&s2);
+    __half2 h;
+    h = __hmul2(*reinterpret_cast<const __half2*>(&a0), s); o0 = *reinterpret_cast<const uint32_t*>(&h);
+    h = __hmul2(*reinterpret_cast<const __half2*>(&a1), s); o1 = *reinterpret_cast<const uint32_t*>(&h);
+    h = __hmul2(*reinterpret_cast<const __half2*>(&a2), s); o2 = *reinterpret_cast<const uint32_t*>(&h);
+    h = __hmul2(*reinterpret_cast<const __half2*>(&a3), s); o3 = *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // One dequant warpgroup (128 threads) decodes the K (IS_V false) or V codes of
-// each tile from the raw ring into the bf16 operand tile the MMA reads: K
+// each tile from the raw ring into the fp16 operand tile the MMA reads: K
 // chunk-major across the tile's keys, V page by page, 128-byte swizzled like
-// the TMA-loaded bf16 tiles.  Keys at or past key_hi are written as zeros.
+// the TMA-loaded bf16 tiles.  A unit is one key's 64-element chunk (32 code
+// bytes, 4 scales, one 128-byte swizzle row of the tile); eight consecutive
+// keys of one chunk run side by side, so the row stores hit distinct banks.
+// Keys at or past key_hi are written as zeros.
 template <int D, bool IS_V, bool TRACE>
 __device__ __forceinline__ void dequant(const SplitParams& p, int key_lo, int key_hi, int T, const unsigned char* raw,
-                                        unsigned char* tile, const uint16_t* scale_lut, TcAux* aux,
-                                        volatile int* abort, int dt) {
+                                        unsigned char* tile_ring, TcAux* aux, volatile int* abort, int dt) {
     using L = TcLayout<D, 1>;
     constexpr int NR = L::kNR;
-    constexpr int kPieces = kBN * (D / 16);   // 16-element pieces per tile
+    constexpr int NS = IS_V ? L::kNV : L::kNK;   // operand tile slots
+    constexpr int CPK = D / 64;                  // 64-element chunks per key
+    constexpr int kUnits = kBN * CPK;
     const int lane = dt & 31;
     uint64_t* full = IS_V ? aux->v_full : aux->k_full;
     uint64_t* empty = IS_V ? aux->v_empty : aux->k_empty;
+    // the query tile lands in the V slots: they are free once it is in TMEM
+    if (IS_V && !warp_wait(&aux->q_ready, 0, abort)) return;
     for (int t = 0; t < T; ++t) {
-        const int slot = t % NR;
+        const int slot = t % NR, ts = t % NS;
         if (!warp_wait(&aux->raw_full[slot], (t / NR) & 1, abort)) break;
-        if (t >= 1 && !warp_wait(&empty[0], (t - 1) & 1, abort)) break;
+        if (t >= NS && !warp_wait(&empty[ts], ((t / NS) - 1) & 1, abort)) break;
         const int nvalid = key_hi - (key_lo + t * kBN);
         const unsigned char* src = raw + slot * L::kRawTile;
         const unsigned char* codes = src + (IS_V ? L::kRawVC : 0);
         const unsigned char* scales = src + (IS_V ? L::kRawVS : L::kRawKS);
-#pragma unroll 2
-        for (int u = dt; u < kPieces; u += 128) {
-            const int j = u / (D / 16);           // key within the tile
-            const int e0 = (u % (D / 16)) * 16;   // first head_dim element
+        unsigned char* tile = tile_ring + ts * L::kTileBytes;
+        for (int u = dt; u < kUnits; u += 128) {
+            // u -> (group of 8 keys, chunk c, key within the group)
+            const int j = (u / (8 * CPK)) * 8 + (u & 7);
+            const int c = (u >> 3) % CPK;
             const int pg = j >> 4, sl = j & 15;
-            uint4 lo8 = make_uint4(0u, 0u, 0u, 0u), hi8 = lo8;
+            uint4 outp[8];
             if (j < nvalid) {
-                const uint2 cw = *reinterpret_cast<const uint2*>(codes + pg * L::kRawCodePage + sl * (D / 2) + e0 / 2);
-                decode16(cw, scale_lut[scales[pg * L::kRawScalePage + sl * (D / 16) + e0 / 16]], lo8, hi8);
+                const unsigned char* kr = codes + pg * L::kRawCodePage + sl * (D / 2);
+                const uint4 w0 = *reinterpret_cast<const uint4*>(kr + raw_code_chunk<D>(sl, 2 * c) * 16);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(kr + raw_code_chunk<D>(sl, 2 * c + 1) * 16);
+                const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + pg * L::kRawScalePage +
+                                                                        sl * (D / 16) + c * 4);
+                const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    // word q holds elements 8q .. 8q + 7 of the chunk; block scale q / 2
+                    const uint32_t s2 = e4m3_pair_f16x2((sc4 >> (8 * (q >> 1))) & 0xFFu);
+                    e2m1x8_f16(words[q], s2, outp[q].x, outp[q].y, outp[q].z, outp[q].w);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) outp[q] = make_uint4(0u, 0u, 0u, 0u);
             }
-            const int c = e0 >> 6, q = (e0 & 63) >> 3;   // 64-element chunk, 16-byte piece
             unsigned char* row = IS_V ? tile + pg * L::kPageBytes + c * 2048 + sl * 128
                                       : tile + c * (kBN * 128) + j * 128;
-            *reinterpret_cast<uint4*>(row + ((q ^ (j & 7)) << 4)) = lo8;
-            *reinterpret_cast<uint4*>(row + (((q + 1) ^ (j & 7)) << 4)) = hi8;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(row + ((q ^ (j & 7)) << 4)) = outp[q];
         }
-        if (TRACE && IS_V && dt < kPPT) aux->pages_v[0][dt] = aux->raw_pages[slot][dt];
+        if (TRACE && IS_V && dt < kPPT) aux->pages_v[ts][dt] = aux->raw_pages[slot][dt];
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&full[0]);
+            mbar_arrive(&full[ts]);
             mbar_arrive(&aux->raw_empty[slot]);
         }
     }
@@ -372,7 +411,8 @@ __device__ __forceinline__ void drain_copies(uint64_t* full, int issued) {
 template <int D, int KV, bool TRACE>
 __global__ void __launch_bounds__(KV ? kTcThreadsFp4 : kTcThreadsBf16, 1)
 split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tmq,
-                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const __grid_constant__ CUtensorMap tmks, const __grid_constant__ CUtensorMap tmvs) {
     using L = TcLayout<D, KV>;
     constexpr int NK = L::kNK, NV = L::kNV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -381,13 +421,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* sQ = smem;
-    unsigned char* sP = sQ + L::kQBytes;
+    unsigned char* sP = smem + L::kQSmem;
     unsigned char* sK = sP + L::kPBytes;
     unsigned char* sV = sK + NK * L::kTileBytes;
+    unsigned char* sQ = KV ? sV : smem;   // NVFP4: the query tile lands in the V slots
     unsigned char* sRaw = sV + NV * L::kTileBytes;   // NVFP4 only
-    uint16_t* sLut = reinterpret_cast<uint16_t*>(sRaw + L::kNR * L::kRawTile);   // NVFP4 only
-    TcAux* aux = reinterpret_cast<TcAux*>(sRaw + L::kNR * L::kRawTile + L::kLutBytes);
+    TcAux* aux = reinterpret_cast<TcAux*>(sRaw + L::kNR * L::kRawTile);
     volatile int* abort = &aux->abort;
 
     if (tid == 0) {
@@ -402,7 +441,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             mbar_init(&aux->v_empty[s], 1);
         }
         for (int s = 0; s < L::kNR; ++s) {
-            mbar_init(&aux->raw_full[s], 32);
+            mbar_init(&aux->raw_full[s], 1);
             mbar_init(&aux->raw_empty[s], 8);
         }
         for (int b = 0; b < 2; ++b) {
@@ -414,14 +453,18 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         mbar_init(&aux->o_done, 1);
         mbar_init(&aux->o_final, 1);
         mbar_init(&aux->q_full, 1);
+        mbar_init(&aux->q_ready, 4);
         mbar_init(&aux->drain, 1);
+        mbar_init(&aux->drain_pv, 1);
         aux->abort = 0;
         fence_mbarrier_init();
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmq);
-        if (!KV) {
-            tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        if (KV) {
+            tma_prefetch_desc(&tmks);
+            tma_prefetch_desc(&tmvs);
         }
     }
     if (warp == 1) tmem_alloc(&aux->tmem_base, L::kTmemCols);
@@ -472,8 +515,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         }
         __syncwarp();
         if constexpr (KV) {
-            produce_raw<D>(p, r, kvh, key_lo, key_hi, T, sRaw, aux, abort, lane, pre0, pre1);
-            if (*abort && lane == 0) atomicOr(p.status, kDevWaitTimeout);
+            const int issued = produce_raw<D>(p, r, kvh, key_lo, key_hi, T, sRaw, aux, &tmk, &tmv, &tmks, &tmvs,
+                                              abort, lane, pre0, pre1);
+            if (*abort && lane == 0) {
+                drain_copies<L::kNR>(aux->raw_full, issued);
+                atomicOr(p.status, kDevWaitTimeout);
+            }
         } else {
             const int issued = produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK, aux->k_full,
                                                             aux->k_empty, aux->list_k, aux, &tmk, abort, lane,
@@ -496,44 +543,96 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     } else if (KV && warp >= 8) {
         // ------------------------------------------------------------ NVFP4 dequant (K: 8-11, V: 12-15)
         // e4m3 -> bf16 table for the block scales, from the format definition
-        sLut[tid - 256] = __bfloat16_as_ushort(__float2bfloat16_rn(e4m3_to_float(static_cast<uint32_t>(tid - 256))));
-        asm volatile("bar.sync 1, 256;" ::: "memory");   // the two dequant warpgroups only
         if (warp < 12)
-            dequant<D, false, TRACE>(p, key_lo, key_hi, T, sRaw, sK, sLut, aux, abort, tid - 256);
+            dequant<D, false, TRACE>(p, key_lo, key_hi, T, sRaw, sK, aux, abort, tid - 256);
         else
-            dequant<D, true, TRACE>(p, key_lo, key_hi, T, sRaw, sV, sLut, aux, abort, tid - 384);
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Issues S_t = Q K_t^T and O += P_t V_t in whichever order their inputs
-        // become ready (non-blocking polls), so a late K tile never holds back
-        // a P V and vice versa.
+            dequant<D, true, TRACE>(p, key_lo, key_hi, T, sRaw, sV, aux, abort, tid - 384);
+    } else if (warp == 1 || (KV && warp == 3)) {
+        // ------------------------------------------------------------ MMA issuers
+        // bf16: warp 1 issues S_t = Q K_t^T and O += P_t V_t in whichever order
+        // their inputs become ready (non-blocking polls), so a late K tile never
+        // holds back a P V and vice versa.  NVFP4: warp 1 issues the S MMAs and
+        // warp 3 the P V MMAs, each in tile order with blocking (bounded) waits,
+        // so neither stream waits behind the other's barriers.
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kBN, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kM, D, 0, 1);
+            // NVFP4: fp16 operands (query tile in TMEM, K / V decoded, P fp16);
+            // bf16 KV: bf16 operands
+            constexpr uint32_t idesc_s = KV ? idesc_f16_f32(kM, kBN, 0, 0) : idesc_bf16_f32(kM, kBN, 0, 0);
+            constexpr uint32_t idesc_o = KV ? idesc_f16_f32(kM, D, 0, 1) : idesc_bf16_f32(kM, D, 0, 1);
             const uint32_t q_addr = smem_addr(sQ);
             const uint32_t p_addr = smem_addr(sP);
-            bool ok = mbar_wait(&aux->q_full, 0, abort, kWaitLimit);
+            const bool pv_issuer = KV && warp == 3;
+            bool ok = pv_issuer || mbar_wait(KV ? &aux->q_ready : &aux->q_full, 0, abort, kWaitLimit);
             tc_fence_after();
             int ns = 0, npv = 0;
+            constexpr int NSB = L::kSBufs;
+            // S_n = Q K_n^T into S buffer n % NSB
+            auto issue_s = [&](int n) {
+                const int ks = n % NK, b = n % NSB;
+                tc_fence_after();
+                const uint32_t k_addr = smem_addr(sK + ks * L::kTileBytes);
+                const uint32_t d_tmem = tmem + D + b * kBN;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c = kk >> 2, sub = kk & 3;
+                    const uint64_t bd = smem_desc_sw128(k_addr + c * (kBN * 128) + sub * 32, 16, 1024);
+                    if constexpr (KV) {
+                        // query elements 16 kk .. 16 kk + 15: TMEM columns 8 kk .. 8 kk + 7
+                        mma_f16_ts(d_tmem, tmem + L::kQCol + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    } else {
+                        const uint64_t a = smem_desc_sw128(q_addr + c * (kM * 128) + sub * 32, 16, 1024);
+                        mma_bf16_ss(d_tmem, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(&aux->k_empty[ks]);
+                mma_commit(&aux->s_full[b]);
+            };
+            // O += P_n V_n, one MMA per 16-key page
+            auto issue_pv = [&](int n) {
+                const int vs = n % NV, b = n & 1;
+                tc_fence_after();
+                const int np = min(kPPT, (key_hi - (key_lo + n * kBN) + 15) / 16);
+                const uint32_t v_addr = smem_addr(sV + vs * L::kTileBytes);
+                for (int kk = 0; kk < np; ++kk) {
+                    // V page kk: [chunk][16 keys][128 B]; MN atoms (64 head_dim
+                    // elements) 2 KB apart, 8-key groups 1 KB apart
+                    const uint64_t bd = smem_desc_sw128(v_addr + kk * L::kPageBytes, 2048, 1024);
+                    if constexpr (KV) {
+                        // P keys 16 kk .. 16 kk + 15: TMEM columns 8 kk .. 8 kk + 7 of buffer b
+                        mma_f16_ts(tmem, tmem + L::kPCol + b * (kBN / 2) + kk * 8, bd, idesc_o,
+                                   (n > 0 || kk > 0) ? 1u : 0u);
+                    } else {
+                        const uint64_t a = smem_desc_sw128(p_addr + p_tile_offset(b) + kk * 32, 16, 1024);
+                        mma_bf16_ss(tmem, a, bd, idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&aux->v_empty[vs]);
+                mma_commit(&aux->p_free[b]);
+                mma_commit(&aux->o_done);
+            };
             long long t_idle = clock64();
-            while (ok && npv < T) {
+            if constexpr (KV) {
+                if (!pv_issuer) {
+                    for (int t = 0; t < T && ok; ++t) {
+                        ok = mbar_wait(&aux->k_full[t % NK], (t / NK) & 1, abort, kWaitLimit) &&
+                             (t < NSB || mbar_wait(&aux->s_empty[t % NSB], ((t / NSB) - 1) & 1, abort, kWaitLimit));
+                        if (ok) issue_s(t);
+                    }
+                } else {
+                    for (int t = 0; t < T && ok; ++t) {
+                        ok = mbar_wait(&aux->p_full[t & 1], (t >> 1) & 1, abort, kWaitLimit) &&
+                             mbar_wait(&aux->v_full[t % NV], (t / NV) & 1, abort, kWaitLimit);
+                        if (ok) issue_pv(t);
+                    }
+                }
+            }
+            while (!KV && ok && npv < T) {
                 bool progressed = false;
                 if (ns < T) {
-                    const int ks = ns % NK, b = ns & 1;
+                    const int ks = ns % NK, b = ns % NSB;
                     if (mbar_test_wait(&aux->k_full[ks], (ns / NK) & 1) &&
-                        (ns < 2 || mbar_test_wait(&aux->s_empty[b], ((ns >> 1) - 1) & 1))) {
-                        tc_fence_after();
-                        const uint32_t k_addr = smem_addr(sK + ks * L::kTileBytes);
-                        const uint32_t d_tmem = tmem + D + b * kBN;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const int c = kk >> 2, sub = kk & 3;
-                            const uint64_t a = smem_desc_sw128(q_addr + c * (kM * 128) + sub * 32, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(k_addr + c * (kBN * 128) + sub * 32, 16, 1024);
-                            mma_bf16_ss(d_tmem, a, bd, idesc_s, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&aux->k_empty[ks]);
-                        mma_commit(&aux->s_full[b]);
+                        (ns < NSB || mbar_test_wait(&aux->s_empty[b], ((ns / NSB) - 1) & 1))) {
+                        issue_s(ns);
                         ++ns;
                         progressed = true;
                     }
@@ -542,19 +641,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     const int vs = npv % NV, b = npv & 1;
                     if (mbar_test_wait(&aux->p_full[b], (npv >> 1) & 1) &&
                         mbar_test_wait(&aux->v_full[vs], (npv / NV) & 1)) {
-                        tc_fence_after();
-                        const int np = min(kPPT, (key_hi - (key_lo + npv * kBN) + 15) / 16);
-                        const uint32_t v_addr = smem_addr(sV + vs * L::kTileBytes);
-                        for (int kk = 0; kk < np; ++kk) {
-                            const uint64_t a = smem_desc_sw128(p_addr + p_tile_offset(b) + kk * 32, 16, 1024);
-                            // V page kk: [chunk][16 keys][128 B]; MN atoms (64 head_dim
-                            // elements) 2 KB apart, 8-key groups 1 KB apart
-                            const uint64_t bd = smem_desc_sw128(v_addr + kk * L::kPageBytes, 2048, 1024);
-                            mma_bf16_ss(tmem, a, bd, idesc_o, (npv > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&aux->v_empty[vs]);
-                        mma_commit(&aux->p_free[b]);
-                        mma_commit(&aux->o_done);
+                        issue_pv(npv);
                         ++npv;
                         progressed = true;
                     }
@@ -571,11 +658,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             // O is final once every P V is done.  A separate barrier: the softmax
             // warps can finish their loop while two P V are still pending, and a
             // parity wait on o_done would then match an older phase.
-            if (ok) mma_commit(&aux->o_final);
+            if (ok && (!KV || pv_issuer)) mma_commit(&aux->o_final);
             // every MMA this thread issued completes before TMEM is released
-            mma_commit(&aux->drain);
+            uint64_t* drain = pv_issuer ? &aux->drain_pv : &aux->drain;
+            mma_commit(drain);
             volatile int no_abort = 0;
-            mbar_wait(&aux->drain, 0, &no_abort, kDrainLimit);
+            mbar_wait(drain, 0, &no_abort, kDrainLimit);
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -592,18 +680,48 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         float m_ref = -INFINITY, l_sum = 0.f;
         long long tr_cnt = 0, tr_sum = 0;
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
-            const int b = t & 1;
-            if (!(ok = warp_wait(&aux->s_full[b], (t >> 1) & 1, abort))) break;
+        if constexpr (KV) {
+            // The query tile arrives as bf16 (in the V slots); the NVFP4 MMAs
+            // take fp16.  Thread m converts its row (saturating at +-65504; exact
+            // for every bf16 value of magnitude 2^-14 .. 65504) into the TMEM
+            // columns the S = Q K^T MMA reads as its A operand, two elements per
+            // column, the lower one in the low half.
+            if ((ok = warp_wait(&aux->q_full, 0, abort))) {
+                const uint32_t qb = smem_addr(sQ);
+#pragma unroll 1
+                for (int c = 0; c < L::kChunks; ++c) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        // logical 16-byte piece q of row m sits at piece q ^ (m & 7)
+                        const uint4 v = ld_shared_v4(qb + c * (kM * 128) + m * 128 + ((q ^ (m & 7)) << 4));
+                        w[4 * q + 0] = bf16x2_to_f16x2_sat(v.x);
+                        w[4 * q + 1] = bf16x2_to_f16x2_sat(v.y);
+                        w[4 * q + 2] = bf16x2_to_f16x2_sat(v.z);
+                        w[4 * q + 3] = bf16x2_to_f16x2_sat(v.w);
+                    }
+                    tmem_st32u(lane_tmem + L::kQCol + c * 32, w);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&aux->q_ready);
+            }
+        }
+        for (int t = 0; t < T && ok; ++t) {
+            const int b = t & 1;                      // P buffer
+            constexpr int NSB = L::kSBufs;
+            const int sb = t % NSB;                   // S buffer
+            if (!(ok = warp_wait(&aux->s_full[sb], (t / NSB) & 1, abort))) break;
             tc_fence_after();
             float sv[kBN];
 #pragma unroll
             for (int h = 0; h < kBN / 32; ++h)
-                tmem_ld32(lane_tmem + D + b * kBN + h * 32, *reinterpret_cast<float(*)[32]>(sv + h * 32));
+                tmem_ld32(lane_tmem + D + sb * kBN + h * 32, *reinterpret_cast<float(*)[32]>(sv + h * 32));
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&aux->s_empty[b]);
+            if (lane == 0) mbar_arrive(&aux->s_empty[sb]);
 
             const int key0 = key_lo + t * kBN;
             const int lim = valid ? (min(key_hi - 1, hi) - key0) : -1;  // visible iff c <= lim
@@ -633,12 +751,16 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             for (int c = 0; c < kBN; c += 2) {
                 const float p0 = fast_exp2(fmaf(sv[c], sc, nref));
                 const float p1 = fast_exp2(fmaf(sv[c + 1], sc, nref));
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                // the normaliser sums the fp32 weights: rounding P to bf16 for
+                // the normaliser sums the fp32 weights: rounding P to 16 bits for
                 // the PV MMA must not leak into l (and so into LSE) on rows
                 // that see only a few keys
                 psum += p0 + p1;
-                pk[c >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+                if constexpr (KV) {
+                    pk[c >> 1] = pack_half2(p0, p1);
+                } else {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                    pk[c >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
             }
             l_sum = l_sum * alpha + psum;
             m_ref = ref;
@@ -688,14 +810,22 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     tr_sum += (long long)aux->pages_v[vs][c >> 4] * 16 + (key & 15);
                 }
             }
-            // P row m into buffer b of the 128-byte-swizzled K-major A tile
+            if constexpr (KV) {
+                // P row m (fp16 pairs, key 2c in the low half) into TMEM buffer b
+                static_assert(kBN == 64, "one 32-column store per P row");
+                tmem_st32u(lane_tmem + L::kPCol + b * (kBN / 2), pk);
+                tmem_wait_st();
+            } else {
+                // P row m into buffer b of the 128-byte-swizzled K-major A tile
 #pragma unroll
-            for (int j = 0; j < kBN / 8; ++j) {
-                const int chunk = (kBN == 32 ? b * 4 : 0) + j;
-                *reinterpret_cast<uint4*>(sP + (kBN == 64 ? b * (kM * 128) : 0) + m * 128 + ((chunk ^ (m & 7)) << 4)) =
-                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                for (int j = 0; j < kBN / 8; ++j) {
+                    const int chunk = (kBN == 32 ? b * 4 : 0) + j;
+                    *reinterpret_cast<uint4*>(sP + (kBN == 64 ? b * (kM * 128) : 0) + m * 128 +
+                                              ((chunk ^ (m & 7)) << 4)) =
+                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aux->p_full[b]);
@@ -844,7 +974,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     }
 }
 
-using TcKernel = void (*)(const SplitParams, const CUtensorMap, const CUtensorMap, const CUtensorMap);
+using TcKernel = void (*)(const SplitParams, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                          const CUtensorMap, const CUtensorMap);
 
 template <int D, int KV>
 TcKernel pick_trace(bool traced) {
@@ -918,6 +1049,40 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int hkv,
     return res == CUDA_SUCCESS;
 }
 
+// NVFP4 code pool [num_pages, Hkv, 16, d/2] bytes viewed as (d/2 bytes, slot,
+// page-head); box = one page-head, swizzled 128/64/32 bytes for d = 256/128/64
+// (the row is d/2 bytes).
+bool encode_code_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d / 2, 16, (cuuint64_t)num_pages * hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)d / 2, (cuuint64_t)d / 2 * 16};
+    cuuint32_t box[3] = {(cuuint32_t)d / 2, 16, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = d == 256 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+// NVFP4 scale pool [num_pages, Hkv, 16, d/16] bytes viewed as (d bytes, page-head);
+// box = one page-head's scales.
+bool encode_scale_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)num_pages * hkv};
+    cuuint64_t strides[1] = {(cuuint64_t)d};
+    cuuint32_t box[2] = {(cuuint32_t)d, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
 // Q [total_rows, Hq, d] bf16 viewed as (d, head, row); box = 64 elements x G heads
 // x max_w rows, 128-byte swizzle, out-of-range rows zero-filled.
 bool encode_q_map(CUtensorMap* map, const void* q, int total_rows, int hq, int d, int group, int max_w) {
@@ -958,11 +1123,17 @@ bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
     if (!encode_q_map(reinterpret_cast<CUtensorMap*>(maps->q), p.q, p.total_rows, p.num_q_heads, p.head_dim,
                       p.group, p.max_w))
         return false;
-    if (kv_dtype != 0) {   // NVFP4 pools are read with cp.async, not TMA
-        memset(maps->k, 0, sizeof(maps->k));
-        memset(maps->v, 0, sizeof(maps->v));
-        return true;
-    }
+    if (kv_dtype != 0)
+        return encode_code_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
+                               p.head_dim) &&
+               encode_code_map(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,
+                               p.head_dim) &&
+               encode_scale_map(reinterpret_cast<CUtensorMap*>(maps->ks), p.k_scales, p.num_pages,
+                                p.num_kv_heads, p.head_dim) &&
+               encode_scale_map(reinterpret_cast<CUtensorMap*>(maps->vs), p.v_scales, p.num_pages,
+                                p.num_kv_heads, p.head_dim);
+    memset(maps->ks, 0, sizeof(maps->ks));
+    memset(maps->vs, 0, sizeof(maps->vs));
     return encode_pool_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
                            p.head_dim) &&
            encode_pool_map_pages(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,
@@ -985,7 +1156,9 @@ cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bo
     lc.numAttrs = programmatic ? 1 : 0;
     return cudaLaunchKernelEx(&lc, k, p, *reinterpret_cast<const CUtensorMap*>(maps.q),
                               *reinterpret_cast<const CUtensorMap*>(maps.k),
-                              *reinterpret_cast<const CUtensorMap*>(maps.v));
+                              *reinterpret_cast<const CUtensorMap*>(maps.v),
+                              *reinterpret_cast<const CUtensorMap*>(maps.ks),
+                              *reinterpret_cast<const CUtensorMap*>(maps.vs));
 }
 
 }  // namespace spec_attn
