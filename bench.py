@@ -116,7 +116,7 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+        return {"sm_mhz": statistics.mean(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
 
 
@@ -337,9 +337,9 @@ def run_ours(args, rank, world, local_rank):
         ts, _ = time_calls([dw], flush, max(10, args.steps), 3, stream)
         te, _ = time_calls([dw], flush, max(10, args.steps), 3, stream, graphs=False)
         _, sk = time_calls([dw], flush, max(10, args.steps), 3, stream, timing_events=True)
-        us = statistics.median(ts) * 1e3
+        us = statistics.mean(ts) * 1e3
         per_call.append({"workload": wl.name, "w": wl.max_w, "us": round(us, 2),
-                         "us_eager": round(statistics.median(te) * 1e3, 2),
+                         "us_eager": round(statistics.mean(te) * 1e3, 2),
                          "gbs": round(wl.kv_bytes / (us * 1e-6) / 1e9, 1),
                          "pct_peak": round(100 * wl.kv_bytes / (us * 1e-6) / 1e9 / peak, 1),
                          "split_kernel_us": round(sk[0] * 1e3, 2), "plan": dw.plan.info})
@@ -365,7 +365,7 @@ def run_ours(args, rank, world, local_rank):
                 dw = sa.DeviceWorkload(wl, dev, kernel_variant=sa.SPEC_ATTN_VARIANT_AUTO)
             ts, _ = time_calls([dw], flush, max(10, args.steps), 3, stream)
             _, sk = time_calls([dw], flush, max(10, args.steps), 3, stream, timing_events=True)
-            us = statistics.median(ts) * 1e3
+            us = statistics.mean(ts) * 1e3
             gbs = wl.kv_bytes / (us * 1e-6) / 1e9
             table.append({"workload": name, "us": round(us, 2), "gbs": round(gbs, 1),
                           "split_kernel_us": round(sk[0] * 1e3, 2),

@@ -165,10 +165,10 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 with fp16 inputs: A (M x 16)
-// is read from TMEM columns a_tmem .. a_tmem + 7, two fp16 per column with the
-// lower k in the low half.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (fp16 or bf16 inputs, as the
+// instruction descriptor says): A (M x 16) is read from TMEM columns
+// a_tmem .. a_tmem + 7, two elements per column with the lower k in the low half.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"

@@ -13,29 +13,29 @@
 //
 // Warp roles, bf16 KV (256 threads):
 //   warp 0      loads the query tile once (TMA, one box per 64 head_dim
-//               elements covering G heads x max_w window rows), then streams
-//               the K tiles: 64 keys (four 16-key pages, one 2 KB box per page
-//               and 64 head_dim elements, issued from 16 lanes), 128-byte
-//               swizzled, chunk-major, into a ring of slots.
-//   warp 2      streams the V tiles into a second ring, one box per page-head
-//               (a K slot frees as soon as its S is computed, a V slot only
-//               after P V).
-//   warp 1      allocates TMEM; one lane issues the MMAs as their inputs land:
-//                 S_t = Q K_t^T   (M 128, N 64, -> fp32 in TMEM, double-buffered)
-//                 O  += P_t V_t   (M 128, N head_dim, one MMA per page, V MN-major)
-//   warp 3      idle.
-//   warps 4-7   softmax: thread m owns row m (TMEM lane m).  Per tile it reads
-//               its 64 scores, applies the causal-in-block / non-causal mask by
-//               key index, updates a base-2 online softmax whose reference
-//               maximum moves only when a score exceeds it by more than 2^8
-//               (then the row of O in TMEM is rescaled), and writes P into
-//               one half of a double buffer; at the end it normalises O and
-//               stages the row for the output (or a split partial), which
-//               every warp then copies out.
-// NVFP4 KV (512 threads): warp 0 copies the tiles' codes and scales with
-// cp.async into a raw ring instead of TMA; warps 8-11 decode K and 12-15 decode
-// V into fp16 operand tiles; the softmax warps first convert the query tile to
-// fp16 in place, and P (fp16) goes to TMEM, where the P V MMA reads it.
+//               elements covering G heads x max_w window rows, into the V
+//               slots), then streams the K tiles: 64 keys (four 16-key pages,
+//               one 2 KB box per page and 64 head_dim elements, issued from 16
+//               lanes), 128-byte swizzled, chunk-major, into a ring of slots.
+//   warp 2      streams the V tiles into a second ring, one box per page-head,
+//               once the query tile has left the V slots.
+//   warp 1      allocates TMEM and issues S_t = Q K_t^T (M 128, N 64, query
+//               tile from TMEM, -> fp32 in TMEM, double-buffered).
+//   warp 3      issues O += P_t V_t (M 128, N head_dim, one MMA per page, P
+//               from shared memory, V MN-major).  Each issuer waits only on its
+//               own inputs, in tile order.
+//   warps 4-7   softmax: thread m owns row m (TMEM lane m).  First it moves its
+//               query row into TMEM.  Per tile it reads its 64 scores, applies
+//               the causal-in-block / non-causal mask by key index, updates a
+//               base-2 online softmax whose reference maximum moves only when a
+//               score exceeds it by more than 2^8 (then the row of O in TMEM is
+//               rescaled), and writes P into one half of a double buffer; at
+//               the end it normalises O and stages the row for the output (or a
+//               split partial), which every warp then copies out.
+// NVFP4 KV (512 threads): warp 0 streams the tiles' codes and scales by TMA
+// into a raw ring; warps 8-11 decode K and 12-15 decode V into fp16 operand
+// tiles; the query row is converted to fp16 on its way into TMEM, S is single-
+// buffered, and P (fp16) goes to TMEM, where the P V MMA reads it.
 //
 // Every wait on an mbarrier is bounded: on time-out the CTA raises the
 // device-status bit, stops issuing, drains its in-flight copies and MMAs,
@@ -68,21 +68,22 @@ constexpr int kPageListCap = 64;                 // page ids staged in shared me
 constexpr int kMaxNR = 8;                        // NVFP4 raw (codes + scales) ring slots
 constexpr int kMaxNK = 8, kMaxNV = 16;
 
-// Shared memory: [query tile] | P tile | K ring | V ring | [NVFP4 raw ring] | barriers.
-// bf16 KV: the query tile, P (bf16) and the K and V tiles are MMA operands in
-// shared memory; K and V arrive by TMA into rings of kNK / kNV slots.
+// Shared memory: [P tile] | K ring | V ring | [NVFP4 raw ring] | barriers.
+// The query tile lands (bf16, by TMA) in the V slots before any V does; the
+// softmax warps move it into TMEM (NVFP4: converted to fp16), where the
+// S = Q K^T MMA reads its A operand.  An MMA with its A operand in TMEM issues
+// at about twice the rate of one reading it from shared memory, and the
+// 128-row tile costs no shared memory or shared-memory bandwidth.
+// bf16 KV: K and V arrive by TMA into rings of kNK / kNV slots; P (bf16) is an
+// A operand in shared memory.
 // NVFP4 KV: codes and scales arrive by TMA into a ring of kNR raw slots and are
-// decoded into fp16 K and V operand tiles (two slots each).  The query tile
-// lands (bf16, by TMA) in the V slots, which it exactly fills, and the softmax
-// warps move it, converted to fp16, into TMEM; P (fp16) is written to TMEM too.
-// Both MMAs then take their A operand from TMEM: that keeps the 128-row tiles
-// out of shared memory, whose bandwidth the decode needs, and an MMA with its
-// A operand in TMEM issues at about twice the rate.
+// decoded into fp16 K and V operand tiles (two slots each); P (fp16) is
+// written to TMEM, where the P V MMA reads it.
 template <int D, int KV>
 struct TcLayout {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along head_dim
     static constexpr int kQBytes = kM * D * 2;             // the query tile (16-bit elements)
-    static constexpr int kQSmem = KV ? 0 : kQBytes;        // its own region in the shared-memory layout
+    static constexpr int kQSmem = 0;                       // no region of its own: it lands in the V slots
     // P: two tiles (double buffer).  32-key tiles share each 128-byte swizzle row
     // (one half each); 64-key tiles fill a row, so the buffers are separate.
     static constexpr int kPBytes = KV ? 0 : kM * 128 * (kBN == 64 ? 2 : 1);
@@ -98,25 +99,27 @@ struct TcLayout {
     static constexpr int kMaxDyn = 232448;                  // 227 KB opt-in limit
     static constexpr int kFixed = 1024 + kQSmem + kPBytes + kAuxBytes;
     static constexpr int kRing = (kMaxDyn - kFixed) / kTileBytes;
-    // bf16: K tiles are released as soon as their S = Q K^T is done, V tiles only
-    // after P V, so V gets the larger share of the ring.
-    static constexpr int kNK = KV ? 2 : ((kRing / 3) > kMaxNK ? kMaxNK : ((kRing / 3) < 2 ? 2 : (kRing / 3)));
+    // bf16: the ring is split evenly: every tile needs its K and its V, and
+    // loads land in about the order they are issued, so a V ring running far
+    // ahead of a short K ring only delays the K tiles the next S waits for.
+    static constexpr int kNK = KV ? 2 : ((kRing / 2) > kMaxNK ? kMaxNK : ((kRing / 2) < 2 ? 2 : (kRing / 2)));
     static constexpr int kNV = KV ? 2 : ((kRing - kNK) > kMaxNV ? kMaxNV : (kRing - kNK));
     static constexpr int kRawFit = (kMaxDyn - kFixed - (kNK + kNV) * kTileBytes) / kRawTile;
     static constexpr int kNR = KV ? (kRawFit > kMaxNR ? kMaxNR : kRawFit) : 0;
     static constexpr int kSmem = kFixed + (kNK + kNV) * kTileBytes + kNR * kRawTile;
-    // TMEM columns.  bf16: O [0, D), S double buffer [D, D + 2 BN).  NVFP4: O
-    // [0, D), S single buffer [D, D + BN), P double buffer (fp16 pairs)
-    // [D + BN, D + 2 BN), query tile (fp16 pairs) [D + 2 BN, D + 2 BN + D / 2).
+    // TMEM columns.  bf16: O [0, D), S double buffer [D, D + 2 BN), query tile
+    // (bf16 pairs) [D + 2 BN, D + 2 BN + D / 2).  NVFP4: O [0, D), S single
+    // buffer [D, D + BN), P double buffer (fp16 pairs) [D + BN, D + 2 BN),
+    // query tile (fp16 pairs) [D + 2 BN, D + 2 BN + D / 2).
     static constexpr int kSBufs = KV ? 1 : 2;
     static constexpr int kPCol = D + kBN;
     static constexpr int kQCol = D + 2 * kBN;
-    static constexpr int kTmemNeed = D + 2 * kBN + (KV ? D / 2 : 0);
+    static constexpr int kTmemNeed = D + 2 * kBN + D / 2;
     static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128u : (kTmemNeed <= 256 ? 256u : 512u);
     static_assert(KV ? (kNR >= 2) : (kNK >= 2 && kNV >= 2), "ring too small");
     static_assert(kSmem <= kMaxDyn, "shared memory");
     static_assert(kTmemNeed <= 512, "tensor memory");
-    static_assert(!KV || kQBytes == kNV * kTileBytes, "NVFP4: the query tile lands in the V slots");
+    static_assert(kQBytes <= kNV * kTileBytes, "the query tile lands in the V slots");
     // the epilogue stages kM rows of fp32 O (+16 B padding) and kM row scales
     // over the query/P/operand/raw buffers (all idle by then)
     static_assert(kM * (D * 4 + 16) + kM * 4 <= kQSmem + kPBytes + (kNK + kNV) * kTileBytes + kNR * kRawTile,
@@ -137,7 +140,7 @@ struct TcAux {
     uint64_t q_full;
     uint64_t q_ready;    // NVFP4: the query tile converted to fp16 (one arrival per softmax warp)
     uint64_t drain;
-    uint64_t drain_pv;   // NVFP4: the P V issuer's own MMAs
+    uint64_t drain_pv;   // the P V issuer's own MMAs
     uint64_t raw_full[kMaxNR];             // NVFP4: codes/scales of a tile landed (32 lane arrivals)
     uint64_t raw_empty[kMaxNR];            // NVFP4: both dequant warpgroups are done with a raw slot
     int32_t pages_v[kMaxNV][kPPT];         // physical pages of each V slot (index trace)
@@ -424,7 +427,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     unsigned char* sP = smem + L::kQSmem;
     unsigned char* sK = sP + L::kPBytes;
     unsigned char* sV = sK + NK * L::kTileBytes;
-    unsigned char* sQ = KV ? sV : smem;   // NVFP4: the query tile lands in the V slots
+    unsigned char* sQ = sV;   // the query tile lands in the V slots, then moves to TMEM
     unsigned char* sRaw = sV + NV * L::kTileBytes;   // NVFP4 only
     TcAux* aux = reinterpret_cast<TcAux*>(sRaw + L::kNR * L::kRawTile);
     volatile int* abort = &aux->abort;
@@ -534,10 +537,14 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     } else if (warp == 2) {
         // ------------------------------------------------------------ V producer (bf16)
         if constexpr (!KV) {
-            const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
-                                                           aux->v_empty, aux->list_v, aux, &tmv, abort, lane,
-                                                           pre0, pre1);
-            if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
+            // the query tile sits in the V slots until the softmax warps have
+            // moved it into TMEM
+            if (warp_wait(&aux->q_ready, 0, abort)) {
+                const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
+                                                               aux->v_empty, aux->list_v, aux, &tmv, abort, lane,
+                                                               pre0, pre1);
+                if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
+            }
         }
         __syncwarp();
     } else if (KV && warp >= 8) {
@@ -547,24 +554,20 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             dequant<D, false, TRACE>(p, key_lo, key_hi, T, sRaw, sK, aux, abort, tid - 256);
         else
             dequant<D, true, TRACE>(p, key_lo, key_hi, T, sRaw, sV, aux, abort, tid - 384);
-    } else if (warp == 1 || (KV && warp == 3)) {
+    } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ MMA issuers
-        // bf16: warp 1 issues S_t = Q K_t^T and O += P_t V_t in whichever order
-        // their inputs become ready (non-blocking polls), so a late K tile never
-        // holds back a P V and vice versa.  NVFP4: warp 1 issues the S MMAs and
-        // warp 3 the P V MMAs, each in tile order with blocking (bounded) waits,
-        // so neither stream waits behind the other's barriers.
+        // Warp 1 issues S_t = Q K_t^T and warp 3 O += P_t V_t, each in tile order
+        // with blocking (bounded) waits on its own inputs only: a late K tile
+        // never holds back a P V, nor a P not yet written the next S.
         if (lane == 0) {
             // NVFP4: fp16 operands (query tile in TMEM, K / V decoded, P fp16);
             // bf16 KV: bf16 operands
             constexpr uint32_t idesc_s = KV ? idesc_f16_f32(kM, kBN, 0, 0) : idesc_bf16_f32(kM, kBN, 0, 0);
             constexpr uint32_t idesc_o = KV ? idesc_f16_f32(kM, D, 0, 1) : idesc_bf16_f32(kM, D, 0, 1);
-            const uint32_t q_addr = smem_addr(sQ);
             const uint32_t p_addr = smem_addr(sP);
-            const bool pv_issuer = KV && warp == 3;
-            bool ok = pv_issuer || mbar_wait(KV ? &aux->q_ready : &aux->q_full, 0, abort, kWaitLimit);
+            const bool pv_issuer = (warp == 3);
+            bool ok = pv_issuer || mbar_wait(&aux->q_ready, 0, abort, kWaitLimit);
             tc_fence_after();
-            int ns = 0, npv = 0;
             constexpr int NSB = L::kSBufs;
             // S_n = Q K_n^T into S buffer n % NSB
             auto issue_s = [&](int n) {
@@ -576,13 +579,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const int c = kk >> 2, sub = kk & 3;
                     const uint64_t bd = smem_desc_sw128(k_addr + c * (kBN * 128) + sub * 32, 16, 1024);
-                    if constexpr (KV) {
-                        // query elements 16 kk .. 16 kk + 15: TMEM columns 8 kk .. 8 kk + 7
-                        mma_f16_ts(d_tmem, tmem + L::kQCol + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
-                    } else {
-                        const uint64_t a = smem_desc_sw128(q_addr + c * (kM * 128) + sub * 32, 16, 1024);
-                        mma_bf16_ss(d_tmem, a, bd, idesc_s, kk > 0 ? 1u : 0u);
-                    }
+                    // query elements 16 kk .. 16 kk + 15: TMEM columns 8 kk .. 8 kk + 7
+                    mma_ts(d_tmem, tmem + L::kQCol + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&aux->k_empty[ks]);
                 mma_commit(&aux->s_full[b]);
@@ -599,7 +597,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     const uint64_t bd = smem_desc_sw128(v_addr + kk * L::kPageBytes, 2048, 1024);
                     if constexpr (KV) {
                         // P keys 16 kk .. 16 kk + 15: TMEM columns 8 kk .. 8 kk + 7 of buffer b
-                        mma_f16_ts(tmem, tmem + L::kPCol + b * (kBN / 2) + kk * 8, bd, idesc_o,
+                        mma_ts(tmem, tmem + L::kPCol + b * (kBN / 2) + kk * 8, bd, idesc_o,
                                    (n > 0 || kk > 0) ? 1u : 0u);
                     } else {
                         const uint64_t a = smem_desc_sw128(p_addr + p_tile_offset(b) + kk * 32, 16, 1024);
@@ -611,54 +609,23 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 mma_commit(&aux->o_done);
             };
             long long t_idle = clock64();
-            if constexpr (KV) {
-                if (!pv_issuer) {
-                    for (int t = 0; t < T && ok; ++t) {
-                        ok = mbar_wait(&aux->k_full[t % NK], (t / NK) & 1, abort, kWaitLimit) &&
-                             (t < NSB || mbar_wait(&aux->s_empty[t % NSB], ((t / NSB) - 1) & 1, abort, kWaitLimit));
-                        if (ok) issue_s(t);
-                    }
-                } else {
-                    for (int t = 0; t < T && ok; ++t) {
-                        ok = mbar_wait(&aux->p_full[t & 1], (t >> 1) & 1, abort, kWaitLimit) &&
-                             mbar_wait(&aux->v_full[t % NV], (t / NV) & 1, abort, kWaitLimit);
-                        if (ok) issue_pv(t);
-                    }
+            if (!pv_issuer) {
+                for (int t = 0; t < T && ok; ++t) {
+                    ok = mbar_wait(&aux->k_full[t % NK], (t / NK) & 1, abort, kWaitLimit) &&
+                         (t < NSB || mbar_wait(&aux->s_empty[t % NSB], ((t / NSB) - 1) & 1, abort, kWaitLimit));
+                    if (ok) issue_s(t);
                 }
-            }
-            while (!KV && ok && npv < T) {
-                bool progressed = false;
-                if (ns < T) {
-                    const int ks = ns % NK, b = ns % NSB;
-                    if (mbar_test_wait(&aux->k_full[ks], (ns / NK) & 1) &&
-                        (ns < NSB || mbar_test_wait(&aux->s_empty[b], ((ns / NSB) - 1) & 1))) {
-                        issue_s(ns);
-                        ++ns;
-                        progressed = true;
-                    }
-                }
-                if (npv < ns) {
-                    const int vs = npv % NV, b = npv & 1;
-                    if (mbar_test_wait(&aux->p_full[b], (npv >> 1) & 1) &&
-                        mbar_test_wait(&aux->v_full[vs], (npv / NV) & 1)) {
-                        issue_pv(npv);
-                        ++npv;
-                        progressed = true;
-                    }
-                }
-                if (progressed) {
-                    t_idle = clock64();
-                } else if (*abort) {
-                    ok = false;
-                } else if (clock64() - t_idle > kWaitLimit) {
-                    *abort = 1;
-                    ok = false;
+            } else {
+                for (int t = 0; t < T && ok; ++t) {
+                    ok = mbar_wait(&aux->p_full[t & 1], (t >> 1) & 1, abort, kWaitLimit) &&
+                         mbar_wait(&aux->v_full[t % NV], (t / NV) & 1, abort, kWaitLimit);
+                    if (ok) issue_pv(t);
                 }
             }
             // O is final once every P V is done.  A separate barrier: the softmax
             // warps can finish their loop while two P V are still pending, and a
             // parity wait on o_done would then match an older phase.
-            if (ok && (!KV || pv_issuer)) mma_commit(&aux->o_final);
+            if (ok && pv_issuer) mma_commit(&aux->o_final);
             // every MMA this thread issued completes before TMEM is released
             uint64_t* drain = pv_issuer ? &aux->drain_pv : &aux->drain;
             mma_commit(drain);
@@ -680,12 +647,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         float m_ref = -INFINITY, l_sum = 0.f;
         long long tr_cnt = 0, tr_sum = 0;
         bool ok = true;
-        if constexpr (KV) {
-            // The query tile arrives as bf16 (in the V slots); the NVFP4 MMAs
-            // take fp16.  Thread m converts its row (saturating at +-65504; exact
-            // for every bf16 value of magnitude 2^-14 .. 65504) into the TMEM
-            // columns the S = Q K^T MMA reads as its A operand, two elements per
-            // column, the lower one in the low half.
+        {
+            // The query tile arrives as bf16 in the V slots.  Thread m moves its
+            // row into the TMEM columns the S = Q K^T MMA reads as its A operand,
+            // two elements per column, the lower one in the low half.  NVFP4:
+            // its MMAs take fp16, so the row is converted on the way (saturating
+            // at +-65504; exact for every bf16 value of magnitude 2^-14 .. 65504).
             if ((ok = warp_wait(&aux->q_full, 0, abort))) {
                 const uint32_t qb = smem_addr(sQ);
 #pragma unroll 1
@@ -695,10 +662,17 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     for (int q = 0; q < 8; ++q) {
                         // logical 16-byte piece q of row m sits at piece q ^ (m & 7)
                         const uint4 v = ld_shared_v4(qb + c * (kM * 128) + m * 128 + ((q ^ (m & 7)) << 4));
-                        w[4 * q + 0] = bf16x2_to_f16x2_sat(v.x);
-                        w[4 * q + 1] = bf16x2_to_f16x2_sat(v.y);
-                        w[4 * q + 2] = bf16x2_to_f16x2_sat(v.z);
-                        w[4 * q + 3] = bf16x2_to_f16x2_sat(v.w);
+                        if constexpr (KV) {
+                            w[4 * q + 0] = bf16x2_to_f16x2_sat(v.x);
+                            w[4 * q + 1] = bf16x2_to_f16x2_sat(v.y);
+                            w[4 * q + 2] = bf16x2_to_f16x2_sat(v.z);
+                            w[4 * q + 3] = bf16x2_to_f16x2_sat(v.w);
+                        } else {
+                            w[4 * q + 0] = v.x;
+                            w[4 * q + 1] = v.y;
+                            w[4 * q + 2] = v.z;
+                            w[4 * q + 3] = v.w;
+                        }
                     }
                     tmem_st32u(lane_tmem + L::kQCol + c * 32, w);
                 }
