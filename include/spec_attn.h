@@ -131,7 +131,26 @@ typedef struct spec_attn_problem {
     int64_t max_seq_len;         /* upper bound on every seq_len the plan will see */
     int32_t force_splits;        /* 0: heuristic; n > 0: split the longest request's keys n ways */
     int32_t kernel_variant;      /* spec_attn_kernel_variant */
+    int32_t w_invariant;         /* 1: W-invariant mode (below); 0: off */
+    int32_t fixed_keys_per_split;/* W-invariant mode: keys per split, a multiple of 64
+                                    (0 selects 1024); ignored otherwise */
 } spec_attn_problem;
+
+/*
+ * W-invariant mode (w_invariant = 1).  Every output row comes out bit-identical
+ * to the same row computed alone: window row i of request r equals the W = 1
+ * call on the same cache with seq_len = ctx_r + i + 1, whatever W, P or the
+ * other rows are -- the exactness rule of the page "perf(dflash): widen the
+ * verify window past the compact graph's four-row limit" (section
+ * "Exactness"), which greedy speculative decoding needs for its output to
+ * match plain decoding.  The plan then uses split boundaries that depend only
+ * on key positions (every fixed_keys_per_split keys), always writes split
+ * partials and always merges them, in split order, one row at a time.  It
+ * needs the tensor-core kernel (max_w x Hq/Hkv <= 128; E_UNSUPPORTED
+ * otherwise) and ignores force_splits.  Rows computed in W-invariant mode match
+ * rows computed in W-invariant mode; the default mode's splits are chosen for
+ * speed and may round differently.
+ */
 
 typedef struct spec_attn_plan spec_attn_plan;   /* opaque */
 

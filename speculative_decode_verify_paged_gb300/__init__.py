@@ -67,6 +67,7 @@ class spec_attn_problem(ctypes.Structure):
         ("block_table_stride", ctypes.c_int32), ("mask_mode", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32), ("sm_scale", ctypes.c_float), ("max_seq_len", ctypes.c_int64),
         ("force_splits", ctypes.c_int32), ("kernel_variant", ctypes.c_int32),
+        ("w_invariant", ctypes.c_int32), ("fixed_keys_per_split", ctypes.c_int32),
     ]
 
 
@@ -201,11 +202,12 @@ class Plan:
 def spec_attn_plan_create(*, num_reqs, total_q_rows, max_w, num_q_heads, num_kv_heads, head_dim,
                           num_pages, block_table_stride, max_seq_len, mask_mode=0, kv_dtype=0,
                           page_size=16, sm_scale=0.0, force_splits=0, kernel_variant=0,
-                          seq_lens=None, q_indptr=None) -> Plan:
+                          seq_lens=None, q_indptr=None, w_invariant=0, fixed_keys_per_split=0) -> Plan:
     lib = load_library()
     prob = spec_attn_problem(num_reqs, total_q_rows, max_w, num_q_heads, num_kv_heads, head_dim,
                              page_size, num_pages, block_table_stride, mask_mode, kv_dtype,
-                             float(sm_scale), int(max_seq_len), force_splits, kernel_variant)
+                             float(sm_scale), int(max_seq_len), force_splits, kernel_variant,
+                             int(w_invariant), int(fixed_keys_per_split))
     sl, _k1 = _host_i32(seq_lens)
     qi, _k2 = _host_i32(q_indptr)
     handle = ctypes.c_void_p()
@@ -295,7 +297,8 @@ def spec_attn_last_cuda_error() -> int:
 class DeviceWorkload:
     """A workload's tensors moved to a CUDA device, plus output and workspace buffers."""
 
-    def __init__(self, wl, device="cuda", force_splits=0, kernel_variant=0, host_lens=True):
+    def __init__(self, wl, device="cuda", force_splits=0, kernel_variant=0, host_lens=True, w_invariant=0,
+                 fixed_keys_per_split=0):
         import torch
         self.wl = wl
         dev = torch.device(device)
@@ -316,7 +319,8 @@ class DeviceWorkload:
             max_seq_len=max(1, wl.max_seq_len), mask_mode=wl.mask_mode, kv_dtype=wl.kv_dtype,
             page_size=wl.page_size, sm_scale=wl.sm_scale, force_splits=force_splits,
             kernel_variant=kernel_variant, seq_lens=wl.seq_lens if host_lens else None,
-            q_indptr=wl.q_indptr if host_lens else None)
+            q_indptr=wl.q_indptr if host_lens else None, w_invariant=w_invariant,
+            fixed_keys_per_split=fixed_keys_per_split)
         self.workspace = torch.zeros(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device=dev)
 
     def run(self, stream=None):

@@ -17,7 +17,9 @@
 // combination).  A 256-thread CTA covers 256 / (D/8 * SG) pairs, so short
 // split counts pack many pairs per CTA.  Groups are combined once through
 // shared memory.  Requests with a single split were finished by the split
-// kernel and are skipped.  The kernel may be launched as a programmatic
+// kernel and are skipped, except in W-invariant mode, where every request is
+// merged with SG = 1: one thread folds a pair's splits in split order, so a
+// row's result does not depend on how many splits other rows have.  The kernel may be launched as a programmatic
 // dependent of the split kernel: it waits on griddepcontrol before touching
 // partials, and it lets the next kernel in the stream launch early (that
 // kernel waits for this grid's completion before reading its outputs).
@@ -51,7 +53,7 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
     ReqInfo ri;
     const bool req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
                                      p.bt_capacity_keys, p.keys_per_split, nullptr, ri);
-    const bool active = lp < ppc && req_ok && i < ri.w && ri.nsplits > 1;
+    const bool active = lp < ppc && req_ok && i < ri.w && (ri.nsplits > 1 || p.w_invariant);
     // Wait for the split kernel's partials (no-op without a programmatic edge).
     pdl_wait_primary();
 
@@ -142,6 +144,7 @@ cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool program
     int sg = (p.max_splits + kBatch - 1) / kBatch;
     if (sg < 1) sg = 1;
     if (sg > kMergeThreads / vec) sg = kMergeThreads / vec;
+    if (p.w_invariant) sg = 1;   // one thread folds a pair's splits in split order
     const int ppc = kMergeThreads / (vec * sg);
     const int pairs = p.max_w * p.num_q_heads;
     dim3 grid((pairs + ppc - 1) / ppc, p.num_reqs, 1);

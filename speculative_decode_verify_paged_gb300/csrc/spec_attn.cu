@@ -38,6 +38,7 @@ struct spec_attn_plan {
     int threads;
     int smem;
     bool uses_merge;
+    bool w_invariant;
     size_t ws_bytes;
     size_t ws_ls_off;
     size_t ws_o_off;
@@ -115,6 +116,9 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
     if (p->num_reqs < 0 || p->total_q_rows < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
         p->head_dim <= 0 || p->page_size <= 0 || p->max_w < 1 || p->max_seq_len < 0 ||
         p->block_table_stride < 0 || p->num_pages < 0 || p->force_splits < 0)
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (p->w_invariant != 0 && p->w_invariant != 1) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->w_invariant && (p->fixed_keys_per_split < 0 || p->fixed_keys_per_split % 64 != 0))
         return SPEC_ATTN_E_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return SPEC_ATTN_E_INVALID_ARG;
     if (p->mask_mode != SPEC_ATTN_MASK_CAUSAL_IN_BLOCK && p->mask_mode != SPEC_ATTN_MASK_NON_CAUSAL)
@@ -199,10 +203,16 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     const int G = p.num_q_heads / p.num_kv_heads;
     const int max_rows = p.max_w * G;
     const bool tc_ok = tc_supported(p.head_dim, p.kv_dtype, max_rows);
-    if (p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05 && !tc_ok) {
+    // W-invariant mode needs one kernel for every width: the tensor-core one
+    if ((p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05 || p.w_invariant) && !tc_ok) {
         delete plan;
         return SPEC_ATTN_E_UNSUPPORTED;
     }
+    if (p.w_invariant && p.kernel_variant == SPEC_ATTN_VARIANT_CUDA_CORE) {
+        delete plan;
+        return SPEC_ATTN_E_UNSUPPORTED;
+    }
+    plan->w_invariant = p.w_invariant != 0;
     // AUTO takes the tensor-core kernel wherever it applies (W x G <= 128, bf16 KV).
     const bool use_tc = p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05 ||
                         (p.kernel_variant == SPEC_ATTN_VARIANT_AUTO && tc_ok);
@@ -263,7 +273,10 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     }
     // per split: fp16 partial rows + (lse, scale), written once and read once
     const double partial_bytes = static_cast<double>(p.total_q_rows) * p.num_q_heads * (p.head_dim * 2.0 + 8.0) * 2.0;
-    if (p.force_splits > 0) {
+    if (plan->w_invariant) {
+        // split boundaries fixed by key position alone (never by W, P or lengths)
+        plan->keys_per_split = p.fixed_keys_per_split > 0 ? p.fixed_keys_per_split : 1024;
+    } else if (p.force_splits > 0) {
         int64_t c = (max_seq + p.force_splits - 1) / p.force_splits;
         c = (c + kSplitUnit - 1) / kSplitUnit * kSplitUnit;
         plan->keys_per_split = static_cast<int>(std::max<int64_t>(c, kSplitUnit));
@@ -272,7 +285,7 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
                                                      plan->num_sms * occ, total_bytes, partial_bytes, cm);
     }
     plan->max_splits = static_cast<int>((max_seq + plan->keys_per_split - 1) / plan->keys_per_split);
-    plan->uses_merge = plan->max_splits > 1;
+    plan->uses_merge = plan->max_splits > 1 || plan->w_invariant;
 
     plan->grid = dim3(static_cast<unsigned>(plan->max_splits * plan->row_groups),
                       static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(std::max(1, p.num_reqs)));
@@ -367,6 +380,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.lse = lse;
     sp.trace = reinterpret_cast<long long*>(trace);
     sp.status = reinterpret_cast<unsigned int*>(ws);
+    sp.always_partials = plan->w_invariant ? 1 : 0;
     sp.ws_ls = reinterpret_cast<float2*>(ws + plan->ws_ls_off);
     sp.ws_o = reinterpret_cast<uint16_t*>(ws + plan->ws_o_off);
     sp.num_reqs = p.num_reqs;
@@ -440,6 +454,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         mp.max_splits = plan->max_splits;
         mp.max_seq_len = p.max_seq_len;
         mp.bt_capacity_keys = p.block_table_stride * p.page_size;
+        mp.w_invariant = plan->w_invariant ? 1 : 0;
         // programmatic launch lets the merge's CTAs become resident while the
         // split kernel drains; it is skipped when a timing event sits between.
         e = merge_launch(mp, stream, plan->ev_end == nullptr);

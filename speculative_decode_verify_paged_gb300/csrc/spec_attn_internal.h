@@ -24,6 +24,7 @@ struct SplitParams {
     uint16_t* ws_o;             // split partials: per (row, head) pair, d fp16 values of O_s / scale_s
     float2* ws_ls;              // per pair: (lse_s in log2 units, scale_s = max |O_s|), same order
     unsigned int* status;       // sticky device-status word
+    int always_partials;        // W-invariant mode: write split partials even for one split
     int num_reqs;
     int total_rows;
     int max_w;
@@ -61,6 +62,7 @@ struct MergeParams {
     int max_splits;
     long long max_seq_len;
     int bt_capacity_keys;       // bt_stride * page_size
+    int w_invariant;            // merge every request (one split too), splits folded in order
 };
 
 // Split partials.  A split leaves, per (window row, query head) pair, its

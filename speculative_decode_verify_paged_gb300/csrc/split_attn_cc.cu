@@ -320,7 +320,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
         const float inv_l = (l_run[t] > 0.f) ? (p.out_scale / l_run[t]) : 0.f;
         const float lse2 = (l_run[t] > 0.f) ? (m_run[t] + log2f(l_run[t])) : -INFINITY;
         const size_t oi = ((size_t)qrow[t] * p.num_q_heads + hq[t]);
-        if (ri.nsplits == 1) {
+        if (ri.nsplits == 1 && !p.always_partials) {
             uint16_t* op = p.o + oi * D + lane * DPL;
 #pragma unroll
             for (int e = 0; e < DPL; e += 2) {

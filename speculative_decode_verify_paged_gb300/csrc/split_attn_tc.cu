@@ -816,7 +816,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             // copy the rows out below.
             const float inv = (valid && l_sum > 0.f) ? (p.out_scale / l_sum) : 0.f;
             const float lse2 = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) : -INFINITY;
-            const bool final_out = (ri.nsplits == 1);
+            const bool final_out = (ri.nsplits == 1) && !p.always_partials;
             const int rs = (final_out ? D * 2 : D * 4) + 16;
             unsigned char* myrow = smem + m * rs;
             float amax = 0.f;
@@ -888,7 +888,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         constexpr int kBatchPieces = 8;
         const int nt = blockDim.x;
         const uint32_t sbase = smem_addr(smem);
-        if (ri.nsplits == 1) {
+        if (ri.nsplits == 1 && !p.always_partials) {
             constexpr int lg = (D == 64 ? 3 : D == 128 ? 4 : 5);   // 16-byte pieces per bf16 row
             constexpr int rs = D * 2 + 16;
             const int total = R << lg;

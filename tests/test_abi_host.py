@@ -68,6 +68,9 @@ def _problem(**over):
     (dict(sm_scale=-1.0), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(kernel_variant=7), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(num_reqs=-1), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(w_invariant=2), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(w_invariant=1, fixed_keys_per_split=100), sa.SPEC_ATTN_E_INVALID_ARG),   # not a multiple of 64
+    (dict(w_invariant=1, fixed_keys_per_split=-64), sa.SPEC_ATTN_E_INVALID_ARG),
 ])
 def test_plan_rejects_bad_problems_on_the_host(lib, over, status):
     pr = sa.spec_attn_problem(**_problem(**over))

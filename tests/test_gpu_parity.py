@@ -375,3 +375,83 @@ FULL = [
 def test_full_size_sampled(name, make, variant):
     wl = make()
     run_and_check(wl, variant, trace=True, sel=_sample(wl))
+
+
+# --------------------------------------------------------------------------- #
+# W-invariant mode: a window row equals the same row computed alone
+# --------------------------------------------------------------------------- #
+def _row_alone(wl, dw_full, r, i, fixed):
+    """Window row i of request r as its own W = 1 call on the same cache: seq_len
+    ctx_r + i + 1, the row's own queries, the same pools and block table."""
+    lens = wl.seq_lens.tolist()
+    ind = wl.q_indptr.tolist()
+    w_r = ind[r + 1] - ind[r]
+    ctx = lens[r] - w_r
+    row = ind[r] + i
+    plan = sa.spec_attn_plan_create(
+        num_reqs=1, total_q_rows=1, max_w=1, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+        head_dim=wl.head_dim, num_pages=wl.num_pages, block_table_stride=int(wl.block_table.shape[1]),
+        max_seq_len=ctx + i + 1, mask_mode=wl.mask_mode, kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale,
+        w_invariant=1, fixed_keys_per_split=fixed)
+    q = dw_full.q[row:row + 1].contiguous()
+    bt = dw_full.block_table[r:r + 1].contiguous()
+    sl = torch.tensor([ctx + i + 1], dtype=torch.int32, device="cuda")
+    qi = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    o = torch.zeros(1, wl.num_q_heads, wl.head_dim, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, wl.num_q_heads, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    sa.spec_attn_run(plan, q, dw_full.k_pool, dw_full.v_pool, bt, sl, qi, o, lse, ws, dw_full.k_scales,
+                     dw_full.v_scales, wl.k_gscale, wl.v_gscale)
+    torch.cuda.synchronize()
+    assert sa.spec_attn_check_device_status(ws) == 0
+    return o[0], lse[0]
+
+
+@pytest.mark.parametrize("kv,d,fixed", [(W.KV_BF16, 256, 0), (W.KV_BF16, 128, 192), (W.KV_NVFP4, 256, 512)])
+def test_w_invariant_rows_match_the_row_alone_bitwise(kv, d, fixed):
+    """Exactness rule: in W-invariant mode every row of a batched causal
+    verify call is bit-identical to its own W = 1 decode at seq_len ctx + i + 1,
+    and the call still matches the oracle."""
+    wl = W.make_workload("winv", [2300, 700, 90], [16, 9, 5], 24, 4, d, W.MASK_CAUSAL_IN_BLOCK, kv_dtype=kv,
+                         seed=71, pool_slack=0.2)
+    dw = sa.DeviceWorkload(wl, "cuda", w_invariant=1, fixed_keys_per_split=fixed)
+    assert dw.plan.info["uses_merge"] == 1
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() == 0
+    o_ref, lse_ref, _ = oracle.run_workload(wl)
+    check_close(dw.o, dw.lse, o_ref, lse_ref)
+    ind = wl.q_indptr.tolist()
+    for r in range(wl.num_reqs):
+        for i in range(ind[r + 1] - ind[r]):
+            o1, l1 = _row_alone(wl, dw, r, i, fixed)
+            row = ind[r] + i
+            assert torch.equal(dw.o[row], o1), (r, i)
+            assert torch.equal(dw.lse[row], l1), (r, i)
+
+
+def test_w_invariant_is_independent_of_the_batch():
+    """The same request alone and inside a batch of others gives identical bits."""
+    kw = dict(num_q_heads=24, num_kv_heads=4, head_dim=256, mask_mode=W.MASK_CAUSAL_IN_BLOCK, seed=72,
+              pool_slack=0.2)
+    batch = W.make_workload("winvb", [1500, 3100, 400], [8, 12, 3], **kw)
+    a = sa.DeviceWorkload(batch, "cuda", w_invariant=1)
+    a.run()
+    torch.cuda.synchronize()
+    ind = batch.q_indptr.tolist()
+    r = 1
+    alone = W.Workload(**{**batch.__dict__, "seq_lens": batch.seq_lens[r:r + 1],
+                          "q_indptr": torch.tensor([0, ind[r + 1] - ind[r]], dtype=torch.int32),
+                          "block_table": batch.block_table[r:r + 1],
+                          "q": batch.q[ind[r]:ind[r + 1]]})
+    b = sa.DeviceWorkload(alone, "cuda", w_invariant=1)
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.o[ind[r]:ind[r + 1]], b.o) and torch.equal(a.lse[ind[r]:ind[r + 1]], b.lse)
+
+
+def test_w_invariant_needs_the_tensor_core_kernel():
+    wl = W.make_workload("winvu", [300], [16], 64, 4, 128, 0, seed=73)    # 256 rows per KV head
+    with pytest.raises(sa.SpecAttnError) as ei:
+        sa.DeviceWorkload(wl, "cuda", w_invariant=1)
+    assert ei.value.status == sa.SPEC_ATTN_E_UNSUPPORTED
