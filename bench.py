@@ -140,7 +140,12 @@ def table_workloads():
     from speculative_decode_verify_paged_gb300 import workloads as W
     return [("long_verify_w8", lambda: W.long_verify(8)), ("long_verify_w9", lambda: W.long_verify(9)),
             ("long_verify_w12", lambda: W.long_verify(12)), ("long_verify_w16", lambda: W.long_verify(16)),
-            ("batched_draft", W.batched_draft), ("nvfp4", W.nvfp4)]
+            ("batched_draft", W.batched_draft), ("nvfp4", W.nvfp4),
+            ("verify_w16_ctx16k_w_invariant", lambda: W.verify_sweep(16), {"w_invariant": 1}),
+            ("verify_w1_ctx16k_w_invariant", lambda: W.verify_sweep(1), {"w_invariant": 1}),
+            ("long_verify_w16_w_invariant", lambda: W.long_verify(16), {"w_invariant": 1}),
+            ("long_verify_w16_w_invariant_2048", lambda: W.long_verify(16),
+             {"w_invariant": 1, "fixed_keys_per_split": 2048})]
 
 
 def run_reference(args, rank, world):
@@ -355,14 +360,15 @@ def run_ours(args, rank, world, local_rank):
 
     table = []
     if not args.quick:
-        for name, make in table_workloads():
+        for name, make, *extra in table_workloads():
             wl = make()
+            kw = extra[0] if extra else {}
             try:
-                dw = sa.DeviceWorkload(wl, dev, kernel_variant=args.variant)
+                dw = sa.DeviceWorkload(wl, dev, kernel_variant=args.variant, **kw)
             except sa.SpecAttnError as e:  # forced variant not available for this shape
                 if e.status != sa.SPEC_ATTN_E_UNSUPPORTED:
                     raise
-                dw = sa.DeviceWorkload(wl, dev, kernel_variant=sa.SPEC_ATTN_VARIANT_AUTO)
+                dw = sa.DeviceWorkload(wl, dev, kernel_variant=sa.SPEC_ATTN_VARIANT_AUTO, **kw)
             ts, _ = time_calls([dw], flush, max(10, args.steps), 3, stream)
             _, sk = time_calls([dw], flush, max(10, args.steps), 3, stream, timing_events=True)
             us = statistics.mean(ts) * 1e3

@@ -133,7 +133,7 @@ typedef struct spec_attn_problem {
     int32_t kernel_variant;      /* spec_attn_kernel_variant */
     int32_t w_invariant;         /* 1: W-invariant mode (below); 0: off */
     int32_t fixed_keys_per_split;/* W-invariant mode: keys per split, a multiple of 64
-                                    (0 selects 1024); ignored otherwise */
+                                    (0 selects 512); ignored otherwise */
 } spec_attn_problem;
 
 /*
@@ -145,11 +145,16 @@ typedef struct spec_attn_problem {
  * "Exactness"), which greedy speculative decoding needs for its output to
  * match plain decoding.  The plan then uses split boundaries that depend only
  * on key positions (every fixed_keys_per_split keys), always writes split
- * partials and always merges them, in split order, one row at a time.  It
+ * partials and always merges them in a fold order fixed by the split index
+ * alone (split s in group s mod G, G a constant of head_dim).  It
  * needs the tensor-core kernel (max_w x Hq/Hkv <= 128; E_UNSUPPORTED
  * otherwise) and ignores force_splits.  Rows computed in W-invariant mode match
- * rows computed in W-invariant mode; the default mode's splits are chosen for
- * speed and may round differently.
+ * rows computed in W-invariant mode with the same fixed_keys_per_split; the
+ * default mode's splits are chosen for speed and may round differently.  The
+ * cost is the split count this fixes: one CTA per (split, KV head, request),
+ * so the call is fastest when fixed_keys_per_split is near the typical
+ * context length x P x Hkv / (number of SMs), e.g. 512 for one request with
+ * 4 KV heads at 16K keys, 2048 at 64K.
  */
 
 typedef struct spec_attn_plan spec_attn_plan;   /* opaque */

@@ -18,8 +18,12 @@
 // split counts pack many pairs per CTA.  Groups are combined once through
 // shared memory.  Requests with a single split were finished by the split
 // kernel and are skipped, except in W-invariant mode, where every request is
-// merged with SG = 1: one thread folds a pair's splits in split order, so a
-// row's result does not depend on how many splits other rows have.  The kernel may be launched as a programmatic
+// merged and SG is the largest the CTA allows for D, a constant.  Split s then
+// always lands in group s mod SG, each group folds its splits in ascending
+// order and the groups are combined in group order, so the sum order of a
+// (row, head) pair never depends on the split count: a row that sees fewer
+// keys than its request's last row only has trailing splits with lse = -inf,
+// which every fold step skips.  The kernel may be launched as a programmatic
 // dependent of the split kernel: it waits on griddepcontrol before touching
 // partials, and it lets the next kernel in the stream launch early (that
 // kernel waits for this grid's completion before reading its outputs).
@@ -144,7 +148,7 @@ cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool program
     int sg = (p.max_splits + kBatch - 1) / kBatch;
     if (sg < 1) sg = 1;
     if (sg > kMergeThreads / vec) sg = kMergeThreads / vec;
-    if (p.w_invariant) sg = 1;   // one thread folds a pair's splits in split order
+    if (p.w_invariant) sg = kMergeThreads / vec;   // a constant of D: the fold order is fixed
     const int ppc = kMergeThreads / (vec * sg);
     const int pairs = p.max_w * p.num_q_heads;
     dim3 grid((pairs + ppc - 1) / ppc, p.num_reqs, 1);

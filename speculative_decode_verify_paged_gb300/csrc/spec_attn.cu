@@ -275,7 +275,7 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     const double partial_bytes = static_cast<double>(p.total_q_rows) * p.num_q_heads * (p.head_dim * 2.0 + 8.0) * 2.0;
     if (plan->w_invariant) {
         // split boundaries fixed by key position alone (never by W, P or lengths)
-        plan->keys_per_split = p.fixed_keys_per_split > 0 ? p.fixed_keys_per_split : 1024;
+        plan->keys_per_split = p.fixed_keys_per_split > 0 ? p.fixed_keys_per_split : 512;
     } else if (p.force_splits > 0) {
         int64_t c = (max_seq + p.force_splits - 1) / p.force_splits;
         c = (c + kSplitUnit - 1) / kSplitUnit * kSplitUnit;
