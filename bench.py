@@ -177,10 +177,15 @@ def run_reference(args, rank, world):
 # --------------------------------------------------------------------------- #
 # GPU arm
 # --------------------------------------------------------------------------- #
+# the sources the attention call's kernels and its plan are built from
+HASHED_SOURCES = ("common.cuh", "sm100.cuh", "spec_attn_internal.h", "spec_attn.cu", "split_attn_tc.cu",
+                  "split_attn_cc.cu", "merge_lse.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decode_verify_paged_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in HASHED_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

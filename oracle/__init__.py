@@ -6,15 +6,21 @@ and the CPU-baseline leg of ``bench.py`` may load it.  It shares no code with
 the CUDA library and never serves as a fallback for it.
 
 The arithmetic lives in ``spec_attn_oracle.c`` (plain C, fp64, OpenMP over
-independent output rows only); this module compiles it with gcc into
-``oracle/_build/libspec_attn_oracle.so`` and wraps it with ctypes.
+independent output rows only) and ``kv_append_oracle.c`` (the KV append that
+precedes a verify call, with its NVFP4 quantiser); this module compiles both
+with gcc into ``oracle/_build/libspec_attn_oracle.so`` and wraps them with
+ctypes.
 
 Parity pins (tests/test_oracle_pins.py) hold every function here to values
 fixed independently of this code: torch's fp64 scaled-dot-product attention on
 CPU for W=1 decode, a pure-Python brute force on tiny shapes, closed forms
 (zero queries, one visible key, constant power-of-two values), invariances
 (page permutation, row-wise reduction to decode, last-row agreement of the two
-masks) and the OCP e2m1 / e4m3 format definitions.
+masks) and the OCP e2m1 / e4m3 format definitions.  The append and its
+quantiser are pinned in tests/test_oracle_append_pins.py: exact round trips of
+representable blocks, midpoint and saturation cases of both encoders, a
+rational-arithmetic brute force of every code, torch's own e4m3 rounding, and
+the placement of every row checked slot by slot.
 """
 from __future__ import annotations
 
@@ -26,7 +32,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "spec_attn_oracle.c")
+_SRCS = (os.path.join(_HERE, "spec_attn_oracle.c"), os.path.join(_HERE, "kv_append_oracle.c"))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libspec_attn_oracle.so")
 _lock = threading.Lock()
@@ -37,11 +43,11 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no fast-math) and return the .so path."""
     os.makedirs(_BUILD, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+           "-fno-fast-math", "-ffp-contract=off", *_SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -65,6 +71,16 @@ def _load():
             lib.oracle_bf16_value.argtypes = [ctypes.c_uint]
             lib.oracle_round_bf16.restype = ctypes.c_uint
             lib.oracle_round_bf16.argtypes = [f64]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint
+            lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+            lib.oracle_nvfp4_quantise_block.restype = None
+            lib.oracle_nvfp4_quantise_block.argtypes = [vp, ctypes.c_float, vp, vp]
+            lib.spec_attn_oracle_append_kv.restype = i32
+            lib.spec_attn_oracle_append_kv.argtypes = [
+                i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                ctypes.c_float, vp, i32, vp, vp]
             lib.spec_attn_oracle_num_threads.restype = i32
             lib.spec_attn_oracle_num_threads.argtypes = []
             _lib = lib
@@ -101,6 +117,53 @@ def e4m3(byte: int) -> float:
 
 def round_bf16_bits(x: float) -> int:
     return _load().oracle_round_bf16(float(x))
+
+
+def e4m3_encode(x: float) -> int:
+    """binary32 value -> E4M3 byte (nearest even, saturating at 448)."""
+    return _load().oracle_e4m3_encode(float(x))
+
+
+def e2m1_encode(x: float) -> int:
+    """binary32 value -> E2M1 code (nearest even, saturating at 6)."""
+    return _load().oracle_e2m1_encode(float(x))
+
+
+def nvfp4_quantise_block(x_bf16_bits, g: float):
+    """16 bf16 bit patterns -> (8 code bytes, scale byte) against decode scale g."""
+    x = np.ascontiguousarray(np.asarray(x_bf16_bits, dtype=np.uint16).reshape(16))
+    codes = np.zeros(8, dtype=np.uint8)
+    sc = np.zeros(1, dtype=np.uint8)
+    _load().oracle_nvfp4_quantise_block(_ptr(x), float(g), _ptr(codes), _ptr(sc))
+    return codes, int(sc[0])
+
+
+def append_kv(*, num_kv_heads, head_dim, page_size, kv_dtype, k_new, v_new, k_pool, v_pool,
+              block_table, seq_lens, q_indptr, k_scales=None, v_scales=None, k_gscale=1.0,
+              v_gscale=1.0):
+    """Write every request's window rows of ``k_new`` / ``v_new`` ([total_rows,
+    Hkv, d] bf16) into copies of the pools.  Returns numpy arrays
+    ``(k_pool, v_pool, k_scales, v_scales)`` (scales None for bf16)."""
+    lib = _load()
+    kn = _np(k_new, np.uint16).copy()
+    vn = _np(v_new, np.uint16).copy()
+    pool_t = np.uint16 if kv_dtype == 0 else np.uint8
+    kp = _np(k_pool, pool_t).copy()
+    vp_ = _np(v_pool, pool_t).copy()
+    ks = None if k_scales is None else _np(k_scales, np.uint8).copy()
+    vs = None if v_scales is None else _np(v_scales, np.uint8).copy()
+    btn = _np(block_table, np.int32)
+    sln = _np(seq_lens, np.int32)
+    qin = _np(q_indptr, np.int32)
+    num_pages = kp.shape[0]
+    bt_stride = btn.shape[1] if btn.ndim == 2 else btn.shape[0]
+    rc = lib.spec_attn_oracle_append_kv(
+        sln.shape[0], kn.shape[0], num_kv_heads, head_dim, page_size, num_pages, kv_dtype,
+        _ptr(kn), _ptr(vn), _ptr(kp), _ptr(vp_), _ptr(ks), _ptr(vs), float(k_gscale),
+        float(v_gscale), _ptr(btn), bt_stride, _ptr(sln), _ptr(qin))
+    if rc != 0:
+        raise ValueError(f"spec_attn_oracle_append_kv failed with code {rc}")
+    return kp, vp_, ks, vs
 
 
 def num_threads() -> int:

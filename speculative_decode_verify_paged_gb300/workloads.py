@@ -28,10 +28,11 @@ The named workloads mirror the shapes the pages measure or describe:
                      sections "The cost" and "Scope": k = 8, ctx ~ 1300,
                      non-causal draft layers, shared paged pool).
 * ``nvfp4``          4 requests, ctx 16384, W 8, Hq 24, Hkv 4, d 256, causal,
-                     K/V quantised to e2m1 codes + one e4m3 scale per 16
-                     head_dim elements + one fp32 scale per tensor, shuffled
-                     pool (page "ChunkedSmallT ...", section "Measurement",
-                     16K nvfp4 row; the format is this library's reading).
+                     K/V as e2m1 codes + one e4m3 scale per 16 head_dim
+                     elements + one fp32 scale per tensor, codes and scales
+                     drawn directly (``_draw_nvfp4``), shuffled pool (page
+                     "ChunkedSmallT ...", section "Measurement", 16K nvfp4
+                     row; the format is this library's reading).
 """
 from __future__ import annotations
 
@@ -108,41 +109,21 @@ class Workload:
 
 
 # --------------------------------------------------------------------------- #
-# NVFP4 input quantiser (test-input preparation only)
+# NVFP4 pools, drawn directly
 # --------------------------------------------------------------------------- #
-_E2M1_MIDPOINTS = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+NVFP4_GSCALE = 0.3          # decode scale of both drawn tensors: element RMS ~ 1
 
 
-def _quantise_nvfp4(x: torch.Tensor):
-    """fp32 [..., d] -> (codes uint8 [..., d/2], scales uint8 [..., d/16], gscale).
-
-    Global scale = amax / (6 * 448); block scale = e4m3(amax_block / (6 * gscale))
-    rounded to nearest even and saturated at 448; code = nearest e2m1 grid
-    point of x / (block scale * gscale), ties to the even code, saturating at
-    +-6.  An all-zero block gets scale 0 and code 0.
-    """
-    d = x.shape[-1]
-    assert d % 16 == 0
-    amax = float(x.abs().max().item())
-    gscale = amax / (6.0 * 448.0) if amax > 0 else 1.0
-    blocks = x.reshape(*x.shape[:-1], d // 16, 16)
-    amax_blk = blocks.abs().amax(dim=-1)
-    s = (amax_blk / (6.0 * gscale)).clamp(max=448.0)
-    s8 = s.to(torch.float8_e4m3fn)
-    s_dec = s8.to(torch.float32)
-    scales = s8.view(torch.uint8)
-    denom = (s_dec * gscale).unsqueeze(-1)
-    a = torch.where(denom > 0, blocks / torch.where(denom > 0, denom, torch.ones_like(denom)),
-                    torch.zeros_like(blocks))
-    mag = a.abs()
-    idx = torch.bucketize(mag, _E2M1_MIDPOINTS, right=False)
-    lower = idx.clamp(max=6)
-    tie = (idx < 7) & (mag == _E2M1_MIDPOINTS[lower])
-    idx = torch.where(tie & (idx % 2 == 1), idx + 1, idx)
-    code = idx.to(torch.uint8) | torch.where(a < 0, 8, 0).to(torch.uint8)
-    code = code.reshape(*x.shape[:-1], d)
-    packed = code[..., 0::2] | (code[..., 1::2] << 4)
-    return packed.contiguous(), scales.contiguous(), gscale
+def _draw_nvfp4(lead_shape, d: int, gen: torch.Generator):
+    """Random NVFP4 cache contents: codes uint8 [*lead_shape, d/2] (two
+    independent uniform 4-bit codes per byte) and e4m3 block-scale bytes
+    [*lead_shape, d/16] drawn uniformly from 0x30..0x3F (values 0.5 .. 1.875).
+    Drawn rather than quantised, so this module holds no quantiser; with the
+    decode scale NVFP4_GSCALE the elements have an RMS near 1, like the bf16
+    pools' N(0, 1)."""
+    codes = torch.randint(0, 256, (*lead_shape, d // 2), generator=gen, dtype=torch.int32).to(torch.uint8)
+    scales = (0x30 + torch.randint(0, 16, (*lead_shape, d // 16), generator=gen, dtype=torch.int32)).to(torch.uint8)
+    return codes, scales
 
 
 # --------------------------------------------------------------------------- #
@@ -191,8 +172,11 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
     qf = torch.randn(total_rows, Hq, d, generator=g, dtype=torch.float32)
     if q_mode == "zero":
         qf.zero_()
-    kf = torch.randn(pool_pages, Hkv, ps, d, generator=g, dtype=torch.float32)
-    vf = torch.randn(pool_pages, Hkv, ps, d, generator=g, dtype=torch.float32)
+    fp4 = kv_dtype != KV_BF16
+    assert not (fp4 and (v_mode != "randn" or peaky_frac > 0)), "value shaping is bf16-only"
+    # NVFP4 pools are drawn as codes below: no bf16 values to draw for them
+    kf = torch.randn(0 if fp4 else pool_pages, Hkv, ps, d, generator=g, dtype=torch.float32)
+    vf = torch.randn(0 if fp4 else pool_pages, Hkv, ps, d, generator=g, dtype=torch.float32)
     if v_mode == "const":
         # per (kv head, dim) a power of two in [2^-3, 2^3], sign alternating
         expo = torch.randint(-3, 4, (Hkv, d), generator=g).to(torch.float32)
@@ -223,8 +207,9 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
             k_pool[bad] = float("nan")
             v_pool[bad] = float("nan")
     else:
-        kc, ks, kg = _quantise_nvfp4(kf)
-        vc, vs, vg = _quantise_nvfp4(vf)
+        kc, ks = _draw_nvfp4((pool_pages, Hkv, ps), d, g)
+        vc, vs = _draw_nvfp4((pool_pages, Hkv, ps), d, g)
+        kg = vg = NVFP4_GSCALE
         if poison_unread:
             bad = (~owned)[:, None, :, None]
             ks[bad.expand_as(ks)] = 0xFF  # e4m3 NaN
