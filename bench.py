@@ -145,7 +145,11 @@ def table_workloads():
             ("verify_w1_ctx16k_w_invariant", lambda: W.verify_sweep(1), {"w_invariant": 1}),
             ("long_verify_w16_w_invariant", lambda: W.long_verify(16), {"w_invariant": 1}),
             ("long_verify_w16_w_invariant_2048", lambda: W.long_verify(16),
-             {"w_invariant": 1, "fixed_keys_per_split": 2048})]
+             {"w_invariant": 1, "fixed_keys_per_split": 2048}),
+            ("verify_w16_ctx16k_run_append", lambda: W.verify_sweep(16), {"append": "run_append"}),
+            ("nvfp4_run_append", W.nvfp4, {"append": "run_append"}),
+            ("verify_w16_ctx16k_append_only", lambda: W.verify_sweep(16), {"append": "append"}),
+            ("nvfp4_append_only", W.nvfp4, {"append": "append"})]
 
 
 def run_reference(args, rank, world):
@@ -312,6 +316,7 @@ def run_ours(args, rank, world, local_rank):
     import torch
     import speculative_decode_verify_paged_gb300 as sa
     from speculative_decode_verify_paged_gb300 import build as libbuild
+    from speculative_decode_verify_paged_gb300 import workloads as W
 
     libbuild.build()
     torch.cuda.set_device(local_rank)
@@ -367,7 +372,11 @@ def run_ours(args, rank, world, local_rank):
     if not args.quick:
         for name, make, *extra in table_workloads():
             wl = make()
-            kw = extra[0] if extra else {}
+            kw = dict(extra[0]) if extra else {}
+            mode = kw.pop("append", "run")
+            if mode != "run":
+                kw.update(mode=mode, append_rows=W.window_kv_rows(wl.total_rows, wl.num_kv_heads, wl.head_dim,
+                                                                   seed=1, mix=False))
             try:
                 dw = sa.DeviceWorkload(wl, dev, kernel_variant=args.variant, **kw)
             except sa.SpecAttnError as e:  # forced variant not available for this shape
@@ -377,11 +386,14 @@ def run_ours(args, rank, world, local_rank):
             ts, _ = time_calls([dw], flush, max(10, args.steps), 3, stream)
             _, sk = time_calls([dw], flush, max(10, args.steps), 3, stream, timing_events=True)
             us = statistics.mean(ts) * 1e3
-            gbs = wl.kv_bytes / (us * 1e-6) / 1e9
-            table.append({"workload": name, "us": round(us, 2), "gbs": round(gbs, 1),
-                          "split_kernel_us": round(sk[0] * 1e3, 2),
-                          "pct_peak": round(100 * gbs / peak, 1), "kv_bytes": wl.kv_bytes,
-                          "splits": dw.plan.info["max_splits"], "variant": dw.plan.info["kernel_variant"]})
+            nbytes = wl.append_bytes if mode == "append" else wl.kv_bytes
+            gbs = nbytes / (us * 1e-6) / 1e9
+            row = {"workload": name, "us": round(us, 2), "gbs": round(gbs, 1),
+                   "pct_peak": round(100 * gbs / peak, 1), "bytes": nbytes,
+                   "splits": dw.plan.info["max_splits"], "variant": dw.plan.info["kernel_variant"]}
+            if mode != "append":
+                row["split_kernel_us"] = round(sk[0] * 1e3, 2)
+            table.append(row)
             del dw
             torch.cuda.empty_cache()
         lv = {t["workload"]: t["us"] for t in table}

@@ -231,6 +231,52 @@ int spec_attn_run_traced(const spec_attn_plan* plan, const void* q, const void* 
                          size_t workspace_bytes, spec_attn_stream_t stream);
 
 /*
+ * KV append: write the window's new key and value rows into their cache slots
+ * (page "perf(dflash): widen the verify window past the compact graph's
+ * four-row limit", section "What changed": the window's rows go into the
+ * cache, later steps overwrite the rows a rejected tail leaves stale, and
+ * attention reads only seq_len entries).  seq_len_r already counts the
+ * window, so window row i of request r is written at key position
+ * pos = seq_len_r - W_r + i: page block_table[r][pos / 16], slot pos % 16,
+ * for every KV head.
+ *   k_new, v_new  [total_q_rows, Hkv, d] bf16, rows in q_indptr order,
+ *                 16-byte aligned; read only
+ *   k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
+ *   seq_lens, q_indptr   as for spec_attn_run; the pools (and, for NVFP4,
+ *                 the scale pools) are written at the window's slots only
+ *   workspace     as for spec_attn_run; spec_attn_append_kv uses only its
+ *                 device-status word (workspace_bytes >= 256)
+ * bf16 caches receive the bits unchanged.  NVFP4 caches receive each run of
+ * 16 head_dim elements quantised against the cache's decode scale g (k_gscale
+ * or v_gscale): amax = max |x|; scale byte = E4M3(amax / (6 g)); den =
+ * scale * g; code = E2M1(x / den), or +0 throughout when den = 0; every
+ * product and quotient in binary32 rounded to nearest even in that order, the
+ * conversions to nearest even, saturating at 448 and 6 and keeping the sign.
+ * Values beyond 6 * 448 * g clip.  NaN or infinite inputs give unspecified
+ * codes.  Device-side checks (bad window, seq_len or page id) set the same
+ * status bits as spec_attn_run and skip the row; nothing else is written.
+ * Asynchronous on `stream`, allocation-free, graph capturable.
+ */
+int spec_attn_append_kv(const spec_attn_plan* plan, const void* k_new, const void* v_new, void* k_pool,
+                        void* v_pool, void* k_scales, void* v_scales, float k_gscale, float v_gscale,
+                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                        void* workspace, size_t workspace_bytes, spec_attn_stream_t stream);
+
+/*
+ * spec_attn_append_kv followed by spec_attn_run on the same stream: the step
+ * a verify layer takes once it has the window's K and V.  Every argument is
+ * checked before either kernel is launched, so a rejected call writes
+ * nothing.  The attention kernel is launched as a programmatic dependent of
+ * the append and reads the cache only after the append has completed.
+ * workspace as for spec_attn_run (the plan's workspace_bytes).
+ */
+int spec_attn_run_append(const spec_attn_plan* plan, const void* q, const void* k_new, const void* v_new,
+                         void* k_pool, void* v_pool, void* k_scales, void* v_scales, float k_gscale,
+                         float v_gscale, const int32_t* block_table, const int32_t* seq_lens,
+                         const int32_t* q_indptr, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                         spec_attn_stream_t stream);
+
+/*
  * Optional timing hooks: when set (both non-NULL; cudaEvent_t values), every
  * later run records `split_begin` on its stream just before the split-KV
  * kernel launch and `split_end` just after it, so a caller can time that

@@ -49,7 +49,7 @@ EXPORTED_SYMBOLS = (
     "spec_attn_run", "spec_attn_run_traced", "spec_attn_plan_set_timing_events",
     "spec_attn_reset_device_status", "spec_attn_check_device_status",
     "spec_attn_status_string", "spec_attn_last_cuda_error", "spec_attn_version",
-    "spec_attn_run_noalloc",
+    "spec_attn_run_noalloc", "spec_attn_append_kv", "spec_attn_run_append",
 )
 
 
@@ -125,6 +125,11 @@ def load_library(path: Optional[str] = None):
         lib.spec_attn_version.argtypes = []
         lib.spec_attn_run_noalloc.restype = i32
         lib.spec_attn_run_noalloc.argtypes = run_args + [vp]
+        cache_args = [vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp, vp]
+        lib.spec_attn_append_kv.restype = i32
+        lib.spec_attn_append_kv.argtypes = [vp, vp, vp] + cache_args + [vp, sz, vp]
+        lib.spec_attn_run_append.restype = i32
+        lib.spec_attn_run_append.argtypes = [vp, vp, vp, vp] + cache_args + [vp, vp, vp, sz, vp]
         if path is None:
             _lib = lib
         return lib
@@ -267,6 +272,48 @@ def spec_attn_run_noalloc(plan: Plan, q, k_pool, v_pool, block_table, seq_lens, 
     _check(lib.spec_attn_run_noalloc(*args, _stream_handle(stream)), "spec_attn_run_noalloc")
 
 
+def _cache_args(plan, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,
+                q_indptr):
+    import torch
+    fp4 = plan.problem.kv_dtype == SPEC_ATTN_KV_NVFP4
+    return [_dptr(k_pool, "k_pool", torch.uint8 if fp4 else torch.bfloat16),
+            _dptr(v_pool, "v_pool", torch.uint8 if fp4 else torch.bfloat16),
+            _dptr(k_scales, "k_scales", torch.uint8), _dptr(v_scales, "v_scales", torch.uint8),
+            ctypes.c_float(k_gscale), ctypes.c_float(v_gscale),
+            _dptr(block_table, "block_table", torch.int32), _dptr(seq_lens, "seq_lens", torch.int32),
+            _dptr(q_indptr, "q_indptr", torch.int32)]
+
+
+def spec_attn_append_kv(plan: Plan, k_new, v_new, k_pool, v_pool, block_table, seq_lens, q_indptr, workspace,
+                        k_scales=None, v_scales=None, k_gscale=1.0, v_gscale=1.0, stream=None):
+    """Write the windows' new K/V rows ([total_rows, Hkv, d] bf16) into their
+    cache slots, quantising for NVFP4 caches (asynchronous)."""
+    import torch
+    lib = load_library()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.spec_attn_append_kv(plan.handle, _dptr(k_new, "k_new", torch.bfloat16),
+                                   _dptr(v_new, "v_new", torch.bfloat16),
+                                   *_cache_args(plan, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
+                                                block_table, seq_lens, q_indptr),
+                                   _dptr(workspace, "workspace"), ctypes.c_size_t(ws_bytes),
+                                   _stream_handle(stream)), "spec_attn_append_kv")
+
+
+def spec_attn_run_append(plan: Plan, q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, q_indptr, o, lse,
+                         workspace, k_scales=None, v_scales=None, k_gscale=1.0, v_gscale=1.0, stream=None):
+    """KV append, then the attention call, on one stream (asynchronous)."""
+    import torch
+    lib = load_library()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.spec_attn_run_append(plan.handle, _dptr(q, "q", torch.bfloat16),
+                                    _dptr(k_new, "k_new", torch.bfloat16), _dptr(v_new, "v_new", torch.bfloat16),
+                                    *_cache_args(plan, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
+                                                 block_table, seq_lens, q_indptr),
+                                    _dptr(o, "o", torch.bfloat16), _dptr(lse, "lse", torch.float32),
+                                    _dptr(workspace, "workspace"), ctypes.c_size_t(ws_bytes),
+                                    _stream_handle(stream)), "spec_attn_run_append")
+
+
 def spec_attn_reset_device_status(workspace, stream=None):
     _check(load_library().spec_attn_reset_device_status(_dptr(workspace, "workspace"),
                                                         _stream_handle(stream)),
@@ -298,9 +345,15 @@ class DeviceWorkload:
     """A workload's tensors moved to a CUDA device, plus output and workspace buffers."""
 
     def __init__(self, wl, device="cuda", force_splits=0, kernel_variant=0, host_lens=True, w_invariant=0,
-                 fixed_keys_per_split=0):
+                 fixed_keys_per_split=0, append_rows=None, mode="run"):
+        """``append_rows``: (k_new, v_new) [total_rows, Hkv, d] bf16 for the KV
+        append.  ``mode``: what :meth:`run` launches -- "run" (attention),
+        "run_append" (append, then attention) or "append" (the append alone)."""
         import torch
+        assert mode in ("run", "run_append", "append")
+        assert mode == "run" or append_rows is not None
         self.wl = wl
+        self.mode = mode
         dev = torch.device(device)
         self.q = wl.q.to(dev)
         self.k_pool = wl.k_pool.to(dev)
@@ -322,11 +375,24 @@ class DeviceWorkload:
             q_indptr=wl.q_indptr if host_lens else None, w_invariant=w_invariant,
             fixed_keys_per_split=fixed_keys_per_split)
         self.workspace = torch.zeros(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device=dev)
+        self.k_new = self.v_new = None
+        if append_rows is not None:
+            self.k_new = append_rows[0].to(dev).contiguous()
+            self.v_new = append_rows[1].to(dev).contiguous()
 
     def run(self, stream=None):
-        spec_attn_run(self.plan, self.q, self.k_pool, self.v_pool, self.block_table, self.seq_lens,
-                      self.q_indptr, self.o, self.lse, self.workspace, self.k_scales, self.v_scales,
-                      self.wl.k_gscale, self.wl.v_gscale, stream)
+        if self.mode == "append":
+            spec_attn_append_kv(self.plan, self.k_new, self.v_new, self.k_pool, self.v_pool, self.block_table,
+                                self.seq_lens, self.q_indptr, self.workspace, self.k_scales, self.v_scales,
+                                self.wl.k_gscale, self.wl.v_gscale, stream)
+        elif self.mode == "run_append":
+            spec_attn_run_append(self.plan, self.q, self.k_new, self.v_new, self.k_pool, self.v_pool,
+                                 self.block_table, self.seq_lens, self.q_indptr, self.o, self.lse, self.workspace,
+                                 self.k_scales, self.v_scales, self.wl.k_gscale, self.wl.v_gscale, stream)
+        else:
+            spec_attn_run(self.plan, self.q, self.k_pool, self.v_pool, self.block_table, self.seq_lens,
+                          self.q_indptr, self.o, self.lse, self.workspace, self.k_scales, self.v_scales,
+                          self.wl.k_gscale, self.wl.v_gscale, stream)
 
     def run_traced(self, trace, stream=None):
         spec_attn_run_traced(self.plan, self.q, self.k_pool, self.v_pool, self.block_table,

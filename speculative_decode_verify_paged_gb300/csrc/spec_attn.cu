@@ -338,6 +338,86 @@ int spec_attn_plan_set_timing_events(spec_attn_plan* plan, void* split_begin, vo
     return SPEC_ATTN_OK;
 }
 
+// Host-side checks shared by every entry point that reads or writes the cache:
+// the pools, their scales (NVFP4), the request arrays, the workspace and the
+// current device.  min_ws is the workspace the entry point needs.
+static int check_cache_args(const spec_attn_plan* plan, const void* k_pool, const void* v_pool,
+                            const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
+                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                            const void* workspace, size_t workspace_bytes, size_t min_ws) {
+    const spec_attn_problem& p = plan->prob;
+    if (!k_pool || !v_pool || !block_table || !seq_lens || !q_indptr || !workspace) return SPEC_ATTN_E_INVALID_ARG;
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+        !aligned(q_indptr, 4) || !aligned(workspace, 256))
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (p.kv_dtype == SPEC_ATTN_KV_NVFP4) {
+        if (!k_scales || !v_scales || !aligned(k_scales, 16) || !aligned(v_scales, 16))
+            return SPEC_ATTN_E_INVALID_ARG;
+        if (!(k_gscale > 0.f) || !(v_gscale > 0.f) || std::isinf(k_gscale) || std::isinf(v_gscale))
+            return SPEC_ATTN_E_INVALID_ARG;
+    }
+    if (workspace_bytes < min_ws) return SPEC_ATTN_E_WORKSPACE_TOO_SMALL;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev != plan->device) return SPEC_ATTN_E_INVALID_ARG;
+    return SPEC_ATTN_OK;
+}
+
+static int check_run_args(const spec_attn_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                          const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
+                          const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                          const void* o, const float* lse, const int64_t* trace, const void* workspace,
+                          size_t workspace_bytes) {
+    if (!q || !o || !aligned(q, 16) || !aligned(o, 16) || (lse && !aligned(lse, 4)) ||
+        (trace && !aligned(trace, 8)))
+        return SPEC_ATTN_E_INVALID_ARG;
+    return check_cache_args(plan, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,
+                            q_indptr, workspace, workspace_bytes, plan->ws_bytes);
+}
+
+static int check_append_args(const spec_attn_plan* plan, const void* k_new, const void* v_new,
+                             const void* k_pool, const void* v_pool, const void* k_scales, const void* v_scales,
+                             float k_gscale, float v_gscale, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* q_indptr, const void* workspace,
+                             size_t workspace_bytes) {
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return SPEC_ATTN_E_INVALID_ARG;
+    return check_cache_args(plan, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,
+                            q_indptr, workspace, workspace_bytes, kStatusBytes);
+}
+
+static int append_launch_checked(const spec_attn_plan* plan, const void* k_new, const void* v_new, void* k_pool,
+                                 void* v_pool, void* k_scales, void* v_scales, float k_gscale, float v_gscale,
+                                 const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                                 void* workspace, cudaStream_t stream) {
+    const spec_attn_problem& p = plan->prob;
+    AppendParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    ap.k_new = static_cast<const uint16_t*>(k_new);
+    ap.v_new = static_cast<const uint16_t*>(v_new);
+    ap.k_pool = k_pool;
+    ap.v_pool = v_pool;
+    ap.k_scales = static_cast<uint8_t*>(k_scales);
+    ap.v_scales = static_cast<uint8_t*>(v_scales);
+    ap.k_gscale = k_gscale;
+    ap.v_gscale = v_gscale;
+    ap.block_table = block_table;
+    ap.seq_lens = seq_lens;
+    ap.q_indptr = q_indptr;
+    ap.status = static_cast<unsigned int*>(workspace);
+    ap.num_reqs = p.num_reqs;
+    ap.total_rows = p.total_q_rows;
+    ap.max_w = p.max_w;
+    ap.num_kv_heads = p.num_kv_heads;
+    ap.head_dim = p.head_dim;
+    ap.num_pages = p.num_pages;
+    ap.bt_stride = p.block_table_stride;
+    ap.bt_capacity_keys = p.block_table_stride * p.page_size;
+    ap.max_seq_len = p.max_seq_len;
+    const cudaError_t e = append_launch(ap, p.kv_dtype, stream);
+    return e == cudaSuccess ? SPEC_ATTN_OK : cuda_fail(e);
+}
+
 static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_pool, const void* v_pool,
                     const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
                     const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
@@ -346,23 +426,10 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     if (!plan) return SPEC_ATTN_E_INVALID_ARG;
     const spec_attn_problem& p = plan->prob;
     if (p.num_reqs == 0 || p.total_q_rows == 0) return SPEC_ATTN_OK;
-    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !q_indptr || !o || !workspace)
-        return SPEC_ATTN_E_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16) ||
-        !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(q_indptr, 4) ||
-        !aligned(workspace, 256) || (lse && !aligned(lse, 4)) || (trace && !aligned(trace, 8)))
-        return SPEC_ATTN_E_INVALID_ARG;
-    if (p.kv_dtype == SPEC_ATTN_KV_NVFP4) {
-        if (!k_scales || !v_scales || !aligned(k_scales, 16) || !aligned(v_scales, 16))
-            return SPEC_ATTN_E_INVALID_ARG;
-        if (!(k_gscale > 0.f) || !(v_gscale > 0.f) || std::isinf(k_gscale) || std::isinf(v_gscale))
-            return SPEC_ATTN_E_INVALID_ARG;
-    }
-    if (workspace_bytes < plan->ws_bytes) return SPEC_ATTN_E_WORKSPACE_TOO_SMALL;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (dev != plan->device) return SPEC_ATTN_E_INVALID_ARG;
+    const int chk = check_run_args(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
+                                   seq_lens, q_indptr, o, lse, trace, workspace, workspace_bytes);
+    if (chk != SPEC_ATTN_OK) return chk;
+    cudaError_t e = cudaSuccess;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -470,6 +537,42 @@ int spec_attn_run(const spec_attn_plan* plan, const void* q, const void* k_pool,
                   spec_attn_stream_t stream) {
     return run_impl(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
                     seq_lens, q_indptr, o, lse, nullptr, workspace, workspace_bytes, stream);
+}
+
+int spec_attn_append_kv(const spec_attn_plan* plan, const void* k_new, const void* v_new, void* k_pool,
+                        void* v_pool, void* k_scales, void* v_scales, float k_gscale, float v_gscale,
+                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                        void* workspace, size_t workspace_bytes, spec_attn_stream_t stream) {
+    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    const spec_attn_problem& p = plan->prob;
+    if (p.num_reqs == 0 || p.total_q_rows == 0) return SPEC_ATTN_OK;
+    const int chk = check_append_args(plan, k_new, v_new, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
+                                      block_table, seq_lens, q_indptr, workspace, workspace_bytes);
+    if (chk != SPEC_ATTN_OK) return chk;
+    return append_launch_checked(plan, k_new, v_new, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
+                                 block_table, seq_lens, q_indptr, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int spec_attn_run_append(const spec_attn_plan* plan, const void* q, const void* k_new, const void* v_new,
+                         void* k_pool, void* v_pool, void* k_scales, void* v_scales, float k_gscale,
+                         float v_gscale, const int32_t* block_table, const int32_t* seq_lens,
+                         const int32_t* q_indptr, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                         spec_attn_stream_t stream) {
+    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    const spec_attn_problem& p = plan->prob;
+    if (p.num_reqs == 0 || p.total_q_rows == 0) return SPEC_ATTN_OK;
+    // every check before the first launch: a rejected call changes nothing
+    int chk = check_append_args(plan, k_new, v_new, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
+                                block_table, seq_lens, q_indptr, workspace, workspace_bytes);
+    if (chk == SPEC_ATTN_OK)
+        chk = check_run_args(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,
+                             q_indptr, o, lse, nullptr, workspace, workspace_bytes);
+    if (chk != SPEC_ATTN_OK) return chk;
+    chk = append_launch_checked(plan, k_new, v_new, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
+                                block_table, seq_lens, q_indptr, workspace, reinterpret_cast<cudaStream_t>(stream));
+    if (chk != SPEC_ATTN_OK) return chk;
+    return run_impl(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,
+                    q_indptr, o, lse, nullptr, workspace, workspace_bytes, stream);
 }
 
 int spec_attn_run_traced(const spec_attn_plan* plan, const void* q, const void* k_pool,

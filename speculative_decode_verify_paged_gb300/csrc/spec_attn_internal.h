@@ -65,6 +65,31 @@ struct MergeParams {
     int w_invariant;            // merge every request (one split too), splits folded in order
 };
 
+// Everything one KV-append launch needs (append_kv.cu).
+struct AppendParams {
+    const uint16_t* k_new;      // [total_rows, Hkv, d] bf16 bits, rows in q_indptr order
+    const uint16_t* v_new;
+    void* k_pool;               // bf16 [pages, Hkv, ps, d] | nvfp4 codes [pages, Hkv, ps, d/2]
+    void* v_pool;
+    uint8_t* k_scales;          // nvfp4 e4m3 [pages, Hkv, ps, d/16]
+    uint8_t* v_scales;
+    float k_gscale;             // nvfp4 decode scales (> 0)
+    float v_gscale;
+    const int32_t* block_table; // [P, bt_stride]
+    const int32_t* seq_lens;    // [P]
+    const int32_t* q_indptr;    // [P + 1]
+    unsigned int* status;       // sticky device-status word
+    int num_reqs;
+    int total_rows;
+    int max_w;
+    int num_kv_heads;
+    int head_dim;
+    int num_pages;
+    int bt_stride;
+    int bt_capacity_keys;       // bt_stride * page_size
+    long long max_seq_len;
+};
+
 // Split partials.  A split leaves, per (window row, query head) pair, its
 // normalised partial output O_s (d values), lse_s and scale_s = max_e |O_s[e]|;
 // O_s is stored as d fp16 values of O_s / scale_s (in [-1, 1]), so a stored
@@ -121,5 +146,10 @@ cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bo
 
 // ---- LSE merge (merge_lse.cu) ----
 cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic);
+
+// ---- KV append (append_kv.cu) ----
+// Always a programmatic dependent of the previous kernel in the stream (the
+// kernel waits on griddepcontrol before its first global access).
+cudaError_t append_launch(const AppendParams& p, int kv_dtype, cudaStream_t stream);
 
 }  // namespace spec_attn

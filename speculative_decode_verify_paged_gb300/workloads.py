@@ -104,6 +104,13 @@ class Workload:
         request, every KV head, K and V once (a single sweep)."""
         return int(self.seq_lens.sum().item()) * self.num_kv_heads * 2 * self.bytes_per_token_head
 
+    @property
+    def append_bytes(self) -> int:
+        """Algorithmic bytes of the KV append: the windows' new K and V rows
+        read as bf16, written in the pool's format."""
+        rows = int(self.q_indptr[-1].item()) * self.num_kv_heads * 2
+        return rows * (2 * self.head_dim + self.bytes_per_token_head)
+
     def window_lengths(self):
         return (self.q_indptr[1:] - self.q_indptr[:-1]).tolist()
 
@@ -129,13 +136,40 @@ def _draw_nvfp4(lead_shape, d: int, gen: torch.Generator):
 # --------------------------------------------------------------------------- #
 # Generic generator
 # --------------------------------------------------------------------------- #
+def window_kv_rows(total_rows: int, num_kv_heads: int, head_dim: int, seed: int = 0, mix: bool = True):
+    """New key and value rows of the windows, [total_rows, Hkv, d] bf16 each,
+    for the KV append.  With ``mix`` every 16-element run draws one of:
+    N(0, 1) scaled by 2^U(-8, 6) (wide dynamic range); integers in [-48, 48]
+    times 2^U(-10, 2) (dyadic values, so quotients land exactly on rounding
+    midpoints); all zeros, half of them negative zeros; N(0, 1) * 2^-30 (far
+    below any scale); N(0, 1) * 2^12 (far above).  Without ``mix``: N(0, 1)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    shape = (2, total_rows, num_kv_heads, head_dim // 16, 16)
+    x = torch.randn(shape, generator=g, dtype=torch.float32)
+    if mix:
+        kind = torch.randint(0, 10, shape[:-1], generator=g)
+        wide = torch.exp2(torch.randint(-8, 7, shape[:-1], generator=g).float())
+        ints = torch.randint(-48, 49, shape, generator=g).float()
+        dy = ints * torch.exp2(torch.randint(-10, 3, shape[:-1], generator=g).float())[..., None]
+        negz = torch.where(torch.rand(shape, generator=g) < 0.5, -0.0, 0.0)
+        out = x * wide[..., None]
+        out = torch.where((kind >= 4)[..., None] & (kind < 7)[..., None], dy, out)
+        out = torch.where((kind == 7)[..., None], negz, out)
+        out = torch.where((kind == 8)[..., None], x * 2.0 ** -30, out)
+        out = torch.where((kind == 9)[..., None], x * 2.0 ** 12, out)
+        x = out
+    x = x.reshape(2, total_rows, num_kv_heads, head_dim).to(torch.bfloat16)
+    return x[0].contiguous(), x[1].contiguous()
+
+
 def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
                   num_kv_heads: int, head_dim: int, mask_mode: int, kv_dtype: int = KV_BF16,
                   page_size: int = 16, seed: int = 0, pool_pages: Optional[int] = None,
                   pool_slack: float = 0.0, fragmented: bool = True, peaky_frac: float = 0.0,
                   peaky_mult: float = 3.0, poison_unread: bool = False,
                   sm_scale: Optional[float] = None, bt_stride: Optional[int] = None,
-                  q_mode: str = "randn", v_mode: str = "randn") -> Workload:
+                  q_mode: str = "randn", v_mode: str = "randn",
+                  nvfp4_gscale: float = NVFP4_GSCALE) -> Workload:
     """Draw one seeded workload.
 
     ``windows`` is one int (same W for every request) or a per-request list.
@@ -209,7 +243,7 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
     else:
         kc, ks = _draw_nvfp4((pool_pages, Hkv, ps), d, g)
         vc, vs = _draw_nvfp4((pool_pages, Hkv, ps), d, g)
-        kg = vg = NVFP4_GSCALE
+        kg = vg = float(nvfp4_gscale)
         if poison_unread:
             bad = (~owned)[:, None, :, None]
             ks[bad.expand_as(ks)] = 0xFF  # e4m3 NaN

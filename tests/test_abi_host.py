@@ -104,6 +104,10 @@ def test_null_arguments(lib):
     assert lib.spec_attn_plan_get_info(None, None) == sa.SPEC_ATTN_E_INVALID_ARG
     assert lib.spec_attn_reset_device_status(None, None) == sa.SPEC_ATTN_E_INVALID_ARG
     assert lib.spec_attn_check_device_status(None, None, None) == sa.SPEC_ATTN_E_INVALID_ARG
+    assert lib.spec_attn_append_kv(*([None] * 7), ctypes.c_float(1.0), ctypes.c_float(1.0),
+                                   *([None] * 4), 0, None) == sa.SPEC_ATTN_E_INVALID_ARG
+    assert lib.spec_attn_run_append(*([None] * 8), ctypes.c_float(1.0), ctypes.c_float(1.0),
+                                    *([None] * 6), 0, None) == sa.SPEC_ATTN_E_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(tmp_path):
