@@ -25,6 +25,12 @@
  *                      (same page, section "The cost": the draft layers are
  *                      not causal, each row attends over its request's whole
  *                      span).
+ *   Sliding window (window_left > 0; causal only): the same page, same
+ *   section, notes that the non-causal draft layers leave an attention window
+ *   unapplied, without defining it.  The plainest reading, used here: row i
+ *   sees only the window_left most recent keys up to its own,
+ *   max(0, ctx_r + i - window_left + 1) .. ctx_r + i.  Non-causal calls take
+ *   no window.
  *   Only keys below seq_len[r] are ever read (page "perf(dflash): widen the
  *   verify window past the compact graph's four-row limit", section "What
  *   changed": attention reads only seqlen entries).
@@ -125,6 +131,7 @@ unsigned oracle_round_bf16(double x) {
  * kv_dtype 1: k_pool/v_pool are NVFP4 codes [num_pages, Hkv, ps, d/2] bytes,
  *             k_scales/v_scales e4m3 bytes [num_pages, Hkv, ps, d/16].
  * mask_mode 0: causal-in-block, 1: non-causal.
+ * window_left: 0 (none) or the sliding window of causal rows (keys).
  * row_select: optional [total_rows * Hq] bytes; nonzero = compute that
  *             (row, head).  Unselected outputs are left untouched.
  * o:   [total_rows, Hq, d] fp64 (may be NULL when only the trace is wanted)
@@ -134,7 +141,7 @@ unsigned oracle_round_bf16(double x) {
  */
 int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_kv_heads,
                          int head_dim, int page_size, int num_pages, int mask_mode,
-                         int kv_dtype, double sm_scale, const uint16_t* q,
+                         int window_left, int kv_dtype, double sm_scale, const uint16_t* q,
                          const void* k_pool, const void* v_pool, const uint8_t* k_scales,
                          const uint8_t* v_scales, double k_gscale, double v_gscale,
                          const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
@@ -144,6 +151,7 @@ int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_
         page_size <= 0 || head_dim > 1024 || num_q_heads % num_kv_heads != 0)
         return ORACLE_BAD_ARG;
     if (kv_dtype == 1 && head_dim % 16 != 0) return ORACLE_BAD_ARG;
+    if (window_left < 0 || (window_left > 0 && mask_mode != 0)) return ORACLE_BAD_ARG;
     const int G = num_q_heads / num_kv_heads;
     const int d = head_dim;
     const int Hkv = num_kv_heads;
@@ -219,7 +227,8 @@ int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_
                 if (row_select && !row_select[(size_t)row * num_q_heads + h]) continue;
                 const int kvh = h / G;
                 const int hi = (mask_mode == 0) ? ctx + i : L - 1; /* inclusive */
-                const int nvis = hi + 1;
+                const int lo = (window_left > 0 && hi - window_left + 1 > 0) ? hi - window_left + 1 : 0;
+                const int nvis = hi - lo + 1;
                 double* s = (double*)malloc((size_t)nvis * sizeof(double));
                 if (!s) {
                     fail = 1;
@@ -229,8 +238,9 @@ int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_
                 double qd[1024];
                 for (int e = 0; e < d; ++e) qd[e] = oracle_bf16(qrow[e]);
 
+                /* s[j] is the score of key lo + j */
                 for (int j = 0; j < nvis; ++j) {
-                    const double* kd = Kd + ((size_t)j * Hkv + (size_t)kvh) * d;
+                    const double* kd = Kd + ((size_t)(lo + j) * Hkv + (size_t)kvh) * d;
                     double acc = 0.0;
                     for (int e = 0; e < d; ++e) acc += qd[e] * kd[e];
                     s[j] = sm_scale * acc;
@@ -248,14 +258,14 @@ int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_
                     for (int e = 0; e < d; ++e) {
                         double acc = 0.0;
                         for (int j = 0; j < nvis; ++j)
-                            acc += s[j] * Vd[((size_t)j * Hkv + (size_t)kvh) * d + e];
+                            acc += s[j] * Vd[((size_t)(lo + j) * Hkv + (size_t)kvh) * d + e];
                         orow[e] = acc / l;
                     }
                 }
                 if (lse) lse[(size_t)row * num_q_heads + h] = m + log(l);
                 if (trace) {
                     int64_t sum = 0;
-                    for (int j = 0; j < nvis; ++j) sum += slot_id[j];
+                    for (int j = 0; j < nvis; ++j) sum += slot_id[lo + j];
                     trace[((size_t)row * num_q_heads + h) * 2 + 0] = nvis;
                     trace[((size_t)row * num_q_heads + h) * 2 + 1] = sum;
                 }

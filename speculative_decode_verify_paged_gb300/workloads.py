@@ -68,6 +68,7 @@ class Workload:
     v_scales: Optional[torch.Tensor] = None
     k_gscale: float = 1.0
     v_gscale: float = 1.0
+    window_left: int = 0          # causal sliding window (keys); 0 = none
     meta: dict = field(default_factory=dict)
 
     @property
@@ -169,7 +170,7 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
                   peaky_mult: float = 3.0, poison_unread: bool = False,
                   sm_scale: Optional[float] = None, bt_stride: Optional[int] = None,
                   q_mode: str = "randn", v_mode: str = "randn",
-                  nvfp4_gscale: float = NVFP4_GSCALE) -> Workload:
+                  nvfp4_gscale: float = NVFP4_GSCALE, window_left: int = 0) -> Workload:
     """Draw one seeded workload.
 
     ``windows`` is one int (same W for every request) or a per-request list.
@@ -253,6 +254,7 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
     return Workload(name=name, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, page_size=ps,
                     mask_mode=mask_mode, kv_dtype=kv_dtype,
                     sm_scale=(1.0 / math.sqrt(d)) if sm_scale is None else float(sm_scale),
+                    window_left=int(window_left),
                     q=q, k_pool=k_pool, v_pool=v_pool, block_table=block_table,
                     seq_lens=seq_lens, q_indptr=q_indptr,
                     meta=dict(seed=seed, ctx_lens=list(map(int, ctx_lens)),

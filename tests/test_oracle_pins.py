@@ -133,8 +133,9 @@ def _brute(wl):
             for h in range(wl.num_q_heads):
                 kvh = h // G
                 top = (L - W + i) if wl.mask_mode == 0 else (L - 1)
+                bottom = max(0, top - wl.window_left + 1) if wl.window_left > 0 else 0
                 scores = []
-                for j in range(top + 1):
+                for j in range(bottom, top + 1):
                     page, slot = bt[r][j // wl.page_size], j % wl.page_size
                     dot = 0.0
                     for e in range(wl.head_dim):
@@ -166,6 +167,71 @@ def test_brute_force_tiny(mask, seed):
     for (row, h), vec in ref_o.items():
         np.testing.assert_allclose(o[row, h], vec, rtol=1e-12, atol=1e-13)
         assert abs(lse[row, h] - ref_lse[(row, h)]) <= 1e-12 * max(1.0, abs(ref_lse[(row, h)]))
+
+
+@pytest.mark.parametrize("page_size,window", [(32, 0), (64, 0), (32, 9), (16, 3)])
+def test_brute_force_larger_pages_and_window(page_size, window):
+    wl = wlmod.make_workload("brutepw", [70, 5, 130], [4, 3, 2], 4, 2, 8, wlmod.MASK_CAUSAL_IN_BLOCK,
+                             page_size=page_size, seed=7, pool_slack=0.5, window_left=window)
+    o, lse, _ = oracle.run_workload(wl)
+    ref_o, ref_lse = _brute(wl)
+    for (row, h), vec in ref_o.items():
+        np.testing.assert_allclose(o[row, h], vec, rtol=1e-12, atol=1e-13)
+        assert abs(lse[row, h] - ref_lse[(row, h)]) <= 1e-12 * max(1.0, abs(ref_lse[(row, h)]))
+
+
+@pytest.mark.parametrize("window", [1, 5, 37])
+def test_sliding_window_equals_sdpa_with_banded_mask(window):
+    """Causal rows with a sliding window against SDPA with a banded boolean
+    mask built from the definition (keys hi - window + 1 .. hi)."""
+    wl = wlmod.make_workload("band", [60, 3], [6, 2], 4, 2, 16, wlmod.MASK_CAUSAL_IN_BLOCK, seed=12,
+                             pool_slack=0.3, window_left=window)
+    o, lse, _ = oracle.run_workload(wl)
+    G = wl.num_q_heads // wl.num_kv_heads
+    for r in range(wl.num_reqs):
+        row0 = int(wl.q_indptr[r])
+        W = int(wl.q_indptr[r + 1]) - row0
+        L = int(wl.seq_lens[r])
+        hi = (L - W + torch.arange(W))[:, None]
+        j = torch.arange(L)[None, :]
+        keep = (j <= hi) & (j > hi - window)
+        for h in range(wl.num_q_heads):
+            k, v = _gather(wl, r, h // G)
+            q = wl.q[row0:row0 + W, h].to(torch.float64)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                q[None, None], k[None, None], v[None, None], attn_mask=keep[None, None],
+                scale=wl.sm_scale)[0, 0]
+            s = (q @ k.T) * wl.sm_scale
+            ref_lse = torch.logsumexp(s.masked_fill(~keep, float("-inf")), 1)
+            np.testing.assert_allclose(o[row0:row0 + W, h], ref.numpy(), rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(lse[row0:row0 + W, h], ref_lse.numpy(), rtol=1e-12)
+
+
+def test_window_covering_every_key_changes_nothing_and_window_one_is_own_key():
+    base = wlmod.make_workload("wall", [50, 0], [5, 3], 4, 2, 16, wlmod.MASK_CAUSAL_IN_BLOCK, seed=13)
+    o0, l0, t0 = oracle.run_workload(base, want_trace=True)
+    wide = wlmod.Workload(**{**base.__dict__, "window_left": 55})
+    o1, l1, t1 = oracle.run_workload(wide, want_trace=True)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1) and np.array_equal(t0, t1)
+    one = wlmod.Workload(**{**base.__dict__, "window_left": 1})
+    o2, l2, t2 = oracle.run_workload(one, want_trace=True)
+    assert (t2[..., 0] == 1).all()
+    G = 2
+    for r in range(2):
+        row0 = int(base.q_indptr[r]); W = int(base.q_indptr[r + 1]) - row0; L = int(base.seq_lens[r])
+        for i in range(W):
+            for h in range(4):
+                k, v = _gather(base, r, h // G)
+                key = L - W + i
+                np.testing.assert_array_equal(o2[row0 + i, h], v[key].numpy())
+                s = float((base.q[row0 + i, h].to(torch.float64) @ k[key]) * base.sm_scale)
+                assert abs(l2[row0 + i, h] - s) <= 1e-12 * max(1.0, abs(s))
+
+
+def test_window_needs_the_causal_mask():
+    wl = wlmod.make_workload("wnc", [20], [3], 4, 2, 16, wlmod.MASK_NON_CAUSAL, seed=14, window_left=4)
+    with pytest.raises(ValueError):
+        oracle.run_workload(wl)
 
 
 # --------------------------------------------------------------------------- #
@@ -270,17 +336,20 @@ def test_constant_power_of_two_values_come_back_exactly():
                 assert np.array_equal(o[row, h], v[0].numpy())
 
 
-def test_trace_counts_and_slot_sums():
-    wl = wlmod.make_workload("trace", [33, 7], [4, 2], 2, 1, 8, wlmod.MASK_CAUSAL_IN_BLOCK,
-                             seed=15, pool_slack=1.0)
+@pytest.mark.parametrize("page_size,window", [(16, 0), (32, 0), (64, 11)])
+def test_trace_counts_and_slot_sums(page_size, window):
+    wl = wlmod.make_workload("trace", [33, 7, 100], [4, 2, 3], 2, 1, 8, wlmod.MASK_CAUSAL_IN_BLOCK,
+                             seed=15, pool_slack=1.0, page_size=page_size, window_left=window)
     _, _, tr = oracle.run_workload(wl, want_o=False, want_lse=False, want_trace=True)
     bt = wl.block_table.tolist()
+    ps = page_size
     for r in range(wl.num_reqs):
         row0 = int(wl.q_indptr[r]); W = int(wl.q_indptr[r + 1]) - row0; L = int(wl.seq_lens[r])
         for i in range(W):
-            n = L - W + i + 1
-            s = sum(bt[r][j // 16] * 16 + j % 16 for j in range(n))
-            assert tr[row0 + i, 0, 0] == n and tr[row0 + i, 0, 1] == s
+            hi = L - W + i
+            lo = max(0, hi - window + 1) if window else 0
+            s = sum(bt[r][j // ps] * ps + j % ps for j in range(lo, hi + 1))
+            assert tr[row0 + i, 0, 0] == hi - lo + 1 and tr[row0 + i, 0, 1] == s
 
 
 # --------------------------------------------------------------------------- #
