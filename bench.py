@@ -149,7 +149,10 @@ def table_workloads():
             ("verify_w16_ctx16k_run_append", lambda: W.verify_sweep(16), {"append": "run_append"}),
             ("nvfp4_run_append", W.nvfp4, {"append": "run_append"}),
             ("verify_w16_ctx16k_append_only", lambda: W.verify_sweep(16), {"append": "append"}),
-            ("nvfp4_append_only", W.nvfp4, {"append": "append"})]
+            ("nvfp4_append_only", W.nvfp4, {"append": "append"}),
+            ("verify_w16_ctx16k_pages64", lambda: W.verify_sweep(16, page_size=64, pool_pages=512)),
+            ("verify_w16_ctx16k_interleaved_kv", lambda: W.verify_sweep(16), {"interleave": True}),
+            ("long_verify_w16_window4096", lambda: W.long_verify(16, window_left=4096))]
 
 
 def run_reference(args, rank, world):

@@ -12,6 +12,12 @@
  *   causal-in-block: window row i sees keys 0 .. ctx_r + i (inclusive)
  *   non-causal:      every window row sees all seq_len[r] keys
  *
+ * optionally narrowed, for causal calls, by a sliding window: with
+ * window_left = n > 0, row i sees only keys max(0, ctx_r + i - n + 1) ..
+ * ctx_r + i.  (The first page below names an attention window that its
+ * non-causal draft layers leave unapplied, without defining it; this is the
+ * plainest reading, and non-causal calls take no window.)
+ *
  * and outputs are produced for window rows only, never for context rows.
  * Sources (titles of the pages this library restates):
  *   - "DFlash2 leaves the paged graph fast path at every c>1 and re-attends
@@ -34,17 +40,22 @@
  * with fp32 accumulation; O is written as bf16 (round to nearest even),
  * LSE as fp32.
  *
- * Layouts (all row-major, dense):
+ * Layouts (row-major; the pools may have a page stride, everything else is
+ * dense):
  *   Q, O       [total_q_rows, Hq, head_dim] bf16; the rows of request r are
  *              q_indptr[r] .. q_indptr[r+1]-1, in window order.
  *   LSE        [total_q_rows, Hq] fp32.
- *   K/V pools  bf16:  [num_pages, Hkv, page_size, head_dim]
- *              NVFP4: codes [num_pages, Hkv, page_size, head_dim/2] bytes
- *                     (two e2m1 codes per byte, low nibble = even element),
- *                     scales [num_pages, Hkv, page_size, head_dim/16] bytes
- *                     (one OCP e4m3 scale per 16 contiguous elements), and
- *                     one fp32 global scale per tensor:
- *                     value = e2m1(code) * e4m3(scale) * gscale.
+ *   K/V pools  num_pages pages, page p at byte offset p * kv_page_stride
+ *              (default: dense), each page [Hkv, page_size, row] with
+ *              bf16:  row = head_dim bf16 values;
+ *              NVFP4: row = head_dim/2 code bytes (two e2m1 codes per byte,
+ *                     low nibble = even element), and scale pools laid out
+ *                     the same way with page stride scale_page_stride and
+ *                     row = head_dim/16 bytes (one OCP e4m3 scale per 16
+ *                     contiguous elements), plus one fp32 global scale per
+ *                     tensor: value = e2m1(code) * e4m3(scale) * gscale.
+ *              A page stride lets K and V (and their scales) share one
+ *              allocation, e.g. [num_pages, 2, Hkv, page_size, row].
  *   block_table [P, block_table_stride] int32: key j of request r lives in
  *              page block_table[r][j / page_size], slot j % page_size.
  *              Entries past ceil(seq_len[r] / page_size) are never read.
@@ -113,7 +124,8 @@ typedef enum spec_attn_kernel_variant {
 /* Limits of this build. */
 #define SPEC_ATTN_MAX_W 16
 #define SPEC_ATTN_MAX_GROUP 16       /* Hq / Hkv */
-#define SPEC_ATTN_PAGE_SIZE 16
+#define SPEC_ATTN_MIN_PAGE_SIZE 16   /* page_size is 16, 32 or 64 */
+#define SPEC_ATTN_MAX_PAGE_SIZE 64
 
 typedef struct spec_attn_problem {
     int32_t num_reqs;            /* P >= 0 */
@@ -122,7 +134,7 @@ typedef struct spec_attn_problem {
     int32_t num_q_heads;         /* Hq */
     int32_t num_kv_heads;        /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 16 */
     int32_t head_dim;            /* 64, 128 or 256 */
-    int32_t page_size;           /* 16 */
+    int32_t page_size;           /* keys per page: 16, 32 or 64 */
     int32_t num_pages;           /* pages in each pool (device bounds check) */
     int32_t block_table_stride;  /* int32 entries per block-table row */
     int32_t mask_mode;           /* spec_attn_mask_mode */
@@ -134,6 +146,13 @@ typedef struct spec_attn_problem {
     int32_t w_invariant;         /* 1: W-invariant mode (below); 0: off */
     int32_t fixed_keys_per_split;/* W-invariant mode: keys per split, a multiple of 64
                                     (0 selects 512); ignored otherwise */
+    int32_t window_left;         /* causal sliding window in keys; 0 = none (required
+                                    for the non-causal mask) */
+    int64_t kv_page_stride;      /* bytes from a K (or V) page to the next: 0 = dense
+                                    (Hkv * page_size * row bytes); else a multiple of 16
+                                    and at least the dense size */
+    int64_t scale_page_stride;   /* NVFP4 scale pools, likewise (dense: Hkv * page_size
+                                    * head_dim/16 bytes); ignored for bf16 */
 } spec_attn_problem;
 
 /*

@@ -68,6 +68,8 @@ class spec_attn_problem(ctypes.Structure):
         ("kv_dtype", ctypes.c_int32), ("sm_scale", ctypes.c_float), ("max_seq_len", ctypes.c_int64),
         ("force_splits", ctypes.c_int32), ("kernel_variant", ctypes.c_int32),
         ("w_invariant", ctypes.c_int32), ("fixed_keys_per_split", ctypes.c_int32),
+        ("window_left", ctypes.c_int32), ("kv_page_stride", ctypes.c_int64),
+        ("scale_page_stride", ctypes.c_int64),
     ]
 
 
@@ -158,12 +160,14 @@ def _host_i32(t):
     return a.ctypes.data_as(ctypes.c_void_p), a
 
 
-def _dptr(t, what, dtype=None, align=16):
+def _dptr(t, what, dtype=None, contiguous=True):
+    """Device pointer of a CUDA tensor.  contiguous=False admits a view whose
+    layout the plan describes (a pool with a page stride)."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError(f"{what} must be a CUDA tensor")
-    if not t.is_contiguous():
+    if contiguous and not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{what} must be {dtype}, got {t.dtype}")
@@ -207,12 +211,14 @@ class Plan:
 def spec_attn_plan_create(*, num_reqs, total_q_rows, max_w, num_q_heads, num_kv_heads, head_dim,
                           num_pages, block_table_stride, max_seq_len, mask_mode=0, kv_dtype=0,
                           page_size=16, sm_scale=0.0, force_splits=0, kernel_variant=0,
-                          seq_lens=None, q_indptr=None, w_invariant=0, fixed_keys_per_split=0) -> Plan:
+                          seq_lens=None, q_indptr=None, w_invariant=0, fixed_keys_per_split=0,
+                          window_left=0, kv_page_stride=0, scale_page_stride=0) -> Plan:
     lib = load_library()
     prob = spec_attn_problem(num_reqs, total_q_rows, max_w, num_q_heads, num_kv_heads, head_dim,
                              page_size, num_pages, block_table_stride, mask_mode, kv_dtype,
                              float(sm_scale), int(max_seq_len), force_splits, kernel_variant,
-                             int(w_invariant), int(fixed_keys_per_split))
+                             int(w_invariant), int(fixed_keys_per_split), int(window_left),
+                             int(kv_page_stride), int(scale_page_stride))
     sl, _k1 = _host_i32(seq_lens)
     qi, _k2 = _host_i32(q_indptr)
     handle = ctypes.c_void_p()
@@ -222,15 +228,23 @@ def spec_attn_plan_create(*, num_reqs, total_q_rows, max_w, num_q_heads, num_kv_
     return Plan(handle, ws.value, prob)
 
 
+def _pool_ptrs(plan, k_pool, v_pool, k_scales, v_scales):
+    """Pool pointers; a plan with a page stride takes strided views."""
+    import torch
+    fp4 = plan.problem.kv_dtype == SPEC_ATTN_KV_NVFP4
+    dense = plan.problem.kv_page_stride == 0
+    dense_sc = plan.problem.scale_page_stride == 0
+    return [_dptr(k_pool, "k_pool", torch.uint8 if fp4 else torch.bfloat16, dense),
+            _dptr(v_pool, "v_pool", torch.uint8 if fp4 else torch.bfloat16, dense),
+            _dptr(k_scales, "k_scales", torch.uint8, dense_sc), _dptr(v_scales, "v_scales", torch.uint8, dense_sc)]
+
+
 def _run_args(plan, q, k_pool, v_pool, block_table, seq_lens, q_indptr, o, lse, k_scales, v_scales,
               k_gscale, v_gscale):
     import torch
-    fp4 = plan.problem.kv_dtype == SPEC_ATTN_KV_NVFP4
     return [plan.handle,
             _dptr(q, "q", torch.bfloat16),
-            _dptr(k_pool, "k_pool", torch.uint8 if fp4 else torch.bfloat16),
-            _dptr(v_pool, "v_pool", torch.uint8 if fp4 else torch.bfloat16),
-            _dptr(k_scales, "k_scales", torch.uint8), _dptr(v_scales, "v_scales", torch.uint8),
+            *_pool_ptrs(plan, k_pool, v_pool, k_scales, v_scales),
             ctypes.c_float(k_gscale), ctypes.c_float(v_gscale),
             _dptr(block_table, "block_table", torch.int32), _dptr(seq_lens, "seq_lens", torch.int32),
             _dptr(q_indptr, "q_indptr", torch.int32), _dptr(o, "o", torch.bfloat16),
@@ -275,10 +289,7 @@ def spec_attn_run_noalloc(plan: Plan, q, k_pool, v_pool, block_table, seq_lens, 
 def _cache_args(plan, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,
                 q_indptr):
     import torch
-    fp4 = plan.problem.kv_dtype == SPEC_ATTN_KV_NVFP4
-    return [_dptr(k_pool, "k_pool", torch.uint8 if fp4 else torch.bfloat16),
-            _dptr(v_pool, "v_pool", torch.uint8 if fp4 else torch.bfloat16),
-            _dptr(k_scales, "k_scales", torch.uint8), _dptr(v_scales, "v_scales", torch.uint8),
+    return [*_pool_ptrs(plan, k_pool, v_pool, k_scales, v_scales),
             ctypes.c_float(k_gscale), ctypes.c_float(v_gscale),
             _dptr(block_table, "block_table", torch.int32), _dptr(seq_lens, "seq_lens", torch.int32),
             _dptr(q_indptr, "q_indptr", torch.int32)]
@@ -345,10 +356,13 @@ class DeviceWorkload:
     """A workload's tensors moved to a CUDA device, plus output and workspace buffers."""
 
     def __init__(self, wl, device="cuda", force_splits=0, kernel_variant=0, host_lens=True, w_invariant=0,
-                 fixed_keys_per_split=0, append_rows=None, mode="run"):
+                 fixed_keys_per_split=0, append_rows=None, mode="run", interleave=False):
         """``append_rows``: (k_new, v_new) [total_rows, Hkv, d] bf16 for the KV
         append.  ``mode``: what :meth:`run` launches -- "run" (attention),
-        "run_append" (append, then attention) or "append" (the append alone)."""
+        "run_append" (append, then attention) or "append" (the append alone).
+        ``interleave``: K and V pages (and NVFP4 scale pages) share one
+        allocation [num_pages, 2, Hkv, page_size, row], so the pools are views
+        with a page stride of twice their dense page."""
         import torch
         assert mode in ("run", "run_append", "append")
         assert mode == "run" or append_rows is not None
@@ -356,10 +370,23 @@ class DeviceWorkload:
         self.mode = mode
         dev = torch.device(device)
         self.q = wl.q.to(dev)
-        self.k_pool = wl.k_pool.to(dev)
-        self.v_pool = wl.v_pool.to(dev)
-        self.k_scales = None if wl.k_scales is None else wl.k_scales.to(dev)
-        self.v_scales = None if wl.v_scales is None else wl.v_scales.to(dev)
+        kv_stride = sc_stride = 0
+        if interleave:
+            both = torch.stack([wl.k_pool, wl.v_pool], 1).to(dev)          # [pages, 2, Hkv, ps, row]
+            self.kv_storage = both
+            self.k_pool, self.v_pool = both[:, 0], both[:, 1]
+            kv_stride = both[0].numel() * both.element_size()
+            self.k_scales = self.v_scales = None
+            if wl.k_scales is not None:
+                sboth = torch.stack([wl.k_scales, wl.v_scales], 1).to(dev)
+                self.scale_storage = sboth
+                self.k_scales, self.v_scales = sboth[:, 0], sboth[:, 1]
+                sc_stride = sboth[0].numel()
+        else:
+            self.k_pool = wl.k_pool.to(dev)
+            self.v_pool = wl.v_pool.to(dev)
+            self.k_scales = None if wl.k_scales is None else wl.k_scales.to(dev)
+            self.v_scales = None if wl.v_scales is None else wl.v_scales.to(dev)
         self.block_table = wl.block_table.to(dev)
         self.seq_lens = wl.seq_lens.to(dev)
         self.q_indptr = wl.q_indptr.to(dev)
@@ -373,7 +400,8 @@ class DeviceWorkload:
             page_size=wl.page_size, sm_scale=wl.sm_scale, force_splits=force_splits,
             kernel_variant=kernel_variant, seq_lens=wl.seq_lens if host_lens else None,
             q_indptr=wl.q_indptr if host_lens else None, w_invariant=w_invariant,
-            fixed_keys_per_split=fixed_keys_per_split)
+            fixed_keys_per_split=fixed_keys_per_split, window_left=wl.window_left, kv_page_stride=kv_stride,
+            scale_page_stride=sc_stride)
         self.workspace = torch.zeros(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device=dev)
         self.k_new = self.v_new = None
         if append_rows is not None:

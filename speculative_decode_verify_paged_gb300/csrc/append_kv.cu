@@ -5,7 +5,8 @@
 // steps overwrite the rows a rejection leaves stale, and attention reads only
 // seq_len entries).  seq_len_r already counts the window, so window row i of
 // request r is key ctx_r + i = seq_len_r - W_r + i: page
-// block_table[r][pos / 16], slot pos % 16, for K, V and every KV head.
+// block_table[r][pos / page_size], slot pos % page_size, for K, V and every
+// KV head.
 //
 // bf16 caches take the bits as they are.  NVFP4 caches quantise each run of
 // 16 head_dim elements against the tensor's decode scale g (one g per cache,
@@ -37,7 +38,6 @@ namespace spec_attn {
 namespace {
 
 constexpr int kAppendThreads = 256;
-constexpr int kPage = 16;
 
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
     uint4 v;
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const AppendP
     ReqInfo ri;
     // one thread per CTA reports a bad window or length
     if (!load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len, p.bt_capacity_keys,
-                      kPage, threadIdx.x == 0 ? p.status : nullptr, ri))
+                      p.page_size, threadIdx.x == 0 ? p.status : nullptr, ri))
         return;
     const int piece = idx % kPieces;
     int t = idx / kPieces;
@@ -100,15 +100,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const AppendP
     const uint4 a = ld_global_nc_v4(src);
     uint4 b = make_uint4(0u, 0u, 0u, 0u);
     if constexpr (FP4) b = ld_global_nc_v4(src + 8);
-    const int page = p.block_table[(size_t)r * p.bt_stride + pos / kPage];
+    const int page = p.block_table[(size_t)r * p.bt_stride + pos / p.page_size];
     if (page < 0 || page >= p.num_pages) {
         atomicOr(p.status, kDevBadPage);
         return;
     }
-    // token-head index of the destination slot
-    const size_t th = ((size_t)page * p.num_kv_heads + h) * kPage + (pos % kPage);
+    // the destination row within its page: KV head h, slot pos % page_size
+    const size_t slot = (size_t)h * p.page_size + (pos % p.page_size);
     if constexpr (!FP4) {
-        uint16_t* dst = static_cast<uint16_t*>(is_v ? p.v_pool : p.k_pool) + th * D + piece * kUnit;
+        unsigned char* dst = static_cast<unsigned char*>(is_v ? p.v_pool : p.k_pool) +
+                             (size_t)page * p.kv_page_stride + slot * (D * 2) + piece * (kUnit * 2);
         sm100::st_global_v4(dst, a);
     } else {
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -134,8 +135,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const AppendP
             c0 = e2m1x8_rn_sat(t0);
             c1 = e2m1x8_rn_sat(t1);
         }
-        uint8_t* codes = static_cast<uint8_t*>(is_v ? p.v_pool : p.k_pool) + th * (D / 2) + piece * 8;
-        uint8_t* scales = (is_v ? p.v_scales : p.k_scales) + th * (D / 16) + piece;
+        uint8_t* codes = static_cast<uint8_t*>(is_v ? p.v_pool : p.k_pool) + (size_t)page * p.kv_page_stride +
+                         slot * (D / 2) + piece * 8;
+        uint8_t* scales = (is_v ? p.v_scales : p.k_scales) + (size_t)page * p.scale_page_stride + slot * (D / 16) +
+                          piece;
         st_global_v2(codes, c0, c1);
         *scales = static_cast<uint8_t>(sb);
     }

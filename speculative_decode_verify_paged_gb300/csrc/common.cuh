@@ -71,18 +71,24 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
 // A request's window and cache, validated against the plan.  Invalid
 // requests set a status bit (when status != nullptr) and are skipped.
 struct ReqInfo {
-    int row0;     // first Q/O row
-    int w;        // window rows
-    int len;      // seq_len (keys in cache incl. the window's)
-    int ctx;      // len - w
-    int nsplits;  // splits of keys_per_split covering len
+    int row0;      // first Q/O row
+    int w;         // window rows
+    int len;       // seq_len (keys in cache incl. the window's)
+    int ctx;       // len - w
+    int key_base;  // first key any row may see, rounded down to the split alignment
+    int nsplits;   // splits of keys_per_split covering [key_base, len)
+    int split0;    // key_base / keys_per_split (whole when the alignment is keys_per_split)
 };
 
+// window_left > 0: a causal sliding window; no row sees a key below
+// ctx - window_left + 1 (row 0's bound), so the splits start at that key
+// rounded down to split_align (64, the key tile; or keys_per_split where
+// split boundaries must sit at fixed key positions).
 __device__ __forceinline__ bool load_request(const int32_t* seq_lens, const int32_t* q_indptr,
                                              int r, int max_w, int total_rows,
                                              long long max_seq_len, int cap_keys,
                                              int keys_per_split, unsigned int* status,
-                                             ReqInfo& ri) {
+                                             ReqInfo& ri, int window_left = 0, int split_align = 64) {
     // three independent loads: one memory round trip
     const int row0 = q_indptr[r];
     const int row1 = q_indptr[r + 1];
@@ -101,7 +107,14 @@ __device__ __forceinline__ bool load_request(const int32_t* seq_lens, const int3
     ri.w = w;
     ri.len = len;
     ri.ctx = len - w;
-    ri.nsplits = (len + keys_per_split - 1) / keys_per_split;
+    ri.key_base = 0;
+    ri.split0 = 0;
+    if (window_left > 0) {
+        const int lo0 = max(0, ri.ctx - window_left + 1);
+        ri.key_base = lo0 / split_align * split_align;
+        ri.split0 = ri.key_base / keys_per_split;
+    }
+    ri.nsplits = (len - ri.key_base + keys_per_split - 1) / keys_per_split;
     return true;
 }
 

@@ -18,12 +18,13 @@
 // split counts pack many pairs per CTA.  Groups are combined once through
 // shared memory.  Requests with a single split were finished by the split
 // kernel and are skipped, except in W-invariant mode, where every request is
-// merged and SG is the largest the CTA allows for D, a constant.  Split s then
-// always lands in group s mod SG, each group folds its splits in ascending
-// order and the groups are combined in group order, so the sum order of a
-// (row, head) pair never depends on the split count: a row that sees fewer
-// keys than its request's last row only has trailing splits with lse = -inf,
-// which every fold step skips.  The kernel may be launched as a programmatic
+// merged and SG is the largest the CTA allows for D, a constant.  Split s
+// (counted from key 0, also when a sliding window lets the request's splits
+// start later) then always lands in group s mod SG, each group folds its
+// splits in ascending order and the groups are combined in group order, so
+// the sum order of a (row, head) pair never depends on the split count: a
+// row that sees fewer keys than its request's last row only has splits with
+// lse = -inf, which every fold step skips.  The kernel may be launched as a programmatic
 // dependent of the split kernel: it waits on griddepcontrol before touching
 // partials, and it lets the next kernel in the stream launch early (that
 // kernel waits for this grid's completion before reading its outputs).
@@ -56,7 +57,8 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
 
     ReqInfo ri;
     const bool req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
-                                     p.bt_capacity_keys, p.keys_per_split, nullptr, ri);
+                                     p.bt_capacity_keys, p.keys_per_split, nullptr, ri, p.window_left,
+                                     p.split_align);
     const bool active = lp < ppc && req_ok && i < ri.w && (ri.nsplits > 1 || p.w_invariant);
     // Wait for the split kernel's partials (no-op without a programmatic edge).
     pdl_wait_primary();
@@ -70,7 +72,10 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
         const size_t pair0 = partial_pair(0, p.total_rows, p.num_q_heads, p.group, h / p.group, ri.row0 + i,
                                           h % p.group);
         const int n = ri.nsplits;
-        for (int s0 = g; s0 < n; s0 += sg * kBatch) {
+        // W-invariant mode: group g takes the splits whose index counted from
+        // key 0 (split0 + s) is g mod SG, whatever the request's first split
+        const int first = p.w_invariant ? ((g - ri.split0) % sg + sg) % sg : g;
+        for (int s0 = first; s0 < n; s0 += sg * kBatch) {
             float ls[kBatch], sc[kBatch];
             uint4 hv[kBatch];
 #pragma unroll

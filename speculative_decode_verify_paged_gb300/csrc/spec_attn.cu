@@ -39,6 +39,9 @@ struct spec_attn_plan {
     int smem;
     bool uses_merge;
     bool w_invariant;
+    int split_align;
+    int64_t kv_page_stride;     // bytes, resolved (dense when the problem gives 0)
+    int64_t scale_page_stride;
     size_t ws_bytes;
     size_t ws_ls_off;
     size_t ws_o_off;
@@ -131,7 +134,20 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
     if (p->max_w > SPEC_ATTN_MAX_W) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->num_q_heads / p->num_kv_heads > SPEC_ATTN_MAX_GROUP) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return SPEC_ATTN_E_UNSUPPORTED;
-    if (p->page_size != SPEC_ATTN_PAGE_SIZE) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->page_size != 16 && p->page_size != 32 && p->page_size != 64) return SPEC_ATTN_E_UNSUPPORTED;
+    if (p->window_left < 0 || (p->window_left > 0 && p->mask_mode != SPEC_ATTN_MASK_CAUSAL_IN_BLOCK))
+        return SPEC_ATTN_E_INVALID_ARG;
+    {
+        const int64_t row = static_cast<int64_t>(bytes_per_token_head(p->kv_dtype, p->head_dim) -
+                                                 (p->kv_dtype == SPEC_ATTN_KV_NVFP4 ? p->head_dim / 16 : 0));
+        const int64_t dense = static_cast<int64_t>(p->num_kv_heads) * p->page_size * row;
+        if (p->kv_page_stride != 0 && (p->kv_page_stride < dense || p->kv_page_stride % 16 != 0))
+            return SPEC_ATTN_E_INVALID_ARG;
+        const int64_t dense_sc = static_cast<int64_t>(p->num_kv_heads) * p->page_size * (p->head_dim / 16);
+        if (p->kv_dtype == SPEC_ATTN_KV_NVFP4 && p->scale_page_stride != 0 &&
+            (p->scale_page_stride < dense_sc || p->scale_page_stride % 16 != 0))
+            return SPEC_ATTN_E_INVALID_ARG;
+    }
     if (p->max_seq_len > INT32_MAX) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->num_kv_heads > 65535 || p->num_reqs > 65535) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->num_reqs > 0) {
@@ -170,7 +186,7 @@ const char* spec_attn_status_string(int status) {
     switch (status) {
         case SPEC_ATTN_OK: return "ok";
         case SPEC_ATTN_E_INVALID_ARG: return "invalid argument";
-        case SPEC_ATTN_E_UNSUPPORTED: return "unsupported by this build (W > 16, head_dim not in {64,128,256}, page_size != 16, group > 16, ...)";
+        case SPEC_ATTN_E_UNSUPPORTED: return "unsupported by this build (W > 16, head_dim not in {64,128,256}, page_size not in {16,32,64}, group > 16, ...)";
         case SPEC_ATTN_E_WORKSPACE_TOO_SMALL: return "workspace too small";
         case SPEC_ATTN_E_CUDA: return "CUDA runtime error";
         case SPEC_ATTN_E_DEVICE_CHECK: return "a device-side check tripped";
@@ -237,15 +253,42 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         return cuda_fail(e);
     }
 
+    {
+        const int64_t row = static_cast<int64_t>(p.kv_dtype == SPEC_ATTN_KV_NVFP4 ? p.head_dim / 2 : 2 * p.head_dim);
+        plan->kv_page_stride = p.kv_page_stride ? p.kv_page_stride
+                                                : static_cast<int64_t>(p.num_kv_heads) * p.page_size * row;
+        plan->scale_page_stride = p.scale_page_stride
+                                      ? p.scale_page_stride
+                                      : static_cast<int64_t>(p.num_kv_heads) * p.page_size * (p.head_dim / 16);
+    }
+
     // ---- split heuristic ----
+    // With a sliding window a request's splits cover only [key_base, len),
+    // key_base = its first visible key rounded down to split_align (the key
+    // tile, or the fixed split length in W-invariant mode); the lengths the
+    // heuristic weighs are those spans.
+    const int fixed_kps = p.fixed_keys_per_split > 0 ? p.fixed_keys_per_split : 512;
+    plan->split_align = plan->w_invariant ? fixed_kps : kSplitUnit;
+    auto span = [&](int64_t len, int64_t w) {
+        if (p.window_left <= 0) return len;
+        const int64_t lo0 = std::max<int64_t>(0, len - w - p.window_left + 1);
+        return len - lo0 / plan->split_align * plan->split_align;
+    };
     std::vector<int64_t> lens;
     lens.reserve(static_cast<size_t>(p.num_reqs));
+    // without host lengths: the longest span any request can have
+    const int64_t span_bound =
+        p.window_left > 0
+            ? std::min<int64_t>(p.max_seq_len, static_cast<int64_t>(p.max_w) + p.window_left - 1 + plan->split_align - 1)
+            : p.max_seq_len;
     for (int r = 0; r < p.num_reqs; ++r) {
-        int64_t L = h_seq_lens ? h_seq_lens[r] : p.max_seq_len;
+        int64_t L = span_bound;
+        if (h_seq_lens && h_q_indptr) L = span(h_seq_lens[r], h_q_indptr[r + 1] - h_q_indptr[r]);
+        else if (h_seq_lens) L = std::min<int64_t>(h_seq_lens[r], span_bound);
         if (h_q_indptr && h_q_indptr[r + 1] == h_q_indptr[r]) L = 0;  // empty window: no CTAs do work
         lens.push_back(L);
     }
-    const int64_t max_seq = std::max<int64_t>(1, p.max_seq_len);
+    const int64_t max_seq = std::max<int64_t>(1, span_bound);
     const size_t bkh = bytes_per_token_head(p.kv_dtype, p.head_dim);
     double total_bytes = 0;
     for (int64_t L : lens) total_bytes += static_cast<double>(L) * p.num_kv_heads * 2.0 * bkh;
@@ -275,7 +318,7 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     const double partial_bytes = static_cast<double>(p.total_q_rows) * p.num_q_heads * (p.head_dim * 2.0 + 8.0) * 2.0;
     if (plan->w_invariant) {
         // split boundaries fixed by key position alone (never by W, P or lengths)
-        plan->keys_per_split = p.fixed_keys_per_split > 0 ? p.fixed_keys_per_split : 512;
+        plan->keys_per_split = fixed_kps;
     } else if (p.force_splits > 0) {
         int64_t c = (max_seq + p.force_splits - 1) / p.force_splits;
         c = (c + kSplitUnit - 1) / kSplitUnit * kSplitUnit;
@@ -414,6 +457,9 @@ static int append_launch_checked(const spec_attn_plan* plan, const void* k_new, 
     ap.bt_stride = p.block_table_stride;
     ap.bt_capacity_keys = p.block_table_stride * p.page_size;
     ap.max_seq_len = p.max_seq_len;
+    ap.page_size = p.page_size;
+    ap.kv_page_stride = plan->kv_page_stride;
+    ap.scale_page_stride = plan->scale_page_stride;
     const cudaError_t e = append_launch(ap, p.kv_dtype, stream);
     return e == cudaSuccess ? SPEC_ATTN_OK : cuda_fail(e);
 }
@@ -470,6 +516,11 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     const bool fp4 = p.kv_dtype == SPEC_ATTN_KV_NVFP4;
     sp.score_scale_log2 = plan->sm_scale * log2e * (fp4 ? k_gscale : 1.0f);
     sp.out_scale = fp4 ? v_gscale : 1.0f;
+    sp.page_shift = p.page_size == 64 ? 2 : p.page_size == 32 ? 1 : 0;
+    sp.kv_page_stride = plan->kv_page_stride;
+    sp.scale_page_stride = plan->scale_page_stride;
+    sp.window_left = p.window_left;
+    sp.split_align = plan->split_align;
 
     spec_attn_plan* mp = const_cast<spec_attn_plan*>(plan);
     std::unique_lock<std::mutex> maps_lock(mp->maps_mutex, std::defer_lock);
@@ -522,6 +573,8 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         mp.max_seq_len = p.max_seq_len;
         mp.bt_capacity_keys = p.block_table_stride * p.page_size;
         mp.w_invariant = plan->w_invariant ? 1 : 0;
+        mp.window_left = p.window_left;
+        mp.split_align = plan->split_align;
         // programmatic launch lets the merge's CTAs become resident while the
         // split kernel drains; it is skipped when a timing event sits between.
         e = merge_launch(mp, stream, plan->ev_end == nullptr);

@@ -43,6 +43,11 @@ struct SplitParams {
     long long max_seq_len;
     float score_scale_log2;     // sm_scale * log2(e) [* k_gscale for NVFP4]
     float out_scale;            // 1, or v_gscale for NVFP4
+    int page_shift;             // log2(page_size / 16): 16-key units per page = 1 << page_shift
+    long long kv_page_stride;   // bytes between pages of a K or V pool
+    long long scale_page_stride;// bytes between pages of a scale pool (NVFP4)
+    int window_left;            // causal sliding window (keys), 0 = none
+    int split_align;            // first split of a request starts at a multiple of this (keys)
 };
 
 struct MergeParams {
@@ -63,6 +68,8 @@ struct MergeParams {
     long long max_seq_len;
     int bt_capacity_keys;       // bt_stride * page_size
     int w_invariant;            // merge every request (one split too), splits folded in order
+    int window_left;            // as SplitParams
+    int split_align;
 };
 
 // Everything one KV-append launch needs (append_kv.cu).
@@ -88,6 +95,9 @@ struct AppendParams {
     int bt_stride;
     int bt_capacity_keys;       // bt_stride * page_size
     long long max_seq_len;
+    int page_size;
+    long long kv_page_stride;   // bytes between pages of a K or V pool
+    long long scale_page_stride;// bytes between pages of a scale pool (NVFP4)
 };
 
 // Split partials.  A split leaves, per (window row, query head) pair, its

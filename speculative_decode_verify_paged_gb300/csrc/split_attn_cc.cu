@@ -6,16 +6,18 @@
 // so the K/V pages of a split are read once for all those rows: the single
 // sweep per window the page "ChunkedSmallT re-streams full KV per query
 // chunk (DFlash K>=8 verify at long context)" (section "Finding") asks for,
-// for every W up to 16.  Pages are fetched through the block table with
-// 16-byte cp.async copies into a ring of shared-memory stages.
+// for every W up to 16.  Keys are fetched in 16-key units (a whole page of 16
+// keys, or a half or quarter of a 32- or 64-key page) through the block table
+// with 16-byte cp.async copies into a ring of shared-memory stages.
 //
 // Each warp owns RPW rows; lane l owns head_dim elements [l*D/32, (l+1)*D/32).
-// Per 16-key page: partial dot products per lane, a transposing butterfly
-// reduction (16 shuffles for 16 keys), the causal-in-block / non-causal mask
-// by key index, an online softmax in base 2 (scores pre-scaled by
-// sm_scale * log2 e), and O += p * V.  A split's result is written as the
-// final bf16 output when the request has one split, else as an fp32 partial
-// (O / l and its log2-sum-exp) for the LSE merge.
+// Per unit: partial dot products per lane, a transposing butterfly reduction
+// (16 shuffles for 16 keys), the causal-in-block / non-causal mask and the
+// sliding window by key index, an online softmax in base 2 (scores
+// pre-scaled by sm_scale * log2 e), and O += p * V.  A split's result is
+// written as the final bf16 output when the request has one split, else as
+// the split partial (fp16 O / l over its scale, the log2-sum-exp and the
+// scale) for the LSE merge.
 //
 // NVFP4 pages are decoded in registers: e2m1 code * e4m3 block scale; the
 // per-tensor global scales are folded into the score scale (K) and the
@@ -28,14 +30,14 @@
 namespace spec_attn {
 namespace {
 
-constexpr int kPage = 16;
+constexpr int kUnit = 16;   // keys per unit
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
 template <int D, int KV>
 struct CcStage {
-    static constexpr int kCodeBytes = (KV == 0) ? kPage * D * 2 : kPage * D / 2;  // per K or V page
-    static constexpr int kScaleBytes = (KV == 0) ? 0 : kPage * D / 16;
+    static constexpr int kCodeBytes = (KV == 0) ? kUnit * D * 2 : kUnit * D / 2;  // per K or V page
+    static constexpr int kScaleBytes = (KV == 0) ? 0 : kUnit * D / 16;
     static constexpr int kHalf = kCodeBytes + kScaleBytes;
     static constexpr int kBytes = 2 * kHalf;  // K then V
     static_assert(kCodeBytes % 16 == 0 && kScaleBytes % 16 == 0, "16-byte chunks");
@@ -152,7 +154,8 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
     ReqInfo ri;
     const bool reporter = (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0);
     if (!load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
-                      p.bt_stride * kPage, p.keys_per_split, reporter ? p.status : nullptr, ri))
+                      p.bt_stride << (4 + p.page_shift), p.keys_per_split, reporter ? p.status : nullptr, ri,
+                      p.window_left, p.split_align))
         return;
     if (split >= ri.nsplits) return;
     const int G = p.group;
@@ -160,14 +163,18 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
     const int row_lo = rg * p.rows_per_cta;
     if (row_lo >= R) return;
 
-    const int key_lo = split * p.keys_per_split;
+    const int key_lo = ri.key_base + split * p.keys_per_split;
     const int key_hi = min(key_lo + p.keys_per_split, ri.len);
-    const int page_first = key_lo / kPage;
-    const int npages = (key_hi - 1) / kPage - page_first + 1;
+    // the loop runs over 16-key units: unit u is slots (u & sub_mask) * 16 .. +15
+    // of page block_table[r][u >> page_shift]
+    const int page_first = key_lo / kUnit;
+    const int npages = (key_hi - 1) / kUnit - page_first + 1;
     const int32_t* bt_row = p.block_table + (size_t)r * p.bt_stride;
+    const int page_keys = kUnit << p.page_shift;
+    const int sub_mask = (1 << p.page_shift) - 1;
 
     // ---- this warp's rows ----
-    int m_row[RPW], hq[RPW], qrow[RPW], hi_key[RPW];
+    int m_row[RPW], hq[RPW], qrow[RPW], hi_key[RPW], lo_key[RPW];
     bool valid[RPW];
     float q[RPW][DPL];
     float o_acc[RPW][DPL];
@@ -183,6 +190,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
         hq[t] = kvh * G + (valid[t] ? m_row[t] % G : 0);
         qrow[t] = ri.row0 + i;
         hi_key[t] = (p.mask_mode == 0) ? (ri.ctx + i) : (ri.len - 1);
+        lo_key[t] = (p.window_left > 0) ? max(0, hi_key[t] - p.window_left + 1) : 0;
         m_run[t] = -INFINITY;
         l_run[t] = 0.f;
         tr_cnt[t] = 0;
@@ -198,22 +206,26 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
     // ---- page loader (all threads) ----
     auto issue_page = [&](int pi) {
         if (pi < npages) {
-            int phys = bt_row[page_first + pi];
+            const int u = page_first + pi;
+            int phys = bt_row[u >> p.page_shift];
             if (phys < 0 || phys >= p.num_pages) {
                 if (tid == 0) atomicOr(p.status, kDevBadPage);
                 phys = 0;
             }
             unsigned char* st = smem + (size_t)(pi % stages) * Stage::kBytes;
-            const size_t tok = ((size_t)phys * p.num_kv_heads + kvh) * kPage;
-            const unsigned char* ksrc = static_cast<const unsigned char*>(p.k_pool) + tok * (Stage::kCodeBytes / kPage);
-            const unsigned char* vsrc = static_cast<const unsigned char*>(p.v_pool) + tok * (Stage::kCodeBytes / kPage);
+            // first slot of the unit within its page-head
+            const size_t slot0 = (size_t)kvh * page_keys + (u & sub_mask) * kUnit;
+            const size_t kv_off = (size_t)phys * p.kv_page_stride + slot0 * (Stage::kCodeBytes / kUnit);
+            const unsigned char* ksrc = static_cast<const unsigned char*>(p.k_pool) + kv_off;
+            const unsigned char* vsrc = static_cast<const unsigned char*>(p.v_pool) + kv_off;
             for (int c = tid; c < Stage::kCodeBytes / 16; c += kThreads) {
                 cp_async16(st + c * 16, ksrc + c * 16);
                 cp_async16(st + Stage::kHalf + c * 16, vsrc + c * 16);
             }
             if constexpr (KV == 1) {
-                const unsigned char* kss = p.k_scales + tok * (D / 16);
-                const unsigned char* vss = p.v_scales + tok * (D / 16);
+                const size_t sc_off = (size_t)phys * p.scale_page_stride + slot0 * (D / 16);
+                const unsigned char* kss = p.k_scales + sc_off;
+                const unsigned char* vss = p.v_scales + sc_off;
                 for (int c = tid; c < Stage::kScaleBytes / 16; c += kThreads) {
                     cp_async16(st + Stage::kCodeBytes + c * 16, kss + c * 16);
                     cp_async16(st + Stage::kHalf + Stage::kCodeBytes + c * 16, vss + c * 16);
@@ -230,7 +242,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
         cp_async_wait_dyn(stages - 1);
         __syncthreads();
         const unsigned char* st = smem + (size_t)(pi % stages) * Stage::kBytes;
-        const int kbase = (page_first + pi) * kPage;
+        const int kbase = (page_first + pi) * kUnit;
         if (any_valid) {
             // scores for the 16 keys of this page
             float part[RPW][16];
@@ -251,7 +263,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
 #pragma unroll
             for (int t = 0; t < RPW; ++t) {
                 const float sc = transpose_reduce16(part[t], lane);
-                const bool vis = (key < key_hi) && (key <= hi_key[t]);
+                const bool vis = (key < key_hi) && (key <= hi_key[t]) && (key >= lo_key[t]);
                 float mx = vis ? sc : -INFINITY;
 #pragma unroll
                 for (int off = 2; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
@@ -268,10 +280,10 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
                 pj[t] = pv;
                 if constexpr (TRACE) {
                     if (vis && (lane & 1) == 0) {
-                        int phys = bt_row[page_first + pi];
+                        int phys = bt_row[(page_first + pi) >> p.page_shift];
                         if (phys < 0 || phys >= p.num_pages) phys = 0;
                         tr_cnt[t] += 1;
-                        tr_sum[t] += (long long)phys * kPage + (key % kPage);
+                        tr_sum[t] += (long long)phys * page_keys + (key & (page_keys - 1));
                     }
                 }
             }
@@ -378,8 +390,8 @@ CcKernel pick(int d, int kv, int rpw, bool traced) {
 }
 
 int stage_bytes(int d, int kv) {
-    const int code = (kv == 0) ? kPage * d * 2 : kPage * d / 2;
-    const int scale = (kv == 0) ? 0 : kPage * d / 16;
+    const int code = (kv == 0) ? kUnit * d * 2 : kUnit * d / 2;
+    const int scale = (kv == 0) ? 0 : kUnit * d / 16;
     return 2 * (code + scale);
 }
 

@@ -89,12 +89,18 @@ struct TcLayout {
     static constexpr int kPBytes = KV ? 0 : kM * 128 * (kBN == 64 ? 2 : 1);
     static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile (16-bit elements)
     static constexpr int kPageBytes = 16 * D * 2;          // one page-head of V (16-bit elements)
-    static constexpr int kRawCodePage = 16 * D / 2;        // NVFP4 codes of one page-head
-    static constexpr int kRawScalePage = 16 * D / 16;      // NVFP4 scales of one page-head
+    // NVFP4 raw slot: the codes and scales of a tile's 16-key units, K then V.
+    // Every TMA tile copy lands on a 128-byte boundary (the tensor copy's
+    // shared-memory alignment), so a unit's scales (d bytes: 64 at d = 64)
+    // take at least 128.
+    static constexpr int kRawCodePage = 16 * D / 2;        // NVFP4 codes of one 16-key unit
+    static constexpr int kRawScaleBox = 16 * D / 16;       // NVFP4 scales of one unit (bytes copied)
+    static constexpr int kRawScalePage = kRawScaleBox < 128 ? 128 : kRawScaleBox;   // their spacing
     static constexpr int kRawKS = kPPT * kRawCodePage;     // offsets inside a raw slot
     static constexpr int kRawVC = kRawKS + kPPT * kRawScalePage;
     static constexpr int kRawVS = kRawVC + kPPT * kRawCodePage;
     static constexpr int kRawTile = 2 * kPPT * (kRawCodePage + kRawScalePage);
+    static_assert(kRawCodePage % 128 == 0 && kRawScalePage % 128 == 0, "TMA destinations on 128 B");
     static constexpr int kAuxBytes = 1536;
     static constexpr int kMaxDyn = 232448;                  // 227 KB opt-in limit
     static constexpr int kFixed = 1024 + kQSmem + kPBytes + kAuxBytes;
@@ -181,23 +187,29 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
                                        TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane,
                                        int pre0, int pre1) {
     using L = TcLayout<D, 0>;
-    const int32_t* bt = p.block_table + (size_t)r * p.bt_stride + key_lo / 16;
-    const int n_pages = (key_hi - key_lo + 15) / 16;
+    const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
+    const int u_lo = key_lo / 16;                    // first 16-key unit of the split
+    const int n_pages = (key_hi - key_lo + 15) / 16;  // 16-key units
+    const int sub_mask = (1 << p.page_shift) - 1;
     int list_base = 0;
-    auto checked = [&](int pg) {
+    // list entries are 16-key units: (page << page_shift) | unit within the page
+    auto unit = [&](int pg, int u) {
         if (pg < 0 || pg >= p.num_pages) {
             if (!IS_V) atomicOr(p.status, kDevBadPage);
             pg = 0;
         }
-        return pg;
+        return (pg << p.page_shift) | (u & sub_mask);
     };
     auto fill_list = [&](int base) {
-        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) list[i] = checked(bt[base + i]);
+        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) {
+            const int u = u_lo + base + i;
+            list[i] = unit(bt[u >> p.page_shift], u);
+        }
         __syncwarp();
     };
-    // the first 64 entries were fetched at kernel start
-    if (lane < n_pages) list[lane] = checked(pre0);
-    if (lane + 32 < n_pages) list[lane + 32] = checked(pre1);
+    // the first 64 entries were fetched by the caller
+    if (lane < n_pages) list[lane] = unit(pre0, u_lo + lane);
+    if (lane + 32 < n_pages) list[lane + 32] = unit(pre1, u_lo + lane + 32);
     __syncwarp();
     int issued = 0;
     for (int t = 0; t < T; ++t) {
@@ -221,14 +233,16 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
             if (lane < np) {
                 const int pg = list[rel - list_base + lane];
                 if (TRACE) aux->pages_v[slot][lane] = pg;
-                tma_load_5d(dst + lane * L::kPageBytes, tm, 0, 0, 0, kvh, pg, &full[slot]);
+                tma_load_5d(dst + lane * L::kPageBytes, tm, 0, (pg & sub_mask) * 16, 0, kvh, pg >> p.page_shift,
+                            &full[slot]);
             }
         } else if (lane < np * L::kChunks) {
-            // lane (pp, c): chunk c of page pp, chunk-major across the tile's
-            // pages so that S = Q K^T spans the tile in one MMA
+            // lane (pp, c): chunk c of unit pp, chunk-major across the tile's
+            // units so that S = Q K^T spans the tile in one MMA
             const int pp = lane / L::kChunks, c = lane % L::kChunks;
             const int pg = list[rel - list_base + pp];
-            tma_load_4d(dst + c * (kBN * 128) + pp * 2048, tm, c * 64, 0, kvh, pg, &full[slot]);
+            tma_load_4d(dst + c * (kBN * 128) + pp * 2048, tm, c * 64, (pg & sub_mask) * 16, kvh,
+                        pg >> p.page_shift, &full[slot]);
         }
         __syncwarp();
         issued = t + 1;
@@ -255,24 +269,29 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
                                            volatile int* abort, int lane, int pre0, int pre1) {
     using L = TcLayout<D, 1>;
     constexpr int NR = L::kNR;
-    const int32_t* bt = p.block_table + (size_t)r * p.bt_stride + key_lo / 16;
-    const int n_pages = (key_hi - key_lo + 15) / 16;
+    const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
+    const int u_lo = key_lo / 16;
+    const int n_pages = (key_hi - key_lo + 15) / 16;   // 16-key units
+    const int sub_mask = (1 << p.page_shift) - 1;
     int32_t* list = aux->list_k;
     int list_base = 0;
-    auto checked = [&](int pg) {
+    auto unit = [&](int pg, int u) {
         if (pg < 0 || pg >= p.num_pages) {
             atomicOr(p.status, kDevBadPage);
             pg = 0;
         }
-        return pg;
+        return (pg << p.page_shift) | (u & sub_mask);
     };
     auto fill_list = [&](int base) {
-        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) list[i] = checked(bt[base + i]);
+        for (int i = lane; i < kPageListCap && base + i < n_pages; i += 32) {
+            const int u = u_lo + base + i;
+            list[i] = unit(bt[u >> p.page_shift], u);
+        }
         __syncwarp();
     };
-    // the first 64 entries were fetched at kernel start
-    if (lane < n_pages) list[lane] = checked(pre0);
-    if (lane + 32 < n_pages) list[lane + 32] = checked(pre1);
+    // the first 64 entries were fetched by the caller
+    if (lane < n_pages) list[lane] = unit(pre0, u_lo + lane);
+    if (lane + 32 < n_pages) list[lane + 32] = unit(pre1, u_lo + lane + 32);
     __syncwarp();
     int issued = 0;
     for (int t = 0; t < T; ++t) {
@@ -291,17 +310,17 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
         __syncwarp();
         if (lane == 0)
             mbar_arrive_expect_tx(&aux->raw_full[slot],
-                                  static_cast<uint32_t>(np * 2 * (L::kRawCodePage + L::kRawScalePage)));
+                                  static_cast<uint32_t>(np * 2 * (L::kRawCodePage + L::kRawScaleBox)));
         __syncwarp();
         if (lane < 4 * np) {
             const int pp = lane >> 2, kind = lane & 3;
             const int pg = list[rel - list_base + pp];
-            const int z = pg * p.num_kv_heads + kvh;   // page-head index
+            const int page = pg >> p.page_shift, sub = pg & sub_mask;
             uint64_t* bar = &aux->raw_full[slot];
-            if (kind == 0) tma_load_3d(dst + pp * L::kRawCodePage, tkc, 0, 0, z, bar);
-            else if (kind == 1) tma_load_3d(dst + L::kRawVC + pp * L::kRawCodePage, tvc, 0, 0, z, bar);
-            else if (kind == 2) tma_load_2d(dst + L::kRawKS + pp * L::kRawScalePage, tks, 0, z, bar);
-            else tma_load_2d(dst + L::kRawVS + pp * L::kRawScalePage, tvs, 0, z, bar);
+            if (kind == 0) tma_load_4d(dst + pp * L::kRawCodePage, tkc, 0, sub * 16, kvh, page, bar);
+            else if (kind == 1) tma_load_4d(dst + L::kRawVC + pp * L::kRawCodePage, tvc, 0, sub * 16, kvh, page, bar);
+            else if (kind == 2) tma_load_3d(dst + L::kRawKS + pp * L::kRawScalePage, tks, sub * D, kvh, page, bar);
+            else tma_load_3d(dst + L::kRawVS + pp * L::kRawScalePage, tvs, sub * D, kvh, page, bar);
         }
         __syncwarp();
         issued = t + 1;
@@ -480,25 +499,34 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     // parameters), which lets it start while the previous kernel in the stream
     // drains; from here on it reads what that kernel may have written.
     pdl_wait_primary();
-    const int key_lo = split * p.keys_per_split;
-    // The split's first block-table entries sit at a fixed place, so the
-    // producers fetch them in the same memory round trip as the request's
-    // window and length (entries past the request's pages are never used).
+    // Without a sliding window the split's first block-table entries sit at a
+    // fixed place, so the producers fetch them in the same memory round trip
+    // as the request's window and length (entries past the request's pages
+    // are never used); with one, the split starts at a key that depends on
+    // the length, so they follow it.
+    int key_lo = split * p.keys_per_split;
     int pre0 = -1, pre1 = -1;
-    if ((warp == 0 || (!KV && warp == 2)) && r < p.num_reqs) {
+    const bool prefetcher = (warp == 0 || (!KV && warp == 2)) && r < p.num_reqs;
+    auto prefetch = [&]() {
         const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
-        const int i0 = key_lo / 16 + lane;
-        if (i0 < p.bt_stride) pre0 = bt[i0];
-        if (i0 + 32 < p.bt_stride) pre1 = bt[i0 + 32];
-    }
+        const int u0 = key_lo / 16 + lane;
+        if ((u0 >> p.page_shift) < p.bt_stride) pre0 = bt[u0 >> p.page_shift];
+        if (((u0 + 32) >> p.page_shift) < p.bt_stride) pre1 = bt[(u0 + 32) >> p.page_shift];
+    };
+    if (prefetcher && p.window_left == 0) prefetch();
     ReqInfo ri;
     const bool reporter = (tid == 0 && split == 0 && kvh == 0);
     const bool active = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
-                                     p.bt_stride * 16, p.keys_per_split, reporter ? p.status : nullptr, ri) &&
+                                     p.bt_stride << (4 + p.page_shift), p.keys_per_split,
+                                     reporter ? p.status : nullptr, ri, p.window_left, p.split_align) &&
                         split < ri.nsplits;
     if (!active) {   // uniform across the CTA
         if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
         return;
+    }
+    if (p.window_left > 0) {
+        key_lo = ri.key_base + split * p.keys_per_split;
+        if (prefetcher) prefetch();
     }
     const int G = p.group;
     const int R = ri.w * G;  // <= 128: the plan admits this kernel only when max_w * G <= 128
@@ -643,6 +671,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         const int hq = kvh * G + (valid ? m % G : 0);
         const int qrow = ri.row0 + i;
         const int hi = (p.mask_mode == 0) ? (ri.ctx + i) : (ri.len - 1);
+        const int lo = (p.window_left > 0) ? max(0, hi - p.window_left + 1) : 0;   // first visible key
         const float sc = p.score_scale_log2;
         float m_ref = -INFINITY, l_sum = 0.f;
         long long tr_cnt = 0, tr_sum = 0;
@@ -698,18 +727,19 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             if (lane == 0) mbar_arrive(&aux->s_empty[sb]);
 
             const int key0 = key_lo + t * kBN;
-            const int lim = valid ? (min(key_hi - 1, hi) - key0) : -1;  // visible iff c <= lim
+            const int lim = valid ? (min(key_hi - 1, hi) - key0) : -1;  // visible iff lim_lo <= c <= lim
+            const int lim_lo = lo - key0;
             // Scores stay unscaled: the maximum is taken on raw scores (sc > 0) and
             // the scale is folded into one FFMA per exponent.  Tiles whose keys
             // are all visible to every row of the warp skip the mask.
             float mraw = -INFINITY;
-            if (__all_sync(kFullMask, lim >= kBN - 1)) {
+            if (__all_sync(kFullMask, lim >= kBN - 1 && lim_lo <= 0)) {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) mraw = fmaxf(mraw, sv[c]);
             } else {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
-                    if (c > lim) sv[c] = -INFINITY;
+                    if (c > lim || c < lim_lo) sv[c] = -INFINITY;
                     mraw = fmaxf(mraw, sv[c]);
                 }
             }
@@ -778,7 +808,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 }
             }
             if (TRACE) {
-                for (int c = 0; c <= lim && c < kBN; ++c) {
+                for (int c = max(0, lim_lo); c <= lim && c < kBN; ++c) {
                     const int key = key0 + c;
                     tr_cnt += 1;
                     tr_sum += (long long)aux->pages_v[vs][c >> 4] * 16 + (key & 15);
@@ -993,28 +1023,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Pool [num_pages, Hkv, 16, d] bf16 viewed as a 4-D tensor (d, slot, kv head, page);
-// box = 64 head_dim elements x 16 slots of one page and head, 128-byte swizzle.
-// The same pool as a 5-D tensor (64 elements, slot, 64-element chunk, kv head,
-// page); box = one whole page-head, landing chunk-major: [chunk][16 slots][128 B].
-bool encode_pool_map_pages(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
+// Pool pages [Hkv, ps, d] bf16, page_stride bytes apart, viewed as a 4-D tensor
+// (d, slot, kv head, page); box = 64 head_dim elements x 16 slots of one page
+// and head (one 16-key unit), 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d, int ps,
+                     long long page_stride) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[5] = {64, 16, (cuuint64_t)d / 64, (cuuint64_t)hkv, (cuuint64_t)num_pages};
-    cuuint64_t strides[4] = {(cuuint64_t)d * 2, 128, (cuuint64_t)d * 2 * 16, (cuuint64_t)d * 2 * 16 * hkv};
-    cuuint32_t box[5] = {64, 16, (cuuint32_t)d / 64, 1, 1};
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return res == CUDA_SUCCESS;
-}
-
-bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)d, 16, (cuuint64_t)hkv, (cuuint64_t)num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * 16, (cuuint64_t)d * 2 * 16 * hkv};
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)ps, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * ps, (cuuint64_t)page_stride};
     cuuint32_t box[4] = {64, 16, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides, box, estr,
@@ -1023,35 +1040,54 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int num_pages, int hkv,
     return res == CUDA_SUCCESS;
 }
 
-// NVFP4 code pool [num_pages, Hkv, 16, d/2] bytes viewed as (d/2 bytes, slot,
-// page-head); box = one page-head, swizzled 128/64/32 bytes for d = 256/128/64
-// (the row is d/2 bytes).
-bool encode_code_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
+// The same pool as a 5-D tensor (64 elements, slot, 64-element chunk, kv head,
+// page); box = one whole 16-key unit of a page-head, landing chunk-major:
+// [chunk][16 slots][128 B].
+bool encode_pool_map_units(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d, int ps,
+                           long long page_stride) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d / 2, 16, (cuuint64_t)num_pages * hkv};
-    cuuint64_t strides[2] = {(cuuint64_t)d / 2, (cuuint64_t)d / 2 * 16};
-    cuuint32_t box[3] = {(cuuint32_t)d / 2, 16, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
+    cuuint64_t dims[5] = {64, (cuuint64_t)ps, (cuuint64_t)d / 64, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)d * 2, 128, (cuuint64_t)d * 2 * ps, (cuuint64_t)page_stride};
+    cuuint32_t box[5] = {64, 16, (cuuint32_t)d / 64, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+// NVFP4 code pool pages [Hkv, ps, d/2] bytes viewed as (d/2 bytes, slot, kv head,
+// page); box = one 16-key unit of a page-head, swizzled 128/64/32 bytes for
+// d = 256/128/64 (the row is d/2 bytes).
+bool encode_code_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d, int ps,
+                     long long page_stride) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d / 2, (cuuint64_t)ps, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)d / 2, (cuuint64_t)d / 2 * ps, (cuuint64_t)page_stride};
+    cuuint32_t box[4] = {(cuuint32_t)d / 2, 16, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapSwizzle sw = d == 256 ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : d == 128 ? CU_TENSOR_MAP_SWIZZLE_64B
                                              : CU_TENSOR_MAP_SWIZZLE_32B;
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool), dims, strides, box, estr,
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(pool), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
 }
 
-// NVFP4 scale pool [num_pages, Hkv, 16, d/16] bytes viewed as (d bytes, page-head);
-// box = one page-head's scales.
-bool encode_scale_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d) {
+// NVFP4 scale pool pages [Hkv, ps, d/16] bytes viewed as (ps * d/16 bytes, kv
+// head, page); box = the d bytes of scales of one 16-key unit.
+bool encode_scale_map(CUtensorMap* map, const void* pool, int num_pages, int hkv, int d, int ps,
+                      long long page_stride) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)num_pages * hkv};
-    cuuint64_t strides[1] = {(cuuint64_t)d};
-    cuuint32_t box[2] = {(cuuint32_t)d, 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box, estr,
+    cuuint64_t dims[3] = {(cuuint64_t)ps * d / 16, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[2] = {(cuuint64_t)ps * d / 16, (cuuint64_t)page_stride};
+    cuuint32_t box[3] = {(cuuint32_t)d, 1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
@@ -1097,21 +1133,22 @@ bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
     if (!encode_q_map(reinterpret_cast<CUtensorMap*>(maps->q), p.q, p.total_rows, p.num_q_heads, p.head_dim,
                       p.group, p.max_w))
         return false;
+    const int ps = 16 << p.page_shift;
     if (kv_dtype != 0)
         return encode_code_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
-                               p.head_dim) &&
+                               p.head_dim, ps, p.kv_page_stride) &&
                encode_code_map(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,
-                               p.head_dim) &&
+                               p.head_dim, ps, p.kv_page_stride) &&
                encode_scale_map(reinterpret_cast<CUtensorMap*>(maps->ks), p.k_scales, p.num_pages,
-                                p.num_kv_heads, p.head_dim) &&
+                                p.num_kv_heads, p.head_dim, ps, p.scale_page_stride) &&
                encode_scale_map(reinterpret_cast<CUtensorMap*>(maps->vs), p.v_scales, p.num_pages,
-                                p.num_kv_heads, p.head_dim);
+                                p.num_kv_heads, p.head_dim, ps, p.scale_page_stride);
     memset(maps->ks, 0, sizeof(maps->ks));
     memset(maps->vs, 0, sizeof(maps->vs));
     return encode_pool_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
-                           p.head_dim) &&
-           encode_pool_map_pages(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,
-                                 p.head_dim);
+                           p.head_dim, ps, p.kv_page_stride) &&
+           encode_pool_map_units(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,
+                                 p.head_dim, ps, p.kv_page_stride);
 }
 
 cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bool traced, dim3 grid,

@@ -101,9 +101,15 @@ class Workload:
 
     @property
     def kv_bytes(self) -> int:
-        """Algorithmic K+V bytes one call reads: every cached key of every
-        request, every KV head, K and V once (a single sweep)."""
-        return int(self.seq_lens.sum().item()) * self.num_kv_heads * 2 * self.bytes_per_token_head
+        """Algorithmic K+V bytes one call reads: every key some window row of
+        the request may see (all cached keys, or with a sliding window the last
+        W + window_left - 1), every KV head, K and V once (a single sweep)."""
+        keys = 0
+        for r in range(self.num_reqs):
+            L = int(self.seq_lens[r])
+            w = int(self.q_indptr[r + 1] - self.q_indptr[r])
+            keys += min(L, w + self.window_left - 1) if self.window_left > 0 and w > 0 else L
+        return keys * self.num_kv_heads * 2 * self.bytes_per_token_head
 
     @property
     def append_bytes(self) -> int:
@@ -270,9 +276,9 @@ def tiny(seed: int = 0, **kw) -> Workload:
                          pool_pages=17, fragmented=False, **kw)
 
 
-def verify_sweep(w: int, seed: int = 0, ctx: int = 16384, **kw) -> Workload:
+def verify_sweep(w: int, seed: int = 0, ctx: int = 16384, pool_pages: int = 2048, **kw) -> Workload:
     return make_workload(f"verify_sweep_ctx{ctx}_w{w}", [ctx], w, 24, 4, 256,
-                         MASK_CAUSAL_IN_BLOCK, seed=seed, pool_pages=2048, **kw)
+                         MASK_CAUSAL_IN_BLOCK, seed=seed, pool_pages=pool_pages, **kw)
 
 
 def long_verify(w: int, seed: int = 0, ctx: int = 65536, **kw) -> Workload:

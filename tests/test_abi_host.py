@@ -58,7 +58,14 @@ def _problem(**over):
 @pytest.mark.parametrize("over,status", [
     (dict(max_w=17), sa.SPEC_ATTN_E_UNSUPPORTED),            # W > 16 fails loudly
     (dict(head_dim=96), sa.SPEC_ATTN_E_UNSUPPORTED),
-    (dict(page_size=32), sa.SPEC_ATTN_E_UNSUPPORTED),
+    (dict(page_size=48), sa.SPEC_ATTN_E_UNSUPPORTED),
+    (dict(page_size=128), sa.SPEC_ATTN_E_UNSUPPORTED),
+    (dict(window_left=-1), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(window_left=8, mask_mode=1), sa.SPEC_ATTN_E_INVALID_ARG),         # the window is causal-only
+    (dict(kv_page_stride=1024), sa.SPEC_ATTN_E_INVALID_ARG),                # below the dense page (2048 B)
+    (dict(kv_page_stride=2056), sa.SPEC_ATTN_E_INVALID_ARG),                # not a multiple of 16
+    (dict(kv_dtype=1, scale_page_stride=32), sa.SPEC_ATTN_E_INVALID_ARG),   # below 16 keys x 4 scale bytes
+    (dict(kv_dtype=1, kv_page_stride=520), sa.SPEC_ATTN_E_INVALID_ARG),     # codes: dense 512 B, not x16
     (dict(num_q_heads=34, num_kv_heads=2), sa.SPEC_ATTN_E_UNSUPPORTED),  # group 17
     (dict(num_q_heads=6, num_kv_heads=4), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(max_w=0), sa.SPEC_ATTN_E_INVALID_ARG),

@@ -53,10 +53,10 @@ def make_dw(wl, variant=0, **kw):
         raise
 
 
-def run_and_check(wl, variant=0, force_splits=0, trace=True, sel=None, host_lens=True):
+def run_and_check(wl, variant=0, force_splits=0, trace=True, sel=None, host_lens=True, **kw):
     """Untraced run vs the oracle, then (if trace) the traced run: outputs vs the
     oracle again and the index/mask trace bit-exactly."""
-    dw = make_dw(wl, variant, force_splits=force_splits, host_lens=host_lens)
+    dw = make_dw(wl, variant, force_splits=force_splits, host_lens=host_lens, **kw)
     o_ref, lse_ref, tr_ref = oracle.run_workload(wl, row_select=sel, want_trace=trace)
     dw.run()
     torch.cuda.synchronize()
@@ -131,8 +131,11 @@ def test_random_shapes_bf16(shape, variant):
     run_and_check(wl, variant)
 
 
+NVFP4_SHAPES = SHAPES[1:5] + [([150, 63, 1000], [12, 16, 1], 16, 2, 64, 0)]   # d 64 on the tensor cores
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("shape", SHAPES[1:5], ids=[f"s{i}" for i in range(1, 5)])
+@pytest.mark.parametrize("shape", NVFP4_SHAPES, ids=[f"s{i}" for i in range(len(NVFP4_SHAPES))])
 def test_random_shapes_nvfp4(shape, variant):
     ctx, win, hq, hkv, d, mask = shape
     wl = W.make_workload("fp4", ctx, win, hq, hkv, d, mask, kv_dtype=W.KV_NVFP4, seed=3,
@@ -392,7 +395,8 @@ def _row_alone(wl, dw_full, r, i, fixed):
         num_reqs=1, total_q_rows=1, max_w=1, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
         head_dim=wl.head_dim, num_pages=wl.num_pages, block_table_stride=int(wl.block_table.shape[1]),
         max_seq_len=ctx + i + 1, mask_mode=wl.mask_mode, kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale,
-        w_invariant=1, fixed_keys_per_split=fixed)
+        page_size=wl.page_size, w_invariant=1, fixed_keys_per_split=fixed, window_left=wl.window_left,
+        kv_page_stride=dw_full.plan.problem.kv_page_stride, scale_page_stride=dw_full.plan.problem.scale_page_stride)
     q = dw_full.q[row:row + 1].contiguous()
     bt = dw_full.block_table[r:r + 1].contiguous()
     sl = torch.tensor([ctx + i + 1], dtype=torch.int32, device="cuda")

@@ -398,6 +398,9 @@ def test_p1_gbs_is_one_sweep_kv_bytes_over_time():
     # and the workload object's own byte count follows the same definition
     wl = wlmod.make_workload("b", [100], 16, 24, 4, 256, 0, seed=0)
     assert wl.kv_bytes == 116 * 4 * 2 * 512
+    # with a sliding window only the keys some row can see count: the last W + window - 1
+    wl = wlmod.make_workload("bw", [100, 3], [16, 2], 24, 4, 256, 0, seed=0, window_left=10)
+    assert wl.kv_bytes == (25 + 5) * 4 * 2 * 512
 
 
 def test_p2_non_causal_pair_count_and_blowup():
