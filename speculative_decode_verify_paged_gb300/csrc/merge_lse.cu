@@ -56,9 +56,18 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
     const int h = pair % p.num_q_heads;
 
     ReqInfo ri;
-    const bool req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
-                                     p.bt_capacity_keys, p.keys_per_split, nullptr, ri, p.window_left,
-                                     p.split_align);
+    bool req_ok;
+    int first = g;   // the first split of this thread's group
+    if (p.window_left > 0 || p.w_invariant) {
+        req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len, p.bt_capacity_keys,
+                              p.keys_per_split, nullptr, ri, p.window_left, p.split_align);
+        // W-invariant mode: group g takes the splits whose index counted from
+        // key 0 (split0 + s) is g mod SG, whatever the request's first split
+        if (req_ok && p.w_invariant) first = ((g - ri.split0) % sg + sg) % sg;
+    } else {
+        req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len, p.bt_capacity_keys,
+                              p.keys_per_split, nullptr, ri);
+    }
     const bool active = lp < ppc && req_ok && i < ri.w && (ri.nsplits > 1 || p.w_invariant);
     // Wait for the split kernel's partials (no-op without a programmatic edge).
     pdl_wait_primary();
@@ -72,9 +81,6 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
         const size_t pair0 = partial_pair(0, p.total_rows, p.num_q_heads, p.group, h / p.group, ri.row0 + i,
                                           h % p.group);
         const int n = ri.nsplits;
-        // W-invariant mode: group g takes the splits whose index counted from
-        // key 0 (split0 + s) is g mod SG, whatever the request's first split
-        const int first = p.w_invariant ? ((g - ri.split0) % sg + sg) % sg : g;
         for (int s0 = first; s0 < n; s0 += sg * kBatch) {
             float ls[kBatch], sc[kBatch];
             uint4 hv[kBatch];

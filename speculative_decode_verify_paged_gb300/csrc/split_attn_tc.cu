@@ -43,6 +43,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -55,6 +56,13 @@ namespace {
 
 using namespace sm100;
 
+// A 32-bit global load the compiler keeps in program order (not sunk past later loads).
+__device__ __forceinline__ int ld_volatile_i32(const int32_t* p) {
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 constexpr int kBN = 64;        // keys per tile (a multiple of the 16-key page; 32 or 64)
 constexpr int kPPT = kBN / 16;  // pages per tile
 static_assert(kBN == 32 || kBN == 64, "tile");
@@ -65,6 +73,7 @@ constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM cycles
 constexpr long long kDrainLimit = 200000000LL;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units: rescale when max grows by > 2^8
 constexpr int kPageListCap = 64;                 // page ids staged in shared memory at a time (2 per lane)
+constexpr int kNoPrefetch = INT_MIN;             // the producer fetches its first page ids itself
 constexpr int kMaxNR = 8;                        // NVFP4 raw (codes + scales) ring slots
 constexpr int kMaxNK = 8, kMaxNV = 16;
 
@@ -207,10 +216,14 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
         }
         __syncwarp();
     };
-    // the first 64 entries were fetched by the caller
-    if (lane < n_pages) list[lane] = unit(pre0, u_lo + lane);
-    if (lane + 32 < n_pages) list[lane + 32] = unit(pre1, u_lo + lane + 32);
-    __syncwarp();
+    // the first 64 entries were fetched by the caller (unless it could not know where)
+    if (pre0 == kNoPrefetch) {
+        fill_list(0);
+    } else {
+        if (lane < n_pages) list[lane] = unit(pre0, u_lo + lane);
+        if (lane + 32 < n_pages) list[lane + 32] = unit(pre1, u_lo + lane + 32);
+        __syncwarp();
+    }
     int issued = 0;
     for (int t = 0; t < T; ++t) {
         const int slot = t % NSLOT;
@@ -289,10 +302,14 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
         }
         __syncwarp();
     };
-    // the first 64 entries were fetched by the caller
-    if (lane < n_pages) list[lane] = unit(pre0, u_lo + lane);
-    if (lane + 32 < n_pages) list[lane + 32] = unit(pre1, u_lo + lane + 32);
-    __syncwarp();
+    // the first 64 entries were fetched by the caller (unless it could not know where)
+    if (pre0 == kNoPrefetch) {
+        fill_list(0);
+    } else {
+        if (lane < n_pages) list[lane] = unit(pre0, u_lo + lane);
+        if (lane + 32 < n_pages) list[lane + 32] = unit(pre1, u_lo + lane + 32);
+        __syncwarp();
+    }
     int issued = 0;
     for (int t = 0; t < T; ++t) {
         const int slot = t % NR;
@@ -502,18 +519,17 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     // Without a sliding window the split's first block-table entries sit at a
     // fixed place, so the producers fetch them in the same memory round trip
     // as the request's window and length (entries past the request's pages
-    // are never used); with one, the split starts at a key that depends on
-    // the length, so they follow it.
+    // are never used).  The loads are volatile so that they stay ahead of the
+    // request's.  With a window the split starts at a key that depends on the
+    // length: those entries are dropped and the producers fetch their own.
     int key_lo = split * p.keys_per_split;
     int pre0 = -1, pre1 = -1;
-    const bool prefetcher = (warp == 0 || (!KV && warp == 2)) && r < p.num_reqs;
-    auto prefetch = [&]() {
+    if ((warp == 0 || (!KV && warp == 2)) && r < p.num_reqs) {
         const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
         const int u0 = key_lo / 16 + lane;
-        if ((u0 >> p.page_shift) < p.bt_stride) pre0 = bt[u0 >> p.page_shift];
-        if (((u0 + 32) >> p.page_shift) < p.bt_stride) pre1 = bt[(u0 + 32) >> p.page_shift];
-    };
-    if (prefetcher && p.window_left == 0) prefetch();
+        if ((u0 >> p.page_shift) < p.bt_stride) pre0 = ld_volatile_i32(bt + (u0 >> p.page_shift));
+        if (((u0 + 32) >> p.page_shift) < p.bt_stride) pre1 = ld_volatile_i32(bt + ((u0 + 32) >> p.page_shift));
+    }
     ReqInfo ri;
     const bool reporter = (tid == 0 && split == 0 && kvh == 0);
     const bool active = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
@@ -526,7 +542,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     }
     if (p.window_left > 0) {
         key_lo = ri.key_base + split * p.keys_per_split;
-        if (prefetcher) prefetch();
+        pre0 = pre1 = kNoPrefetch;
     }
     const int G = p.group;
     const int R = ri.w * G;  // <= 128: the plan admits this kernel only when max_w * G <= 128
@@ -671,7 +687,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         const int hq = kvh * G + (valid ? m % G : 0);
         const int qrow = ri.row0 + i;
         const int hi = (p.mask_mode == 0) ? (ri.ctx + i) : (ri.len - 1);
-        const int lo = (p.window_left > 0) ? max(0, hi - p.window_left + 1) : 0;   // first visible key
+        const bool has_window = p.window_left > 0;
+        const int lo = has_window ? max(0, hi - p.window_left + 1) : 0;   // first visible key
         const float sc = p.score_scale_log2;
         float m_ref = -INFINITY, l_sum = 0.f;
         long long tr_cnt = 0, tr_sum = 0;
@@ -733,9 +750,17 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             // the scale is folded into one FFMA per exponent.  Tiles whose keys
             // are all visible to every row of the warp skip the mask.
             float mraw = -INFINITY;
-            if (__all_sync(kFullMask, lim >= kBN - 1 && lim_lo <= 0)) {
+            // no row's window starts inside this tile (always so without a window)
+            const bool no_lower = !has_window || __all_sync(kFullMask, lim_lo <= 0);
+            if (no_lower && __all_sync(kFullMask, lim >= kBN - 1)) {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) mraw = fmaxf(mraw, sv[c]);
+            } else if (no_lower) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    if (c > lim) sv[c] = -INFINITY;
+                    mraw = fmaxf(mraw, sv[c]);
+                }
             } else {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
