@@ -748,11 +748,14 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             const int lim_lo = lo - key0;
             // Scores stay unscaled: the maximum is taken on raw scores (sc > 0) and
             // the scale is folded into one FFMA per exponent.  Tiles whose keys
-            // are all visible to every row of the warp skip the mask.
+            // are all visible to every output row of the warp skip the mask.
+            // Padding rows (past W x G) never reach an output; their scores are
+            // finite (zero-filled or another window's rows), so they may run
+            // unmasked, and they never ask for a rescale.
             float mraw = -INFINITY;
             // no row's window starts inside this tile (always so without a window)
             const bool no_lower = !has_window || __all_sync(kFullMask, lim_lo <= 0);
-            if (no_lower && __all_sync(kFullMask, lim >= kBN - 1)) {
+            if (no_lower && __all_sync(kFullMask, !valid || lim >= kBN - 1)) {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) mraw = fmaxf(mraw, sv[c]);
             } else if (no_lower) {
@@ -769,7 +772,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 }
             }
             const float mx = mraw * sc;
-            const bool need = (m_ref != -INFINITY) && (mx > m_ref + kRescaleThreshold);
+            const bool need = valid && (m_ref != -INFINITY) && (mx > m_ref + kRescaleThreshold);
             const bool first = (m_ref == -INFINITY) && (mx != -INFINITY);
             const float ref = (need || first) ? mx : m_ref;
             const float alpha = need ? fast_exp2(m_ref - ref) : 1.f;
