@@ -62,7 +62,7 @@ def _load():
             lib.spec_attn_oracle_run.restype = i32
             lib.spec_attn_oracle_run.argtypes = [
                 i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, f64,
-                vp, vp, vp, vp, vp, f64, f64, vp, i32, vp, vp, vp, vp, vp, vp]
+                vp, vp, vp, vp, vp, f64, f64, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
             lib.oracle_e2m1.restype = f64
             lib.oracle_e2m1.argtypes = [ctypes.c_uint]
             lib.oracle_e4m3.restype = f64
@@ -173,7 +173,7 @@ def num_threads() -> int:
 def run(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, mask_mode, kv_dtype,
         sm_scale, q, k_pool, v_pool, block_table, seq_lens, q_indptr, k_scales=None,
         v_scales=None, k_gscale=1.0, v_gscale=1.0, row_select=None, want_o=True,
-        want_lse=True, want_trace=False, window_left=0):
+        want_lse=True, want_trace=False, window_left=0, block_k=None, block_v=None):
     """Run the oracle.  Arrays may be torch tensors (bf16 is taken bit-wise) or
     numpy arrays.  Returns ``(o, lse, trace)`` as numpy arrays (fp64, fp64,
     int64) or ``None`` for outputs not requested.  ``o`` and ``lse`` rows that
@@ -188,6 +188,8 @@ def run(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, mask_mode,
     btn = _np(block_table, np.int32)
     sln = _np(seq_lens, np.int32)
     qin = _np(q_indptr, np.int32)
+    bkn = _np(block_k, np.uint16)
+    bvn = _np(block_v, np.uint16)
     num_reqs = sln.shape[0]
     bt_stride = btn.shape[1] if btn.ndim == 2 else btn.shape[0]
     sel = None if row_select is None else np.ascontiguousarray(
@@ -198,7 +200,7 @@ def run(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, mask_mode,
     rc = lib.spec_attn_oracle_run(
         num_reqs, total_rows, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
         mask_mode, int(window_left), kv_dtype, float(sm_scale), _ptr(qn), _ptr(kn), _ptr(vn), _ptr(ksn),
-        _ptr(vsn), float(k_gscale), float(v_gscale), _ptr(btn), bt_stride, _ptr(sln),
+        _ptr(vsn), float(k_gscale), float(v_gscale), _ptr(bkn), _ptr(bvn), _ptr(btn), bt_stride, _ptr(sln),
         _ptr(qin), _ptr(sel), _ptr(o), _ptr(lse), _ptr(trace))
     if rc != 0:
         raise ValueError(f"spec_attn_oracle_run failed with code {rc}")
@@ -212,4 +214,5 @@ def run_workload(wl, **kw):
                kv_dtype=wl.kv_dtype, sm_scale=wl.sm_scale, q=wl.q, k_pool=wl.k_pool,
                v_pool=wl.v_pool, block_table=wl.block_table, seq_lens=wl.seq_lens,
                q_indptr=wl.q_indptr, k_scales=wl.k_scales, v_scales=wl.v_scales,
-               k_gscale=wl.k_gscale, v_gscale=wl.v_gscale, window_left=wl.window_left, **kw)
+               k_gscale=wl.k_gscale, v_gscale=wl.v_gscale, window_left=wl.window_left, block_k=wl.block_k,
+               block_v=wl.block_v, **kw)

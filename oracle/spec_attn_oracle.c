@@ -25,6 +25,14 @@
  *                      (same page, section "The cost": the draft layers are
  *                      not causal, each row attends over its request's whole
  *                      span).
+ *   Dense block operand (block_k / block_v non-NULL; bf16 caches): the
+ *   window's own W_r keys are not in the cache but in dense [total_rows, Hkv,
+ *   d] tensors, row by row in q_indptr order (page "DFlash2 leaves the paged
+ *   graph fast path ...", section "Scope": the "Narrow" shape keeps the
+ *   window's K/V apart from the paged context).  Key ctx_r + i is then row
+ *   q_indptr[r] + i of the block tensors; keys below ctx_r come from the
+ *   cache as before, and the block table need only cover them.  In the trace
+ *   a block key counts like any other and adds -(1 + its row) to the slot sum.
  *   Sliding window (window_left > 0; causal only): the same page, same
  *   section, notes that the non-causal draft layers leave an attention window
  *   unapplied, without defining it.  The plainest reading, used here: row i
@@ -132,6 +140,8 @@ unsigned oracle_round_bf16(double x) {
  *             k_scales/v_scales e4m3 bytes [num_pages, Hkv, ps, d/16].
  * mask_mode 0: causal-in-block, 1: non-causal.
  * window_left: 0 (none) or the sliding window of causal rows (keys).
+ * block_k, block_v: NULL, or the dense block operand (bf16 bit patterns
+ *        [total_rows, Hkv, d]; kv_dtype 0 only).
  * row_select: optional [total_rows * Hq] bytes; nonzero = compute that
  *             (row, head).  Unselected outputs are left untouched.
  * o:   [total_rows, Hq, d] fp64 (may be NULL when only the trace is wanted)
@@ -144,6 +154,7 @@ int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_
                          int window_left, int kv_dtype, double sm_scale, const uint16_t* q,
                          const void* k_pool, const void* v_pool, const uint8_t* k_scales,
                          const uint8_t* v_scales, double k_gscale, double v_gscale,
+                         const uint16_t* block_k, const uint16_t* block_v,
                          const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                          const int32_t* q_indptr, const uint8_t* row_select, double* o,
                          double* lse, int64_t* trace) {
@@ -152,6 +163,7 @@ int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_
         return ORACLE_BAD_ARG;
     if (kv_dtype == 1 && head_dim % 16 != 0) return ORACLE_BAD_ARG;
     if (window_left < 0 || (window_left > 0 && mask_mode != 0)) return ORACLE_BAD_ARG;
+    if ((block_k == NULL) != (block_v == NULL) || (block_k && kv_dtype != 0)) return ORACLE_BAD_ARG;
     const int G = num_q_heads / num_kv_heads;
     const int d = head_dim;
     const int Hkv = num_kv_heads;
@@ -179,6 +191,22 @@ int spec_attn_oracle_run(int num_reqs, int total_rows, int num_q_heads, int num_
         int bad_page = 0;
 #pragma omp parallel for schedule(static) reduction(| : bad_page)
         for (int j = 0; j < L; ++j) {
+            if (block_k && j >= ctx) {
+                /* the window's own key: row row0 + (j - ctx) of the block operand */
+                const size_t row = (size_t)row0 + (size_t)(j - ctx);
+                slot_id[j] = -1 - (int64_t)row;
+                for (int kvh = 0; kvh < Hkv; ++kvh) {
+                    double* kd = Kd + ((size_t)j * Hkv + (size_t)kvh) * d;
+                    double* vd = Vd + ((size_t)j * Hkv + (size_t)kvh) * d;
+                    const uint16_t* kb = block_k + (row * Hkv + (size_t)kvh) * d;
+                    const uint16_t* vb = block_v + (row * Hkv + (size_t)kvh) * d;
+                    for (int e = 0; e < d; ++e) {
+                        kd[e] = oracle_bf16(kb[e]);
+                        vd[e] = oracle_bf16(vb[e]);
+                    }
+                }
+                continue;
+            }
             const int page = block_table[(size_t)r * (size_t)bt_stride + (size_t)(j / page_size)];
             const int slot = j % page_size;
             if (page < 0 || page >= num_pages) {

@@ -69,6 +69,8 @@ class Workload:
     k_gscale: float = 1.0
     v_gscale: float = 1.0
     window_left: int = 0          # causal sliding window (keys); 0 = none
+    block_k: Optional[torch.Tensor] = None   # dense block operand [sum W, Hkv, d] bf16: the
+    block_v: Optional[torch.Tensor] = None   # windows' own keys, kept out of the cache
     meta: dict = field(default_factory=dict)
 
     @property
@@ -176,7 +178,8 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
                   peaky_mult: float = 3.0, poison_unread: bool = False,
                   sm_scale: Optional[float] = None, bt_stride: Optional[int] = None,
                   q_mode: str = "randn", v_mode: str = "randn",
-                  nvfp4_gscale: float = NVFP4_GSCALE, window_left: int = 0) -> Workload:
+                  nvfp4_gscale: float = NVFP4_GSCALE, window_left: int = 0,
+                  dense_block: bool = False) -> Workload:
     """Draw one seeded workload.
 
     ``windows`` is one int (same W for every request) or a per-request list.
@@ -184,15 +187,19 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
     request's seq_len in its last page, and pages no request owns) with NaN
     (bf16) or NaN block scales (NVFP4).  ``q_mode``/``v_mode`` 'zero' and
     'const' (V only: a per-(kv head, dim) power of two) produce the closed-form
-    cases.
+    cases.  ``dense_block``: the windows' own keys are drawn as dense
+    ``block_k`` / ``block_v`` [sum W, Hkv, d] bf16 tensors and kept out of the
+    cache, whose pages then cover each request's context only (bf16 pools).
     """
+    assert not (dense_block and kv_dtype != KV_BF16), "the dense block operand is bf16"
     P = len(ctx_lens)
     if isinstance(windows, int):
         windows = [windows] * P
     assert len(windows) == P
     g = torch.Generator(device="cpu").manual_seed(seed)
     seq = [int(c) + int(w) for c, w in zip(ctx_lens, windows)]
-    pages_needed = [math.ceil(s / page_size) for s in seq]
+    cached = [int(c) for c in ctx_lens] if dense_block else seq   # keys the cache holds
+    pages_needed = [math.ceil(s / page_size) for s in cached]
     need = sum(pages_needed)
     if pool_pages is None:
         pool_pages = need + int(math.ceil(need * pool_slack))
@@ -225,8 +232,8 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
         vf[:] = (torch.pow(2.0, expo) * sign)[None, :, None, :]
     if peaky_frac > 0:
         for r in range(P):
-            n = max(1, int(round(peaky_frac * seq[r])))
-            pos = torch.randperm(seq[r], generator=g)[:n]
+            n = max(1, int(round(peaky_frac * cached[r])))
+            pos = torch.randperm(cached[r], generator=g)[:n]
             pg = block_table[r, (pos // ps).long()].long()
             sl = (pos % ps).long()
             kf[pg, :, sl, :] *= peaky_mult
@@ -235,11 +242,14 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
     for r in range(P):
         for p_i in range(pages_needed[r]):
             first = p_i * ps
-            n_valid = min(ps, seq[r] - first)
+            n_valid = min(ps, cached[r] - first)
             owned[int(block_table[r, p_i]), :n_valid] = True
 
     q = qf.to(torch.bfloat16)
     wl_kw = {}
+    if dense_block:
+        wl_kw = dict(block_k=torch.randn(total_rows, Hkv, d, generator=g).to(torch.bfloat16),
+                     block_v=torch.randn(total_rows, Hkv, d, generator=g).to(torch.bfloat16))
     if kv_dtype == KV_BF16:
         k_pool = kf.to(torch.bfloat16)
         v_pool = vf.to(torch.bfloat16)

@@ -414,3 +414,74 @@ def test_p2_non_causal_pair_count_and_blowup():
     fallback_pairs = (ctx + W) ** 2                # every context row attends as well
     blowup = fallback_pairs / pairs
     assert abs(blowup / fx["claimed_blowup"] - 1) < 0.05
+
+
+# --------------------------------------------------------------------------- #
+# Dense block operand: the window's own keys outside the cache
+# --------------------------------------------------------------------------- #
+def _as_block_workload(wl):
+    """The same keys, the window's own rows moved out of the cache into dense
+    block tensors (gathered from the cache by torch indexing), and the cache
+    slots they came from poisoned with NaN."""
+    ind = wl.q_indptr.tolist()
+    bk = torch.zeros(wl.total_rows, wl.num_kv_heads, wl.head_dim, dtype=torch.bfloat16)
+    bv = torch.zeros_like(bk)
+    kp, vp = wl.k_pool.clone(), wl.v_pool.clone()
+    for r in range(wl.num_reqs):
+        W = ind[r + 1] - ind[r]
+        L = int(wl.seq_lens[r])
+        for i in range(W):
+            j = L - W + i
+            page, slot = int(wl.block_table[r, j // wl.page_size]), j % wl.page_size
+            bk[ind[r] + i] = kp[page, :, slot]
+            bv[ind[r] + i] = vp[page, :, slot]
+            kp[page, :, slot] = float("nan")
+            vp[page, :, slot] = float("nan")
+    return wlmod.Workload(**{**wl.__dict__, "k_pool": kp, "v_pool": vp, "block_k": bk, "block_v": bv})
+
+
+@pytest.mark.parametrize("mask", [wlmod.MASK_CAUSAL_IN_BLOCK, wlmod.MASK_NON_CAUSAL])
+def test_block_operand_equals_the_cache_holding_the_same_rows(mask):
+    """Moving the window's keys out of the cache into the block operand changes
+    nothing but the trace's slot ids: outputs bit for bit, key counts exactly,
+    and the NaN left in the vacated slots is never read."""
+    wl = wlmod.make_workload("blk", [40, 0, 17], [5, 3, 16], 4, 2, 16, mask, seed=31, pool_slack=0.3)
+    blk = _as_block_workload(wl)
+    o0, l0, t0 = oracle.run_workload(wl, want_trace=True)
+    o1, l1, t1 = oracle.run_workload(blk, want_trace=True)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    assert np.array_equal(t0[..., 0], t1[..., 0])
+    # slot sums: the window's keys now count -(1 + row) instead of their slot id
+    ind = wl.q_indptr.tolist()
+    bt = wl.block_table.tolist()
+    for r in range(wl.num_reqs):
+        W = ind[r + 1] - ind[r]
+        L = int(wl.seq_lens[r])
+        for i in range(W):
+            hi = (L - W + i) if mask == wlmod.MASK_CAUSAL_IN_BLOCK else L - 1
+            want = sum(bt[r][j // 16] * 16 + j % 16 if j < L - W else -1 - (ind[r] + j - (L - W))
+                       for j in range(hi + 1))
+            assert (t1[ind[r] + i, :, 1] == want).all()
+
+
+def test_block_operand_equals_sdpa_on_concatenated_keys():
+    wl = wlmod.make_workload("blks", [33, 70], [4, 9], 4, 2, 16, wlmod.MASK_NON_CAUSAL, seed=32,
+                             pool_slack=0.3, dense_block=True, poison_unread=True)
+    o, lse, _ = oracle.run_workload(wl)
+    G = 2
+    ind = wl.q_indptr.tolist()
+    for r in range(wl.num_reqs):
+        W = ind[r + 1] - ind[r]
+        ctx = int(wl.seq_lens[r]) - W
+        j = torch.arange(ctx)
+        pages = wl.block_table[r, (j // 16)].long()
+        for h in range(4):
+            kvh = h // G
+            k = torch.cat([wl.k_pool[pages, kvh, (j % 16).long()], wl.block_k[ind[r]:ind[r + 1], kvh]]).double()
+            v = torch.cat([wl.v_pool[pages, kvh, (j % 16).long()], wl.block_v[ind[r]:ind[r + 1], kvh]]).double()
+            q = wl.q[ind[r]:ind[r + 1], h].double()
+            ref = torch.nn.functional.scaled_dot_product_attention(q[None, None], k[None, None], v[None, None],
+                                                                   scale=wl.sm_scale)[0, 0]
+            ref_lse = torch.logsumexp((q @ k.T) * wl.sm_scale, 1)
+            np.testing.assert_allclose(o[ind[r]:ind[r + 1], h], ref.numpy(), rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(lse[ind[r]:ind[r + 1], h], ref_lse.numpy(), rtol=1e-12)
