@@ -152,7 +152,8 @@ def table_workloads():
             ("nvfp4_append_only", W.nvfp4, {"append": "append"}),
             ("verify_w16_ctx16k_pages64", lambda: W.verify_sweep(16, page_size=64, pool_pages=512)),
             ("verify_w16_ctx16k_interleaved_kv", lambda: W.verify_sweep(16), {"interleave": True}),
-            ("long_verify_w16_window4096", lambda: W.long_verify(16, window_left=4096))]
+            ("long_verify_w16_window4096", lambda: W.long_verify(16, window_left=4096)),
+            ("batched_draft_dense_block", lambda: W.batched_draft(dense_block=True))]
 
 
 def run_reference(args, rank, world):

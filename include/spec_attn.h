@@ -153,6 +153,9 @@ typedef struct spec_attn_problem {
                                     and at least the dense size */
     int64_t scale_page_stride;   /* NVFP4 scale pools, likewise (dense: Hkv * page_size
                                     * head_dim/16 bytes); ignored for bf16 */
+    int32_t dense_block_kv;      /* 1: the window's own keys come from dense block
+                                    tensors (spec_attn_run_dense_block), not the cache;
+                                    bf16 caches only, not with w_invariant */
 } spec_attn_problem;
 
 /*
@@ -248,6 +251,27 @@ int spec_attn_run_traced(const spec_attn_plan* plan, const void* q, const void* 
                          const int32_t* seq_lens, const int32_t* q_indptr, void* o,
                          float* lse, int64_t* trace, void* workspace,
                          size_t workspace_bytes, spec_attn_stream_t stream);
+
+/*
+ * Dense block operand (dense_block_kv = 1).  The window's own W_r keys are
+ * not in the cache: they come from dense tensors block_k, block_v
+ * [total_q_rows, Hkv, head_dim] bf16 (16-byte aligned), row q_indptr[r] + i
+ * holding key ctx_r + i = seq_len[r] - W_r + i.  The cache holds the context
+ * keys 0 .. ctx_r - 1 only, and the block table need cover just those.  This
+ * is the "Narrow" shape of the page "DFlash2 leaves the paged graph fast path
+ * at every c>1 and re-attends the whole batch context every decode step"
+ * (section "Scope"): the draft's block K/V are discarded after the step, so
+ * they are kept apart from the paged context.  Masks, window and outputs are
+ * as for spec_attn_run, over the keys 0 .. seq_len[r] - 1 so formed.  trace
+ * (nullable, as spec_attn_run_traced) counts a block key with slot id
+ * -(1 + its row).  A plan made with dense_block_kv = 1 runs only here, and
+ * this entry point needs such a plan (else SPEC_ATTN_E_INVALID_ARG).
+ */
+int spec_attn_run_dense_block(const spec_attn_plan* plan, const void* q, const void* block_k,
+                              const void* block_v, const void* k_pool, const void* v_pool,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              const int32_t* q_indptr, void* o, float* lse, int64_t* trace,
+                              void* workspace, size_t workspace_bytes, spec_attn_stream_t stream);
 
 /*
  * KV append: write the window's new key and value rows into their cache slots

@@ -49,7 +49,7 @@ EXPORTED_SYMBOLS = (
     "spec_attn_run", "spec_attn_run_traced", "spec_attn_plan_set_timing_events",
     "spec_attn_reset_device_status", "spec_attn_check_device_status",
     "spec_attn_status_string", "spec_attn_last_cuda_error", "spec_attn_version",
-    "spec_attn_run_noalloc", "spec_attn_append_kv", "spec_attn_run_append",
+    "spec_attn_run_noalloc", "spec_attn_append_kv", "spec_attn_run_append", "spec_attn_run_dense_block",
 )
 
 
@@ -69,7 +69,7 @@ class spec_attn_problem(ctypes.Structure):
         ("force_splits", ctypes.c_int32), ("kernel_variant", ctypes.c_int32),
         ("w_invariant", ctypes.c_int32), ("fixed_keys_per_split", ctypes.c_int32),
         ("window_left", ctypes.c_int32), ("kv_page_stride", ctypes.c_int64),
-        ("scale_page_stride", ctypes.c_int64),
+        ("scale_page_stride", ctypes.c_int64), ("dense_block_kv", ctypes.c_int32),
     ]
 
 
@@ -132,6 +132,8 @@ def load_library(path: Optional[str] = None):
         lib.spec_attn_append_kv.argtypes = [vp, vp, vp] + cache_args + [vp, sz, vp]
         lib.spec_attn_run_append.restype = i32
         lib.spec_attn_run_append.argtypes = [vp, vp, vp, vp] + cache_args + [vp, vp, vp, sz, vp]
+        lib.spec_attn_run_dense_block.restype = i32
+        lib.spec_attn_run_dense_block.argtypes = [vp] * 13 + [sz, vp]
         if path is None:
             _lib = lib
         return lib
@@ -212,13 +214,13 @@ def spec_attn_plan_create(*, num_reqs, total_q_rows, max_w, num_q_heads, num_kv_
                           num_pages, block_table_stride, max_seq_len, mask_mode=0, kv_dtype=0,
                           page_size=16, sm_scale=0.0, force_splits=0, kernel_variant=0,
                           seq_lens=None, q_indptr=None, w_invariant=0, fixed_keys_per_split=0,
-                          window_left=0, kv_page_stride=0, scale_page_stride=0) -> Plan:
+                          window_left=0, kv_page_stride=0, scale_page_stride=0, dense_block_kv=0) -> Plan:
     lib = load_library()
     prob = spec_attn_problem(num_reqs, total_q_rows, max_w, num_q_heads, num_kv_heads, head_dim,
                              page_size, num_pages, block_table_stride, mask_mode, kv_dtype,
                              float(sm_scale), int(max_seq_len), force_splits, kernel_variant,
                              int(w_invariant), int(fixed_keys_per_split), int(window_left),
-                             int(kv_page_stride), int(scale_page_stride))
+                             int(kv_page_stride), int(scale_page_stride), int(dense_block_kv))
     sl, _k1 = _host_i32(seq_lens)
     qi, _k2 = _host_i32(q_indptr)
     handle = ctypes.c_void_p()
@@ -325,6 +327,24 @@ def spec_attn_run_append(plan: Plan, q, k_new, v_new, k_pool, v_pool, block_tabl
                                     _stream_handle(stream)), "spec_attn_run_append")
 
 
+def spec_attn_run_dense_block(plan: Plan, q, block_k, block_v, k_pool, v_pool, block_table, seq_lens, q_indptr,
+                              o, lse, workspace, trace=None, stream=None):
+    """Attention with the window's own keys from dense block tensors
+    ([total_rows, Hkv, d] bf16) and the context from the cache (asynchronous)."""
+    import torch
+    lib = load_library()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dense = plan.problem.kv_page_stride == 0
+    _check(lib.spec_attn_run_dense_block(
+        plan.handle, _dptr(q, "q", torch.bfloat16), _dptr(block_k, "block_k", torch.bfloat16),
+        _dptr(block_v, "block_v", torch.bfloat16), _dptr(k_pool, "k_pool", torch.bfloat16, dense),
+        _dptr(v_pool, "v_pool", torch.bfloat16, dense), _dptr(block_table, "block_table", torch.int32),
+        _dptr(seq_lens, "seq_lens", torch.int32), _dptr(q_indptr, "q_indptr", torch.int32),
+        _dptr(o, "o", torch.bfloat16), _dptr(lse, "lse", torch.float32), _dptr(trace, "trace", torch.int64),
+        _dptr(workspace, "workspace"), ctypes.c_size_t(ws_bytes), _stream_handle(stream)),
+        "spec_attn_run_dense_block")
+
+
 def spec_attn_reset_device_status(workspace, stream=None):
     _check(load_library().spec_attn_reset_device_status(_dptr(workspace, "workspace"),
                                                         _stream_handle(stream)),
@@ -401,8 +421,10 @@ class DeviceWorkload:
             kernel_variant=kernel_variant, seq_lens=wl.seq_lens if host_lens else None,
             q_indptr=wl.q_indptr if host_lens else None, w_invariant=w_invariant,
             fixed_keys_per_split=fixed_keys_per_split, window_left=wl.window_left, kv_page_stride=kv_stride,
-            scale_page_stride=sc_stride)
+            scale_page_stride=sc_stride, dense_block_kv=int(wl.block_k is not None))
         self.workspace = torch.zeros(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device=dev)
+        self.block_k = None if wl.block_k is None else wl.block_k.to(dev)
+        self.block_v = None if wl.block_v is None else wl.block_v.to(dev)
         self.k_new = self.v_new = None
         if append_rows is not None:
             self.k_new = append_rows[0].to(dev).contiguous()
@@ -417,12 +439,21 @@ class DeviceWorkload:
             spec_attn_run_append(self.plan, self.q, self.k_new, self.v_new, self.k_pool, self.v_pool,
                                  self.block_table, self.seq_lens, self.q_indptr, self.o, self.lse, self.workspace,
                                  self.k_scales, self.v_scales, self.wl.k_gscale, self.wl.v_gscale, stream)
+        elif self.block_k is not None:
+            spec_attn_run_dense_block(self.plan, self.q, self.block_k, self.block_v, self.k_pool, self.v_pool,
+                                      self.block_table, self.seq_lens, self.q_indptr, self.o, self.lse,
+                                      self.workspace, stream=stream)
         else:
             spec_attn_run(self.plan, self.q, self.k_pool, self.v_pool, self.block_table, self.seq_lens,
                           self.q_indptr, self.o, self.lse, self.workspace, self.k_scales, self.v_scales,
                           self.wl.k_gscale, self.wl.v_gscale, stream)
 
     def run_traced(self, trace, stream=None):
+        if self.block_k is not None:
+            spec_attn_run_dense_block(self.plan, self.q, self.block_k, self.block_v, self.k_pool, self.v_pool,
+                                      self.block_table, self.seq_lens, self.q_indptr, self.o, self.lse,
+                                      self.workspace, trace=trace, stream=stream)
+            return
         spec_attn_run_traced(self.plan, self.q, self.k_pool, self.v_pool, self.block_table,
                              self.seq_lens, self.q_indptr, self.o, self.lse, trace, self.workspace,
                              self.k_scales, self.v_scales, self.wl.k_gscale, self.wl.v_gscale, stream)

@@ -71,24 +71,28 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
 // A request's window and cache, validated against the plan.  Invalid
 // requests set a status bit (when status != nullptr) and are skipped.
 struct ReqInfo {
-    int row0;      // first Q/O row
-    int w;         // window rows
-    int len;       // seq_len (keys in cache incl. the window's)
-    int ctx;       // len - w
-    int key_base;  // first key any row may see, rounded down to the split alignment
-    int nsplits;   // splits of keys_per_split covering [key_base, len)
-    int split0;    // key_base / keys_per_split (whole when the alignment is keys_per_split)
+    int row0;       // first Q/O row
+    int w;          // window rows
+    int len;        // seq_len (keys incl. the window's)
+    int ctx;        // len - w
+    int cache_len;  // keys read from the cache: len, or ctx with the dense block operand
+    int key_base;   // first key any row may see, rounded down to the split alignment
+    int nsplits;    // splits of keys_per_split covering [key_base, cache_len) (at least one)
+    int split0;     // key_base / keys_per_split (whole when the alignment is keys_per_split)
 };
 
 // window_left > 0: a causal sliding window; no row sees a key below
 // ctx - window_left + 1 (row 0's bound), so the splits start at that key
 // rounded down to split_align (64, the key tile; or keys_per_split where
-// split boundaries must sit at fixed key positions).
+// split boundaries must sit at fixed key positions).  dense_block: the
+// window's own keys come from the dense block operand; the splits cover the
+// cache keys [key_base, ctx) and the last one also takes the window's keys.
 __device__ __forceinline__ bool load_request(const int32_t* seq_lens, const int32_t* q_indptr,
                                              int r, int max_w, int total_rows,
                                              long long max_seq_len, int cap_keys,
                                              int keys_per_split, unsigned int* status,
-                                             ReqInfo& ri, int window_left = 0, int split_align = 64) {
+                                             ReqInfo& ri, int window_left = 0, int split_align = 64,
+                                             int dense_block = 0) {
     // three independent loads: one memory round trip
     const int row0 = q_indptr[r];
     const int row1 = q_indptr[r + 1];
@@ -99,7 +103,8 @@ __device__ __forceinline__ bool load_request(const int32_t* seq_lens, const int3
         return false;
     }
     if (w == 0) return false;
-    if (len < w || (long long)len > max_seq_len || len > cap_keys) {
+    const int cache_len = dense_block ? len - w : len;
+    if (len < w || (long long)len > max_seq_len || cache_len > cap_keys) {
         if (status) atomicOr(status, kDevBadSeqLen);
         return false;
     }
@@ -107,6 +112,7 @@ __device__ __forceinline__ bool load_request(const int32_t* seq_lens, const int3
     ri.w = w;
     ri.len = len;
     ri.ctx = len - w;
+    ri.cache_len = cache_len;
     ri.key_base = 0;
     ri.split0 = 0;
     if (window_left > 0) {
@@ -114,7 +120,7 @@ __device__ __forceinline__ bool load_request(const int32_t* seq_lens, const int3
         ri.key_base = lo0 / split_align * split_align;
         ri.split0 = ri.key_base / keys_per_split;
     }
-    ri.nsplits = (len - ri.key_base + keys_per_split - 1) / keys_per_split;
+    ri.nsplits = max(1, (cache_len - ri.key_base + keys_per_split - 1) / keys_per_split);
     return true;
 }
 

@@ -58,9 +58,9 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
     ReqInfo ri;
     bool req_ok;
     int first = g;   // the first split of this thread's group
-    if (p.window_left > 0 || p.w_invariant) {
+    if (p.window_left > 0 || p.w_invariant || p.dense_block) {
         req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len, p.bt_capacity_keys,
-                              p.keys_per_split, nullptr, ri, p.window_left, p.split_align);
+                              p.keys_per_split, nullptr, ri, p.window_left, p.split_align, p.dense_block);
         // W-invariant mode: group g takes the splits whose index counted from
         // key 0 (split0 + s) is g mod SG, whatever the request's first split
         if (req_ok && p.w_invariant) first = ((g - ri.split0) % sg + sg) % sg;

@@ -121,6 +121,9 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
         p->block_table_stride < 0 || p->num_pages < 0 || p->force_splits < 0)
         return SPEC_ATTN_E_INVALID_ARG;
     if (p->w_invariant != 0 && p->w_invariant != 1) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->dense_block_kv != 0 && p->dense_block_kv != 1) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->dense_block_kv && p->w_invariant) return SPEC_ATTN_E_INVALID_ARG;   // exactness is a cache-only rule
+    if (p->dense_block_kv && p->kv_dtype != SPEC_ATTN_KV_BF16) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->w_invariant && (p->fixed_keys_per_split < 0 || p->fixed_keys_per_split % 64 != 0))
         return SPEC_ATTN_E_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return SPEC_ATTN_E_INVALID_ARG;
@@ -152,8 +155,11 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
     if (p->num_kv_heads > 65535 || p->num_reqs > 65535) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->num_reqs > 0) {
         if (p->max_seq_len < 1 || p->num_pages < 1) return SPEC_ATTN_E_INVALID_ARG;
+        // the cache holds every key (with the dense block operand only the
+        // context: checked per request below when the host lengths are given,
+        // and on the device always)
         const int64_t need_pages = (p->max_seq_len + p->page_size - 1) / p->page_size;
-        if (p->block_table_stride < need_pages) return SPEC_ATTN_E_INVALID_ARG;
+        if (!p->dense_block_kv && p->block_table_stride < need_pages) return SPEC_ATTN_E_INVALID_ARG;
     }
     if (h_q_indptr) {
         if (h_q_indptr[0] != 0) return SPEC_ATTN_E_INVALID_ARG;
@@ -169,6 +175,10 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
         for (int r = 0; r < p->num_reqs; ++r) {
             if (h_seq_lens[r] < 0 || h_seq_lens[r] > p->max_seq_len) return SPEC_ATTN_E_INVALID_ARG;
             if (h_q_indptr && h_seq_lens[r] < h_q_indptr[r + 1] - h_q_indptr[r]) return SPEC_ATTN_E_INVALID_ARG;
+            if (h_q_indptr && p->dense_block_kv &&
+                h_seq_lens[r] - (h_q_indptr[r + 1] - h_q_indptr[r]) >
+                    static_cast<int64_t>(p->block_table_stride) * p->page_size)
+                return SPEC_ATTN_E_INVALID_ARG;
         }
     }
     return SPEC_ATTN_OK;
@@ -269,10 +279,13 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     // heuristic weighs are those spans.
     const int fixed_kps = p.fixed_keys_per_split > 0 ? p.fixed_keys_per_split : 512;
     plan->split_align = plan->w_invariant ? fixed_kps : kSplitUnit;
+    // (dense block operand: the splits cover the cached context; the window's
+    // own keys ride along in the last one)
     auto span = [&](int64_t len, int64_t w) {
-        if (p.window_left <= 0) return len;
+        const int64_t cached = p.dense_block_kv ? len - w : len;
+        if (p.window_left <= 0) return cached;
         const int64_t lo0 = std::max<int64_t>(0, len - w - p.window_left + 1);
-        return len - lo0 / plan->split_align * plan->split_align;
+        return cached - lo0 / plan->split_align * plan->split_align;
     };
     std::vector<int64_t> lens;
     lens.reserve(static_cast<size_t>(p.num_reqs));
@@ -468,9 +481,14 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
                     const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
                     const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
                     void* o, float* lse, int64_t* trace, void* workspace, size_t workspace_bytes,
-                    spec_attn_stream_t stream_handle) {
+                    spec_attn_stream_t stream_handle, const void* block_k = nullptr,
+                    const void* block_v = nullptr) {
     if (!plan) return SPEC_ATTN_E_INVALID_ARG;
     const spec_attn_problem& p = plan->prob;
+    // a dense-block plan runs only with its block tensors, and they need such a plan
+    if ((p.dense_block_kv != 0) != (block_k != nullptr) || (block_k == nullptr) != (block_v == nullptr))
+        return SPEC_ATTN_E_INVALID_ARG;
+    if (block_k && (!aligned(block_k, 16) || !aligned(block_v, 16))) return SPEC_ATTN_E_INVALID_ARG;
     if (p.num_reqs == 0 || p.total_q_rows == 0) return SPEC_ATTN_OK;
     const int chk = check_run_args(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
                                    seq_lens, q_indptr, o, lse, trace, workspace, workspace_bytes);
@@ -521,13 +539,19 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.scale_page_stride = plan->scale_page_stride;
     sp.window_left = p.window_left;
     sp.split_align = plan->split_align;
+    sp.dense_block = p.dense_block_kv;
+    sp.block_k = static_cast<const uint16_t*>(block_k);
+    sp.block_v = static_cast<const uint16_t*>(block_v);
 
     spec_attn_plan* mp = const_cast<spec_attn_plan*>(plan);
     std::unique_lock<std::mutex> maps_lock(mp->maps_mutex, std::defer_lock);
     if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
         maps_lock.lock();
+        // (dense block operand: the block tensors take the scale pools' places)
+        const void* key3 = p.dense_block_kv ? block_k : k_scales;
+        const void* key4 = p.dense_block_kv ? block_v : v_scales;
         if (mp->maps_key[0] != q || mp->maps_key[1] != k_pool || mp->maps_key[2] != v_pool ||
-            mp->maps_key[3] != k_scales || mp->maps_key[4] != v_scales) {
+            mp->maps_key[3] != key3 || mp->maps_key[4] != key4) {
             if (!tc_encode_maps(sp, p.kv_dtype, &mp->maps)) {
                 for (auto& k : mp->maps_key) k = nullptr;
                 return SPEC_ATTN_E_INVALID_ARG;
@@ -535,8 +559,8 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
             mp->maps_key[0] = q;
             mp->maps_key[1] = k_pool;
             mp->maps_key[2] = v_pool;
-            mp->maps_key[3] = k_scales;
-            mp->maps_key[4] = v_scales;
+            mp->maps_key[3] = key3;
+            mp->maps_key[4] = key4;
         }
     }
     if (plan->ev_begin) {
@@ -575,6 +599,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         mp.w_invariant = plan->w_invariant ? 1 : 0;
         mp.window_left = p.window_left;
         mp.split_align = plan->split_align;
+        mp.dense_block = p.dense_block_kv;
         // programmatic launch lets the merge's CTAs become resident while the
         // split kernel drains; it is skipped when a timing event sits between.
         e = merge_launch(mp, stream, plan->ev_end == nullptr);
@@ -592,11 +617,22 @@ int spec_attn_run(const spec_attn_plan* plan, const void* q, const void* k_pool,
                     seq_lens, q_indptr, o, lse, nullptr, workspace, workspace_bytes, stream);
 }
 
+int spec_attn_run_dense_block(const spec_attn_plan* plan, const void* q, const void* block_k,
+                              const void* block_v, const void* k_pool, const void* v_pool,
+                              const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
+                              void* o, float* lse, int64_t* trace, void* workspace, size_t workspace_bytes,
+                              spec_attn_stream_t stream) {
+    if (!plan || !plan->prob.dense_block_kv || !block_k || !block_v) return SPEC_ATTN_E_INVALID_ARG;
+    return run_impl(plan, q, k_pool, v_pool, nullptr, nullptr, 1.0f, 1.0f, block_table, seq_lens, q_indptr, o,
+                    lse, trace, workspace, workspace_bytes, stream, block_k, block_v);
+}
+
 int spec_attn_append_kv(const spec_attn_plan* plan, const void* k_new, const void* v_new, void* k_pool,
                         void* v_pool, void* k_scales, void* v_scales, float k_gscale, float v_gscale,
                         const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
                         void* workspace, size_t workspace_bytes, spec_attn_stream_t stream) {
-    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    // (a dense-block plan keeps the window's keys out of the cache: nothing to append)
+    if (!plan || plan->prob.dense_block_kv) return SPEC_ATTN_E_INVALID_ARG;
     const spec_attn_problem& p = plan->prob;
     if (p.num_reqs == 0 || p.total_q_rows == 0) return SPEC_ATTN_OK;
     const int chk = check_append_args(plan, k_new, v_new, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
@@ -611,7 +647,7 @@ int spec_attn_run_append(const spec_attn_plan* plan, const void* q, const void* 
                          float v_gscale, const int32_t* block_table, const int32_t* seq_lens,
                          const int32_t* q_indptr, void* o, float* lse, void* workspace, size_t workspace_bytes,
                          spec_attn_stream_t stream) {
-    if (!plan) return SPEC_ATTN_E_INVALID_ARG;
+    if (!plan || plan->prob.dense_block_kv) return SPEC_ATTN_E_INVALID_ARG;
     const spec_attn_problem& p = plan->prob;
     if (p.num_reqs == 0 || p.total_q_rows == 0) return SPEC_ATTN_OK;
     // every check before the first launch: a rejected call changes nothing

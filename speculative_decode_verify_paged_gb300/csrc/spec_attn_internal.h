@@ -48,6 +48,9 @@ struct SplitParams {
     long long scale_page_stride;// bytes between pages of a scale pool (NVFP4)
     int window_left;            // causal sliding window (keys), 0 = none
     int split_align;            // first split of a request starts at a multiple of this (keys)
+    int dense_block;            // the window's keys come from block_k / block_v (bf16 caches)
+    const uint16_t* block_k;    // [total_rows, Hkv, d] bf16 bits, or nullptr
+    const uint16_t* block_v;
 };
 
 struct MergeParams {
@@ -70,6 +73,7 @@ struct MergeParams {
     int w_invariant;            // merge every request (one split too), splits folded in order
     int window_left;            // as SplitParams
     int split_align;
+    int dense_block;
 };
 
 // Everything one KV-append launch needs (append_kv.cu).
@@ -138,7 +142,8 @@ cudaError_t cc_launch(const SplitParams& p, int kv_dtype, const CcConfig& cfg, b
 
 // ---- tcgen05 split-KV kernel (split_attn_tc.cu) ----
 // TMA descriptors of one (Q, K pool, V pool) triple; opaque CUtensorMap storage.
-// bf16 KV: K and V pools; NVFP4: K and V code pools, plus their scale pools.
+// bf16 KV: K and V pools, and (dense block operand) the block K and V tensors
+// in the ks / vs slots; NVFP4: K and V code pools, plus their scale pools.
 struct TcMaps {
     alignas(64) unsigned char q[128];
     alignas(64) unsigned char k[128];

@@ -155,7 +155,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
     const bool reporter = (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0);
     if (!load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
                       p.bt_stride << (4 + p.page_shift), p.keys_per_split, reporter ? p.status : nullptr, ri,
-                      p.window_left, p.split_align))
+                      p.window_left, p.split_align, p.dense_block))
         return;
     if (split >= ri.nsplits) return;
     const int G = p.group;
@@ -164,11 +164,15 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
     if (row_lo >= R) return;
 
     const int key_lo = ri.key_base + split * p.keys_per_split;
-    const int key_hi = min(key_lo + p.keys_per_split, ri.len);
+    const int key_hi = min(key_lo + p.keys_per_split, ri.cache_len);
     // the loop runs over 16-key units: unit u is slots (u & sub_mask) * 16 .. +15
-    // of page block_table[r][u >> page_shift]
+    // of page block_table[r][u >> page_shift]; with the dense block operand the
+    // request's last split ends with one more unit, rows row0 .. row0 + W - 1 of
+    // block_k / block_v (keys ctx .. len - 1)
     const int page_first = key_lo / kUnit;
-    const int npages = (key_hi - 1) / kUnit - page_first + 1;
+    const int npages = key_hi > key_lo ? (key_hi - 1) / kUnit - page_first + 1 : 0;
+    const bool has_block = p.dense_block && split == ri.nsplits - 1;
+    const int nunits = npages + (has_block ? 1 : 0);
     const int32_t* bt_row = p.block_table + (size_t)r * p.bt_stride;
     const int page_keys = kUnit << p.page_shift;
     const int sub_mask = (1 << p.page_shift) - 1;
@@ -231,18 +235,38 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
                     cp_async16(st + Stage::kHalf + Stage::kCodeBytes + c * 16, vss + c * 16);
                 }
             }
+        } else if (KV == 0 && pi == npages && has_block) {   // (bf16 caches only)
+            // the window's own rows (bf16): row j of the unit is block row row0 + j;
+            // rows past W are zeros (never read from another window)
+            unsigned char* st = smem + (size_t)(pi % stages) * Stage::kBytes;
+            constexpr int kRowPieces = D * 2 / 16;
+            for (int c = tid; c < kUnit * kRowPieces; c += kThreads) {
+                const int j = c / kRowPieces, piece = c % kRowPieces;
+                unsigned char* kd = st + j * (D * 2) + piece * 16;
+                unsigned char* vd = st + Stage::kHalf + j * (D * 2) + piece * 16;
+                if (j < ri.w) {
+                    const size_t off = (((size_t)(ri.row0 + j) * p.num_kv_heads + kvh) * D) * 2 + piece * 16;
+                    cp_async16(kd, reinterpret_cast<const unsigned char*>(p.block_k) + off);
+                    cp_async16(vd, reinterpret_cast<const unsigned char*>(p.block_v) + off);
+                } else {
+                    *reinterpret_cast<uint4*>(kd) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(vd) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
         }
         cp_async_commit();
     };
 
     for (int pi = 0; pi < stages - 1; ++pi) issue_page(pi);
 
-    for (int pi = 0; pi < npages; ++pi) {
+    for (int pi = 0; pi < nunits; ++pi) {
         issue_page(pi + stages - 1);
         cp_async_wait_dyn(stages - 1);
         __syncthreads();
         const unsigned char* st = smem + (size_t)(pi % stages) * Stage::kBytes;
-        const int kbase = (page_first + pi) * kUnit;
+        const bool blk = pi == npages;   // the dense block unit
+        const int kbase = blk ? ri.ctx : (page_first + pi) * kUnit;
+        const int kend = blk ? ri.len : key_hi;
         if (any_valid) {
             // scores for the 16 keys of this page
             float part[RPW][16];
@@ -263,7 +287,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
 #pragma unroll
             for (int t = 0; t < RPW; ++t) {
                 const float sc = transpose_reduce16(part[t], lane);
-                const bool vis = (key < key_hi) && (key <= hi_key[t]) && (key >= lo_key[t]);
+                const bool vis = (key < kend) && (key <= hi_key[t]) && (key >= lo_key[t]);
                 float mx = vis ? sc : -INFINITY;
 #pragma unroll
                 for (int off = 2; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
@@ -280,10 +304,14 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
                 pj[t] = pv;
                 if constexpr (TRACE) {
                     if (vis && (lane & 1) == 0) {
-                        int phys = bt_row[(page_first + pi) >> p.page_shift];
-                        if (phys < 0 || phys >= p.num_pages) phys = 0;
                         tr_cnt[t] += 1;
-                        tr_sum[t] += (long long)phys * page_keys + (key & (page_keys - 1));
+                        if (blk) {   // a dense block key has no cache slot: -(1 + its row)
+                            tr_sum[t] += -1 - (long long)(ri.row0 + key - ri.ctx);
+                        } else {
+                            int phys = bt_row[(page_first + pi) >> p.page_shift];
+                            if (phys < 0 || phys >= p.num_pages) phys = 0;
+                            tr_sum[t] += (long long)phys * page_keys + (key & (page_keys - 1));
+                        }
                     }
                 }
             }
@@ -294,7 +322,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
                 load_row_slice<D, KV>(st + Stage::kHalf, j, lane, vx);
                 // Slots past seq_len hold stale data (possibly non-finite);
                 // their weight is 0, but 0 * NaN is NaN, so drop the values.
-                if (kbase + j >= key_hi) {
+                if (kbase + j >= kend) {
 #pragma unroll
                     for (int e = 0; e < DPL; ++e) vx[e] = 0.f;
                 }

@@ -190,11 +190,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // One producer warp streams one of K or V: block-table entries are fetched by
 // all 32 lanes at once (coalesced) into a shared-memory list, then lane 0
 // issues one 2 KB TMA box per (page, 64 head_dim elements) into the ring slot.
+// With the dense block operand, tile Tc (the last of the request's last
+// split) holds the window's own keys: one 16-key unit of rows row0 .. row0 + 15
+// of the block tensor (tm_block), laid out like a page unit.
 template <int D, int NSLOT, bool IS_V, bool TRACE>
 __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
                                        unsigned char* ring, uint64_t* full, uint64_t* empty, int32_t* list,
                                        TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane,
-                                       int pre0, int pre1) {
+                                       int pre0, int pre1, int Tc, int row0, const CUtensorMap* tm_block) {
     using L = TcLayout<D, 0>;
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
     const int u_lo = key_lo / 16;                    // first 16-key unit of the split
@@ -228,6 +231,19 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
     for (int t = 0; t < T; ++t) {
         const int slot = t % NSLOT;
         if (t >= NSLOT && !warp_wait(&empty[slot], ((t / NSLOT) - 1) & 1, abort)) break;
+        unsigned char* dst = ring + slot * L::kTileBytes;
+        if (t >= Tc) {   // the dense block unit
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(L::kChunks * 2048));
+            __syncwarp();
+            if (IS_V) {
+                if (lane == 0) tma_load_4d(dst, tm_block, 0, row0, 0, kvh, &full[slot]);
+            } else if (lane < L::kChunks) {
+                tma_load_3d(dst + lane * (kBN * 128), tm_block, lane * 64, row0, kvh, &full[slot]);
+            }
+            __syncwarp();
+            issued = t + 1;
+            continue;
+        }
         const int rel = t * kPPT;  // first page of the tile, relative to the split
         if (rel >= list_base + kPageListCap) {
             __syncwarp();
@@ -238,7 +254,6 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
         // issue takes a while; one lane issuing them all in turn would add
         // that time to every tile's latency).
         const int np = min(kPPT, (key_hi - (key_lo + t * kBN) + 15) / 16);
-        unsigned char* dst = ring + slot * L::kTileBytes;
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(np * L::kChunks * 2048));
         __syncwarp();
         if (IS_V) {
@@ -534,7 +549,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     const bool reporter = (tid == 0 && split == 0 && kvh == 0);
     const bool active = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
                                      p.bt_stride << (4 + p.page_shift), p.keys_per_split,
-                                     reporter ? p.status : nullptr, ri, p.window_left, p.split_align) &&
+                                     reporter ? p.status : nullptr, ri, p.window_left, p.split_align,
+                                     p.dense_block) &&
                         split < ri.nsplits;
     if (!active) {   // uniform across the CTA
         if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
@@ -546,8 +562,11 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     }
     const int G = p.group;
     const int R = ri.w * G;  // <= 128: the plan admits this kernel only when max_w * G <= 128
-    const int key_hi = min(key_lo + p.keys_per_split, ri.len);
-    const int T = (key_hi - key_lo + kBN - 1) / kBN;
+    const int key_hi = min(key_lo + p.keys_per_split, ri.cache_len);
+    const int Tc = (key_hi - key_lo + kBN - 1) / kBN;   // cache tiles
+    // with the dense block operand the request's last split ends with one more
+    // tile: the window's own keys (ctx .. len - 1, from the block tensors)
+    const int T = Tc + ((p.dense_block && split == ri.nsplits - 1) ? 1 : 0);
 
     if (warp == 0) {
         // ------------------------------------------------------------ query tile + K producer
@@ -571,7 +590,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         } else {
             const int issued = produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK, aux->k_full,
                                                             aux->k_empty, aux->list_k, aux, &tmk, abort, lane,
-                                                            pre0, pre1);
+                                                            pre0, pre1, Tc, ri.row0, &tmks);
             if (*abort && lane == 0) {
                 drain_copies<NK>(aux->k_full, issued);
                 atomicOr(p.status, kDevWaitTimeout);
@@ -586,7 +605,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             if (warp_wait(&aux->q_ready, 0, abort)) {
                 const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
                                                                aux->v_empty, aux->list_v, aux, &tmv, abort, lane,
-                                                               pre0, pre1);
+                                                               pre0, pre1, Tc, ri.row0, &tmvs);
                 if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
             }
         }
@@ -633,7 +652,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             auto issue_pv = [&](int n) {
                 const int vs = n % NV, b = n & 1;
                 tc_fence_after();
-                const int np = min(kPPT, (key_hi - (key_lo + n * kBN) + 15) / 16);
+                const int np = n >= Tc ? 1 : min(kPPT, (key_hi - (key_lo + n * kBN) + 15) / 16);
                 const uint32_t v_addr = smem_addr(sV + vs * L::kTileBytes);
                 for (int kk = 0; kk < np; ++kk) {
                     // V page kk: [chunk][16 keys][128 B]; MN atoms (64 head_dim
@@ -743,8 +762,11 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             __syncwarp();
             if (lane == 0) mbar_arrive(&aux->s_empty[sb]);
 
-            const int key0 = key_lo + t * kBN;
-            const int lim = valid ? (min(key_hi - 1, hi) - key0) : -1;  // visible iff lim_lo <= c <= lim
+            // tile t covers keys key0 .. key0 + 63 (the dense block tile: ctx .. ctx + W - 1)
+            const bool block_tile = t >= Tc;
+            const int key0 = block_tile ? ri.ctx : key_lo + t * kBN;
+            const int kend = block_tile ? ri.len : key_hi;
+            const int lim = valid ? (min(kend - 1, hi) - key0) : -1;  // visible iff lim_lo <= c <= lim
             const int lim_lo = lo - key0;
             // Scores stay unscaled: the maximum is taken on raw scores (sc > 0) and
             // the scale is folded into one FFMA per exponent.  Tiles whose keys
@@ -818,13 +840,15 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             // The request's last page may end mid-page: its stale slots hold
             // arbitrary (even non-finite) values and 0 * NaN is NaN, so zero them.
             // (NVFP4 tiles come out of the dequant already zeroed past key_hi)
-            const bool ragged_tail = !KV && key_hi == ri.len && t == T - 1 && (ri.len & 15) != 0;
+            // (the dense block unit holds other windows' rows past W: zeroed likewise)
+            const bool ragged_tail =
+                !KV && (block_tile || (key_hi == ri.cache_len && t == Tc - 1 && (ri.cache_len & 15) != 0));
             if (ragged_tail || TRACE) {
                 if (!(ok = warp_wait(&aux->v_full[vs], (t / NV) & 1, abort))) break;
             }
             if (ragged_tail) {
-                const int np = min(kPPT, (key_hi - key0 + 15) / 16);
-                const int row_first = ri.len - key0, row_end = np * 16;
+                const int np = block_tile ? 1 : min(kPPT, (key_hi - key0 + 15) / 16);
+                const int row_first = block_tile ? ri.w : ri.cache_len - key0, row_end = np * 16;
                 unsigned char* vt = sV + vs * L::kTileBytes;
                 const int pieces = (row_end - row_first) * L::kChunks * 8;
                 for (int u = m; u < pieces; u += 128) {
@@ -839,7 +863,9 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 for (int c = max(0, lim_lo); c <= lim && c < kBN; ++c) {
                     const int key = key0 + c;
                     tr_cnt += 1;
-                    tr_sum += (long long)aux->pages_v[vs][c >> 4] * 16 + (key & 15);
+                    // a dense block key has no cache slot: it counts -(1 + its row)
+                    tr_sum += block_tile ? -1 - (long long)(ri.row0 + c)
+                                         : (long long)aux->pages_v[vs][c >> 4] * 16 + (key & 15);
                 }
             }
             if constexpr (KV) {
@@ -1121,6 +1147,38 @@ bool encode_scale_map(CUtensorMap* map, const void* pool, int num_pages, int hkv
     return res == CUDA_SUCCESS;
 }
 
+// Dense block operand [total_rows, Hkv, d] bf16 viewed as (d, row, kv head);
+// box = 64 elements x 16 rows of one head (a 16-key unit of K), 128-byte
+// swizzle; rows past total_rows are zero-filled.
+bool encode_block_k_map(CUtensorMap* map, const void* t, int total_rows, int hkv, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)total_rows, (cuuint64_t)hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)hkv * d * 2, (cuuint64_t)d * 2};
+    cuuint32_t box[3] = {64, 16, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(t), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
+// The same tensor as (64 elements, row, 64-element chunk, kv head); box = 16
+// rows of one head with all their chunks, landing [chunk][16 rows][128 B] like
+// a page unit of V.
+bool encode_block_v_map(CUtensorMap* map, const void* t, int total_rows, int hkv, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {64, (cuuint64_t)total_rows, (cuuint64_t)d / 64, (cuuint64_t)hkv};
+    cuuint64_t strides[3] = {(cuuint64_t)hkv * d * 2, 128, (cuuint64_t)d * 2};
+    cuuint32_t box[4] = {64, 16, (cuuint32_t)d / 64, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(t), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS;
+}
+
 // Q [total_rows, Hq, d] bf16 viewed as (d, head, row); box = 64 elements x G heads
 // x max_w rows, 128-byte swizzle, out-of-range rows zero-filled.
 bool encode_q_map(CUtensorMap* map, const void* q, int total_rows, int hq, int d, int group, int max_w) {
@@ -1173,6 +1231,12 @@ bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
                                 p.num_kv_heads, p.head_dim, ps, p.scale_page_stride);
     memset(maps->ks, 0, sizeof(maps->ks));
     memset(maps->vs, 0, sizeof(maps->vs));
+    if (p.dense_block &&
+        !(encode_block_k_map(reinterpret_cast<CUtensorMap*>(maps->ks), p.block_k, p.total_rows, p.num_kv_heads,
+                             p.head_dim) &&
+          encode_block_v_map(reinterpret_cast<CUtensorMap*>(maps->vs), p.block_v, p.total_rows, p.num_kv_heads,
+                             p.head_dim)))
+        return false;
     return encode_pool_map(reinterpret_cast<CUtensorMap*>(maps->k), p.k_pool, p.num_pages, p.num_kv_heads,
                            p.head_dim, ps, p.kv_page_stride) &&
            encode_pool_map_units(reinterpret_cast<CUtensorMap*>(maps->v), p.v_pool, p.num_pages, p.num_kv_heads,

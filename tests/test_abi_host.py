@@ -66,6 +66,9 @@ def _problem(**over):
     (dict(kv_page_stride=2056), sa.SPEC_ATTN_E_INVALID_ARG),                # not a multiple of 16
     (dict(kv_dtype=1, scale_page_stride=32), sa.SPEC_ATTN_E_INVALID_ARG),   # below 16 keys x 4 scale bytes
     (dict(kv_dtype=1, kv_page_stride=520), sa.SPEC_ATTN_E_INVALID_ARG),     # codes: dense 512 B, not x16
+    (dict(dense_block_kv=2), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(dense_block_kv=1, w_invariant=1), sa.SPEC_ATTN_E_INVALID_ARG),     # exactness is a cache-only rule
+    (dict(dense_block_kv=1, kv_dtype=1), sa.SPEC_ATTN_E_UNSUPPORTED),       # the block operand is bf16
     (dict(num_q_heads=34, num_kv_heads=2), sa.SPEC_ATTN_E_UNSUPPORTED),  # group 17
     (dict(num_q_heads=6, num_kv_heads=4), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(max_w=0), sa.SPEC_ATTN_E_INVALID_ARG),
@@ -115,6 +118,7 @@ def test_null_arguments(lib):
                                    *([None] * 4), 0, None) == sa.SPEC_ATTN_E_INVALID_ARG
     assert lib.spec_attn_run_append(*([None] * 8), ctypes.c_float(1.0), ctypes.c_float(1.0),
                                     *([None] * 6), 0, None) == sa.SPEC_ATTN_E_INVALID_ARG
+    assert lib.spec_attn_run_dense_block(*([None] * 13), 0, None) == sa.SPEC_ATTN_E_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(tmp_path):
