@@ -48,6 +48,7 @@ struct SplitParams {
     long long scale_page_stride;// bytes between pages of a scale pool (NVFP4)
     int window_left;            // causal sliding window (keys), 0 = none
     int split_align;            // first split of a request starts at a multiple of this (keys)
+    int early_metadata;         // lengths, windows and block table are not written by the previous kernel
     int dense_block;            // the window's keys come from block_k / block_v (bf16 caches)
     const uint16_t* block_k;    // [total_rows, Hkv, d] bf16 bits, or nullptr
     const uint16_t* block_v;

@@ -149,8 +149,9 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
     const int r = blockIdx.z;
 
     // launched as a programmatic dependent: nothing global is touched before
-    // the previous kernel in the stream has completed
-    pdl_wait_primary();
+    // the previous kernel in the stream has completed (with early_metadata,
+    // nothing but the lengths and windows, which that kernel does not write)
+    if (!p.early_metadata) pdl_wait_primary();
     ReqInfo ri;
     const bool reporter = (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0);
     if (!load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
@@ -158,6 +159,7 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
                       p.window_left, p.split_align, p.dense_block))
         return;
     if (split >= ri.nsplits) return;
+    if (p.early_metadata) pdl_wait_primary();
     const int G = p.group;
     const int R = ri.w * G;
     const int row_lo = rg * p.rows_per_cta;

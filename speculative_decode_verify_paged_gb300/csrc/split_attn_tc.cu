@@ -529,8 +529,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
 
     // Up to here the CTA touched only its own resources (and the kernel
     // parameters), which lets it start while the previous kernel in the stream
-    // drains; from here on it reads what that kernel may have written.
-    pdl_wait_primary();
+    // drains; from here on it reads what that kernel may have written -- except
+    // that with early_metadata the caller vouches that the lengths, windows and
+    // block table are not among it, and they are read before the wait.
+    if (!p.early_metadata) pdl_wait_primary();
     // Without a sliding window the split's first block-table entries sit at a
     // fixed place, so the producers fetch them in the same memory round trip
     // as the request's window and length (entries past the request's pages
@@ -556,6 +558,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
         return;
     }
+    if (p.early_metadata) pdl_wait_primary();
     if (p.window_left > 0) {
         key_lo = ri.key_base + split * p.keys_per_split;
         pre0 = pre1 = kNoPrefetch;

@@ -463,3 +463,30 @@ def test_w_invariant_needs_the_tensor_core_kernel():
     with pytest.raises(sa.SpecAttnError) as ei:
         sa.DeviceWorkload(wl, "cuda", w_invariant=1)
     assert ei.value.status == sa.SPEC_ATTN_E_UNSUPPORTED
+
+
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+def test_early_metadata_changes_no_bit(variant):
+    """Reading the lengths, windows and block table before the programmatic
+    wait (early_metadata) gives the same bits as waiting first, also for calls
+    back to back in one captured graph (each a dependent of the previous)."""
+    shapes = [([16000], [16], 24, 4, 256, 0), ([700, 3, 1900], [9, 16, 1], 24, 4, 128, 1),
+              ([100, 2000], [4, 12], 32, 8, 64, 0)]
+    wls = [W.make_workload(f"em{k}", *sh, seed=90 + k, pool_slack=0.1) for k, sh in enumerate(shapes)]
+    late = [make_dw(wl, variant) for wl in wls]
+    early = [make_dw(wl, variant, early_metadata=1) for wl in wls]
+    s = torch.cuda.Stream()
+    outs = []
+    for dws in (late, early):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for dw in dws:
+                dw.run(s)
+        g.replay()
+        torch.cuda.synchronize()
+        outs.append([(dw.o.clone(), dw.lse.clone()) for dw in dws])
+    for (o0, l0), (o1, l1), wl in zip(outs[0], outs[1], wls):
+        assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    for dw, wl in zip(early, wls):
+        o_ref, lse_ref, _ = oracle.run_workload(wl)
+        check_close(dw.o, dw.lse, o_ref, lse_ref)
