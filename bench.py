@@ -191,10 +191,16 @@ HASHED_SOURCES = ("common.cuh", "sm100.cuh", "spec_attn_internal.h", "spec_attn.
 
 
 def kernel_source_hash():
+    """Hash of the attention call's sources with comments and blank space
+    removed: a comment edit leaves the recorded counters valid."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decode_verify_paged_gb300", "csrc")
     for f in HASHED_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

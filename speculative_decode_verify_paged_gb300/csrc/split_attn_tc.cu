@@ -14,24 +14,28 @@
 // Warp roles, bf16 KV (256 threads):
 //   warp 0      loads the query tile once (TMA, one box per 64 head_dim
 //               elements covering G heads x max_w window rows, into the V
-//               slots), then streams the K tiles: 64 keys (four 16-key pages,
-//               one 2 KB box per page and 64 head_dim elements, issued from 16
-//               lanes), 128-byte swizzled, chunk-major, into a ring of slots.
-//   warp 2      streams the V tiles into a second ring, one box per page-head,
-//               once the query tile has left the V slots.
+//               slots), then streams the K tiles: 64 keys (four 16-key units,
+//               a unit being a 16-key page or a quarter/half of a 64/32-key
+//               page; one 2 KB box per unit and 64 head_dim elements, issued
+//               from 16 lanes), 128-byte swizzled, chunk-major, into a ring.
+//   warp 2      streams the V tiles into a second ring, one box per unit of a
+//               page-head, once the query tile has left the V slots.
 //   warp 1      allocates TMEM and issues S_t = Q K_t^T (M 128, N 64, query
 //               tile from TMEM, -> fp32 in TMEM, double-buffered).
-//   warp 3      issues O += P_t V_t (M 128, N head_dim, one MMA per page, P
+//   warp 3      issues O += P_t V_t (M 128, N head_dim, one MMA per unit, P
 //               from shared memory, V MN-major).  Each issuer waits only on its
 //               own inputs, in tile order.
 //   warps 4-7   softmax: thread m owns row m (TMEM lane m).  First it moves its
 //               query row into TMEM.  Per tile it reads its 64 scores, applies
-//               the causal-in-block / non-causal mask by key index, updates a
+//               the causal-in-block / non-causal mask and the sliding window
+//               by key index (rows past W x G run unmasked), updates a
 //               base-2 online softmax whose reference maximum moves only when a
 //               score exceeds it by more than 2^8 (then the row of O in TMEM is
 //               rescaled), and writes P into one half of a double buffer; at
 //               the end it normalises O and stages the row for the output (or a
 //               split partial), which every warp then copies out.
+// With the dense block operand, the request's last split ends with one more
+// tile: the window's own keys, one unit loaded from the block tensors.
 // NVFP4 KV (512 threads): warp 0 streams the tiles' codes and scales by TMA
 // into a raw ring; warps 8-11 decode K and 12-15 decode V into fp16 operand
 // tiles; the query row is converted to fp16 on its way into TMEM, S is single-
@@ -63,7 +67,7 @@ __device__ __forceinline__ int ld_volatile_i32(const int32_t* p) {
     return v;
 }
 
-constexpr int kBN = 64;        // keys per tile (a multiple of the 16-key page; 32 or 64)
+constexpr int kBN = 64;        // keys per tile (a multiple of the 16-key unit; 32 or 64)
 constexpr int kPPT = kBN / 16;  // pages per tile
 static_assert(kBN == 32 || kBN == 64, "tile");
 constexpr int kM = 128;        // MMA rows (query tile, padded)
@@ -97,7 +101,7 @@ struct TcLayout {
     // (one half each); 64-key tiles fill a row, so the buffers are separate.
     static constexpr int kPBytes = KV ? 0 : kM * 128 * (kBN == 64 ? 2 : 1);
     static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile (16-bit elements)
-    static constexpr int kPageBytes = 16 * D * 2;          // one page-head of V (16-bit elements)
+    static constexpr int kPageBytes = 16 * D * 2;          // one 16-key unit of V (16-bit elements)
     // NVFP4 raw slot: the codes and scales of a tile's 16-key units, K then V.
     // Every TMA tile copy lands on a 128-byte boundary (the tensor copy's
     // shared-memory alignment), so a unit's scales (d bytes: 64 at d = 64)
@@ -257,7 +261,7 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(np * L::kChunks * 2048));
         __syncwarp();
         if (IS_V) {
-            // lane pp: the whole page-head pp in one copy, [chunk][16 slots][128 B]
+            // lane pp: all of unit pp in one copy, [chunk][16 slots][128 B]
             if (lane < np) {
                 const int pg = list[rel - list_base + lane];
                 if (TRACE) aux->pages_v[slot][lane] = pg;
@@ -288,8 +292,8 @@ __device__ __forceinline__ int raw_code_chunk(int sl, int ch) {
 }
 
 // NVFP4: one warp streams each tile's e2m1 codes and e4m3 scales, K and V, into
-// a raw ring slot by TMA: per page-head one box of codes (16 keys x d/2 bytes,
-// swizzled) and one of scales (d bytes), issued from 4 lanes per page.
+// a raw ring slot by TMA: per 16-key unit one box of codes (16 keys x d/2
+// bytes, swizzled) and one of scales (d bytes), issued from 4 lanes per unit.
 template <int D>
 __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
                                            unsigned char* raw, TcAux* aux, const CUtensorMap* tkc,
@@ -651,7 +655,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 mma_commit(&aux->k_empty[ks]);
                 mma_commit(&aux->s_full[b]);
             };
-            // O += P_n V_n, one MMA per 16-key page
+            // O += P_n V_n, one MMA per 16-key unit
             auto issue_pv = [&](int n) {
                 const int vs = n % NV, b = n & 1;
                 tc_fence_after();
