@@ -135,7 +135,8 @@ typedef struct spec_attn_problem {
     int32_t num_kv_heads;        /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 16 */
     int32_t head_dim;            /* 64, 128 or 256 */
     int32_t page_size;           /* keys per page: 16, 32 or 64 */
-    int32_t num_pages;           /* pages in each pool (device bounds check) */
+    int32_t num_pages;           /* pages in each pool (device bounds check); >= 1 when
+                                    num_reqs > 0, even if no key is cached */
     int32_t block_table_stride;  /* int32 entries per block-table row */
     int32_t mask_mode;           /* spec_attn_mask_mode */
     int32_t kv_dtype;            /* spec_attn_kv_dtype */

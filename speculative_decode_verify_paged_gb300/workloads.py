@@ -202,7 +202,8 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
     pages_needed = [math.ceil(s / page_size) for s in cached]
     need = sum(pages_needed)
     if pool_pages is None:
-        pool_pages = need + int(math.ceil(need * pool_slack))
+        # at least one page: the library takes a pool even when no key is cached
+        pool_pages = max(1, need + int(math.ceil(need * pool_slack)))
     assert pool_pages >= need, "pool too small"
     perm = torch.randperm(pool_pages, generator=g) if fragmented else torch.arange(pool_pages)
     stride = bt_stride if bt_stride is not None else max(max(pages_needed, default=1), 1)
