@@ -153,7 +153,9 @@ def table_workloads():
             ("verify_w16_ctx16k_pages64", lambda: W.verify_sweep(16, page_size=64, pool_pages=512)),
             ("verify_w16_ctx16k_interleaved_kv", lambda: W.verify_sweep(16), {"interleave": True}),
             ("long_verify_w16_window4096", lambda: W.long_verify(16, window_left=4096)),
-            ("batched_draft_dense_block", lambda: W.batched_draft(dense_block=True))]
+            ("batched_draft_dense_block", lambda: W.batched_draft(dense_block=True)),
+            ("verify_w16_ctx16k_hq64_g16", lambda: W.make_workload("verify_ctx16384_w16_hq64", [16384], 16, 64, 4,
+                                                                      256, W.MASK_CAUSAL_IN_BLOCK, pool_pages=2048))]
 
 
 def run_reference(args, rank, world):

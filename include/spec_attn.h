@@ -176,8 +176,8 @@ typedef struct spec_attn_problem {
  * on key positions (every fixed_keys_per_split keys), always writes split
  * partials and always merges them in a fold order fixed by the split index
  * alone (split s in group s mod G, G a constant of head_dim).  It
- * needs the tensor-core kernel (max_w x Hq/Hkv <= 128; E_UNSUPPORTED
- * otherwise) and ignores force_splits.  Rows computed in W-invariant mode match
+ * needs the tensor-core kernel (E_UNSUPPORTED if the CUDA-core one is
+ * forced) and ignores force_splits.  Rows computed in W-invariant mode match
  * rows computed in W-invariant mode with the same fixed_keys_per_split; the
  * default mode's splits are chosen for speed and may round differently.  The
  * cost is the split count this fixes: one CTA per (split, KV head, request),
@@ -193,7 +193,9 @@ typedef struct spec_attn_plan_info {
     int32_t kernel_variant;      /* the variant that will run (never AUTO) */
     int32_t keys_per_split;      /* keys of one request one CTA sweeps (multiple of 64) */
     int32_t max_splits;          /* splits of the longest request */
-    int32_t row_groups;          /* CTAs sharing one (request, KV head, split); 1 for tcgen05 */
+    int32_t row_groups;          /* CTAs sharing one (request, KV head, split), each with
+                                    its own rows; tcgen05: > 1 only above 128 query rows
+                                    per KV head (groups of whole window rows) */
     int32_t grid_x, grid_y, grid_z;
     int32_t block_threads;
     int32_t smem_bytes;          /* dynamic shared memory of the split kernel */

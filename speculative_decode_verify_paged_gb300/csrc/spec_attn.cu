@@ -240,13 +240,15 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         return SPEC_ATTN_E_UNSUPPORTED;
     }
     plan->w_invariant = p.w_invariant != 0;
-    // AUTO takes the tensor-core kernel wherever it applies (W x G <= 128, bf16 KV).
+    // AUTO takes the tensor-core kernel wherever it applies (every supported
+    // head_dim and KV dtype; windows of more than 128 rows per KV head in row groups).
     const bool use_tc = p.kernel_variant == SPEC_ATTN_VARIANT_TCGEN05 ||
                         (p.kernel_variant == SPEC_ATTN_VARIANT_AUTO && tc_ok);
     if (use_tc) {
         plan->variant = SPEC_ATTN_VARIANT_TCGEN05;
-        plan->rows_per_cta = 128;
-        plan->row_groups = 1;
+        const int wg = tc_window_rows_per_cta(p.max_w, G);
+        plan->rows_per_cta = wg * G;
+        plan->row_groups = (p.max_w + wg - 1) / wg;
         plan->threads = tc_threads(p.kv_dtype);
         plan->smem = tc_smem_bytes(p.head_dim, p.kv_dtype);
         e = tc_prepare(p.head_dim, p.kv_dtype);

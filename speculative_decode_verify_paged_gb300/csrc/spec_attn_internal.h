@@ -38,8 +38,8 @@ struct SplitParams {
     int mask_mode;
     int keys_per_split;         // multiple of 64
     int max_splits;
-    int row_groups;             // CTAs per (request, KV head, split) (CUDA-core path)
-    int rows_per_cta;
+    int row_groups;             // CTAs per (request, KV head, split)
+    int rows_per_cta;           // query rows per CTA (tensor-core kernel: whole window rows x G)
     long long max_seq_len;
     float score_scale_log2;     // sm_scale * log2(e) [* k_gscale for NVFP4]
     float out_scale;            // 1, or v_gscale for NVFP4
@@ -153,6 +153,8 @@ struct TcMaps {
     alignas(64) unsigned char vs[128];
 };
 bool tc_supported(int head_dim, int kv_dtype, int max_rows);
+// window rows one CTA of the tensor-core kernel holds (its row group): Wg x G <= 128
+int tc_window_rows_per_cta(int max_w, int group);
 int tc_smem_bytes(int head_dim, int kv_dtype);
 int tc_threads(int kv_dtype);
 cudaError_t tc_prepare(int head_dim, int kv_dtype);

@@ -474,7 +474,11 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     using L = TcLayout<D, KV>;
     constexpr int NK = L::kNK, NV = L::kNV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
+    // blockIdx.x = split x row groups: a row group is up to 128 / G whole window
+    // rows (all G heads of each), so windows of more than 128 rows per KV head
+    // take several CTAs, each streaming the split's K/V once
+    const int rg = blockIdx.x % p.row_groups, split = blockIdx.x / p.row_groups;
+    const int kvh = blockIdx.y, r = blockIdx.z;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -552,12 +556,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         if (((u0 + 32) >> p.page_shift) < p.bt_stride) pre1 = ld_volatile_i32(bt + ((u0 + 32) >> p.page_shift));
     }
     ReqInfo ri;
-    const bool reporter = (tid == 0 && split == 0 && kvh == 0);
+    const bool reporter = (tid == 0 && blockIdx.x == 0 && kvh == 0);
     const bool active = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
                                      p.bt_stride << (4 + p.page_shift), p.keys_per_split,
                                      reporter ? p.status : nullptr, ri, p.window_left, p.split_align,
                                      p.dense_block) &&
-                        split < ri.nsplits;
+                        split < ri.nsplits && rg * (p.rows_per_cta / p.group) < ri.w;
     if (!active) {   // uniform across the CTA
         if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
         return;
@@ -568,7 +572,9 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         pre0 = pre1 = kNoPrefetch;
     }
     const int G = p.group;
-    const int R = ri.w * G;  // <= 128: the plan admits this kernel only when max_w * G <= 128
+    const int Wg = p.rows_per_cta / G;                 // window rows per row group (Wg x G <= 128)
+    const int w_lo = rg * Wg;                          // this CTA's first window row
+    const int R = min(ri.w - w_lo, Wg) * G;            // its query rows
     const int key_hi = min(key_lo + p.keys_per_split, ri.cache_len);
     const int Tc = (key_hi - key_lo + kBN - 1) / kBN;   // cache tiles
     // with the dense block operand the request's last split ends with one more
@@ -578,13 +584,13 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     if (warp == 0) {
         // ------------------------------------------------------------ query tile + K producer
         if (lane == 0) {
-            // one box of 64 head_dim elements x G heads x max_w rows per 128-byte
-            // atom column; rows past total_q_rows are zero-filled by TMA, rows past
-            // W_r x G belong to no output and are masked in the softmax.
-            const uint32_t qbytes = static_cast<uint32_t>(L::kChunks * 128 * G * p.max_w);
+            // one box of 64 head_dim elements x G heads x Wg window rows per
+            // 128-byte atom column; rows past total_q_rows are zero-filled by TMA,
+            // rows past the group's share of W_r x G belong to no output.
+            const uint32_t qbytes = static_cast<uint32_t>(L::kChunks * 128 * G * Wg);
             mbar_arrive_expect_tx(&aux->q_full, qbytes);
             for (int c = 0; c < L::kChunks; ++c)
-                tma_load_3d(sQ + c * (kM * 128), &tmq, c * 64, kvh * G, ri.row0, &aux->q_full);
+                tma_load_3d(sQ + c * (kM * 128), &tmq, c * 64, kvh * G, ri.row0 + w_lo, &aux->q_full);
         }
         __syncwarp();
         if constexpr (KV) {
@@ -709,7 +715,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         const int m = wq * 32 + lane;
         const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const bool valid = m < R;
-        const int i = valid ? m / G : 0;
+        const int i = w_lo + (valid ? m / G : 0);      // window row
         const int hq = kvh * G + (valid ? m % G : 0);
         const int qrow = ri.row0 + i;
         const int hi = (p.mask_mode == 0) ? (ri.ctx + i) : (ri.len - 1);
@@ -996,7 +1002,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     if (u < total) {
                         const int mm = u >> lg, c = u & ((1 << lg) - 1);
                         unsigned char* dst = reinterpret_cast<unsigned char*>(p.o) +
-                                             (((size_t)(ri.row0 + mm / G) * p.num_q_heads + kvh * G + mm % G) * D) * 2 +
+                                             (((size_t)(ri.row0 + w_lo + mm / G) * p.num_q_heads + kvh * G + mm % G) * D) * 2 +
                                              c * 16;
                         st_global_v4(dst, v[k]);
                     }
@@ -1008,7 +1014,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             const int total = R << lg;
             const float* rinv = reinterpret_cast<const float*>(smem + kM * rs);
             unsigned char* blk = reinterpret_cast<unsigned char*>(
-                p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0, 0) * D);
+                p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0 + w_lo, 0) * D);
             for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
                 uint4 a[kBatchPieces], b[kBatchPieces];
                 float sc[kBatchPieces];
@@ -1203,9 +1209,14 @@ bool encode_q_map(CUtensorMap* map, const void* q, int total_rows, int hq, int d
 
 }  // namespace
 
+// Any row count: windows of more than 128 query rows per KV head are split
+// into row groups of whole window rows (G <= 16 rows each, so a group is never
+// empty).
 bool tc_supported(int head_dim, int kv_dtype, int max_rows) {
-    return (kv_dtype == 0 || kv_dtype == 1) && max_rows <= kM && (head_dim == 64 || head_dim == 128 || head_dim == 256);
+    return (kv_dtype == 0 || kv_dtype == 1) && max_rows >= 1 && (head_dim == 64 || head_dim == 128 || head_dim == 256);
 }
+
+int tc_window_rows_per_cta(int max_w, int group) { return max_w < kM / group ? max_w : kM / group; }
 
 int tc_smem_bytes(int head_dim, int kv_dtype) { return smem_for(head_dim, kv_dtype); }
 int tc_threads(int kv_dtype) { return kv_dtype ? kTcThreadsFp4 : kTcThreadsBf16; }
@@ -1224,7 +1235,7 @@ cudaError_t tc_prepare(int head_dim, int kv_dtype) {
 bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
     static_assert(sizeof(CUtensorMap) == sizeof(maps->q), "tensor map size");
     if (!encode_q_map(reinterpret_cast<CUtensorMap*>(maps->q), p.q, p.total_rows, p.num_q_heads, p.head_dim,
-                      p.group, p.max_w))
+                      p.group, p.rows_per_cta / p.group))
         return false;
     const int ps = 16 << p.page_shift;
     if (kv_dtype != 0)

@@ -461,8 +461,27 @@ def test_w_invariant_is_independent_of_the_batch():
 def test_w_invariant_needs_the_tensor_core_kernel():
     wl = W.make_workload("winvu", [300], [16], 64, 4, 128, 0, seed=73)    # 256 rows per KV head
     with pytest.raises(sa.SpecAttnError) as ei:
-        sa.DeviceWorkload(wl, "cuda", w_invariant=1)
+        sa.DeviceWorkload(wl, "cuda", w_invariant=1, kernel_variant=sa.SPEC_ATTN_VARIANT_CUDA_CORE)
     assert ei.value.status == sa.SPEC_ATTN_E_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_NVFP4])
+def test_w_invariant_across_row_groups(kv):
+    """256 query rows per KV head (G 16, W 16) take two row groups on the
+    tensor cores; every row still equals its own W = 1 call bit for bit."""
+    wl = W.make_workload("winvrg", [900, 40], [16, 11], 64, 4, 128, 0, kv_dtype=kv, seed=74, pool_slack=0.2)
+    dw = sa.DeviceWorkload(wl, "cuda", w_invariant=1, fixed_keys_per_split=128)
+    assert dw.plan.info["row_groups"] == 2 and dw.plan.info["kernel_variant"] == sa.SPEC_ATTN_VARIANT_TCGEN05
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() == 0
+    o_ref, lse_ref, _ = oracle.run_workload(wl)
+    check_close(dw.o, dw.lse, o_ref, lse_ref)
+    ind = wl.q_indptr.tolist()
+    for r in range(wl.num_reqs):
+        for i in range(ind[r + 1] - ind[r]):
+            o1, l1 = _row_alone(wl, dw, r, i, 128)
+            assert torch.equal(dw.o[ind[r] + i], o1) and torch.equal(dw.lse[ind[r] + i], l1), (r, i)
 
 
 @pytest.mark.parametrize("variant", VARIANTS[1:])
