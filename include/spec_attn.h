@@ -163,6 +163,12 @@ typedef struct spec_attn_problem {
                                     layer of a decode step that fills them once per
                                     step); the attention kernel then reads them while
                                     that kernel drains.  0: it waits first (safe). */
+    int32_t test_stall;          /* testing only (needs kernel_variant TCGEN05): 1 makes
+                                    the K producer issue nothing, so its consumers'
+                                    bounded waits run out after about a second; the
+                                    call then sets SPEC_ATTN_DEV_WAIT_TIMEOUT, frees its
+                                    tensor memory and returns, leaving O undefined and
+                                    the context usable.  0 in every real call. */
 } spec_attn_problem;
 
 /*

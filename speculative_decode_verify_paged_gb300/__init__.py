@@ -70,7 +70,7 @@ class spec_attn_problem(ctypes.Structure):
         ("w_invariant", ctypes.c_int32), ("fixed_keys_per_split", ctypes.c_int32),
         ("window_left", ctypes.c_int32), ("kv_page_stride", ctypes.c_int64),
         ("scale_page_stride", ctypes.c_int64), ("dense_block_kv", ctypes.c_int32),
-        ("early_metadata", ctypes.c_int32),
+        ("early_metadata", ctypes.c_int32), ("test_stall", ctypes.c_int32),
     ]
 
 
@@ -216,14 +216,14 @@ def spec_attn_plan_create(*, num_reqs, total_q_rows, max_w, num_q_heads, num_kv_
                           page_size=16, sm_scale=0.0, force_splits=0, kernel_variant=0,
                           seq_lens=None, q_indptr=None, w_invariant=0, fixed_keys_per_split=0,
                           window_left=0, kv_page_stride=0, scale_page_stride=0, dense_block_kv=0,
-                          early_metadata=0) -> Plan:
+                          early_metadata=0, test_stall=0) -> Plan:
     lib = load_library()
     prob = spec_attn_problem(num_reqs, total_q_rows, max_w, num_q_heads, num_kv_heads, head_dim,
                              page_size, num_pages, block_table_stride, mask_mode, kv_dtype,
                              float(sm_scale), int(max_seq_len), force_splits, kernel_variant,
                              int(w_invariant), int(fixed_keys_per_split), int(window_left),
                              int(kv_page_stride), int(scale_page_stride), int(dense_block_kv),
-                             int(early_metadata))
+                             int(early_metadata), int(test_stall))
     sl, _k1 = _host_i32(seq_lens)
     qi, _k2 = _host_i32(q_indptr)
     handle = ctypes.c_void_p()

@@ -123,6 +123,9 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
     if (p->w_invariant != 0 && p->w_invariant != 1) return SPEC_ATTN_E_INVALID_ARG;
     if (p->dense_block_kv != 0 && p->dense_block_kv != 1) return SPEC_ATTN_E_INVALID_ARG;
     if (p->early_metadata != 0 && p->early_metadata != 1) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->test_stall != 0 && p->test_stall != 1) return SPEC_ATTN_E_INVALID_ARG;
+    // the stall exercises the tensor-core kernel's bounded waits
+    if (p->test_stall && p->kernel_variant != SPEC_ATTN_VARIANT_TCGEN05) return SPEC_ATTN_E_INVALID_ARG;
     if (p->dense_block_kv && p->w_invariant) return SPEC_ATTN_E_INVALID_ARG;   // exactness is a cache-only rule
     if (p->dense_block_kv && p->kv_dtype != SPEC_ATTN_KV_BF16) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->w_invariant && (p->fixed_keys_per_split < 0 || p->fixed_keys_per_split % 64 != 0))
@@ -544,6 +547,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.split_align = plan->split_align;
     sp.dense_block = p.dense_block_kv;
     sp.early_metadata = p.early_metadata;
+    sp.test_stall = p.test_stall;
     sp.block_k = static_cast<const uint16_t*>(block_k);
     sp.block_v = static_cast<const uint16_t*>(block_v);
 

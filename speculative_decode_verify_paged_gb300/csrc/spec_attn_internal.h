@@ -49,6 +49,7 @@ struct SplitParams {
     int window_left;            // causal sliding window (keys), 0 = none
     int split_align;            // first split of a request starts at a multiple of this (keys)
     int early_metadata;         // lengths, windows and block table are not written by the previous kernel
+    int test_stall;             // testing: the K (NVFP4: raw) producer issues nothing
     int dense_block;            // the window's keys come from block_k / block_v (bf16 caches)
     const uint16_t* block_k;    // [total_rows, Hkv, d] bf16 bits, or nullptr
     const uint16_t* block_v;

@@ -203,6 +203,7 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
                                        TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane,
                                        int pre0, int pre1, int Tc, int row0, const CUtensorMap* tm_block) {
     using L = TcLayout<D, 0>;
+    if (!IS_V && p.test_stall) return 0;   // testing: K never arrives, its consumers' waits run out
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
     const int u_lo = key_lo / 16;                    // first 16-key unit of the split
     const int n_pages = (key_hi - key_lo + 15) / 16;  // 16-key units
@@ -301,6 +302,7 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
                                            volatile int* abort, int lane, int pre0, int pre1) {
     using L = TcLayout<D, 1>;
     constexpr int NR = L::kNR;
+    if (p.test_stall) return 0;   // testing: nothing arrives, the decoders' waits run out
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
     const int u_lo = key_lo / 16;
     const int n_pages = (key_hi - key_lo + 15) / 16;   // 16-key units
@@ -974,6 +976,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }
+    // whichever role gave up, the call reports it
+    if (tid == 0 && *abort != 0) atomicOr(p.status, kDevWaitTimeout);
     // ------------------------------------------------------------ copy-out (every thread)
     // The staged rows leave in coalesced 16-byte pieces, several loads in
     // flight per thread before their stores.  Split partials of this CTA are one
