@@ -535,6 +535,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.max_splits = plan->max_splits;
     sp.row_groups = plan->row_groups;
     sp.rows_per_cta = plan->rows_per_cta;
+    sp.window_rows_per_cta = plan->rows_per_cta / sp.group;
     sp.max_seq_len = p.max_seq_len;
     const float log2e = 1.4426950408889634f;
     const bool fp4 = p.kv_dtype == SPEC_ATTN_KV_NVFP4;

@@ -40,6 +40,7 @@ struct SplitParams {
     int max_splits;
     int row_groups;             // CTAs per (request, KV head, split)
     int rows_per_cta;           // query rows per CTA (tensor-core kernel: whole window rows x G)
+    int window_rows_per_cta;    // tensor-core kernel: window rows of one row group
     long long max_seq_len;
     float score_scale_log2;     // sm_scale * log2(e) [* k_gscale for NVFP4]
     float out_scale;            // 1, or v_gscale for NVFP4

@@ -203,7 +203,6 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
                                        TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane,
                                        int pre0, int pre1, int Tc, int row0, const CUtensorMap* tm_block) {
     using L = TcLayout<D, 0>;
-    if (!IS_V && p.test_stall) return 0;   // testing: K never arrives, its consumers' waits run out
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
     const int u_lo = key_lo / 16;                    // first 16-key unit of the split
     const int n_pages = (key_hi - key_lo + 15) / 16;  // 16-key units
@@ -302,7 +301,6 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
                                            volatile int* abort, int lane, int pre0, int pre1) {
     using L = TcLayout<D, 1>;
     constexpr int NR = L::kNR;
-    if (p.test_stall) return 0;   // testing: nothing arrives, the decoders' waits run out
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
     const int u_lo = key_lo / 16;
     const int n_pages = (key_hi - key_lo + 15) / 16;   // 16-key units
@@ -468,7 +466,7 @@ __device__ __forceinline__ void drain_copies(uint64_t* full, int issued) {
     }
 }
 
-template <int D, int KV, bool TRACE>
+template <int D, int KV, bool TRACE, bool RG>
 __global__ void __launch_bounds__(KV ? kTcThreadsFp4 : kTcThreadsBf16, 1)
 split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -476,10 +474,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     using L = TcLayout<D, KV>;
     constexpr int NK = L::kNK, NV = L::kNV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // blockIdx.x = split x row groups: a row group is up to 128 / G whole window
-    // rows (all G heads of each), so windows of more than 128 rows per KV head
-    // take several CTAs, each streaming the split's K/V once
-    const int rg = blockIdx.x % p.row_groups, split = blockIdx.x / p.row_groups;
+    // RG: blockIdx.x = split x row groups.  A row group is up to 128 / G whole
+    // window rows (all G heads of each), so windows of more than 128 rows per KV
+    // head take several CTAs, each streaming the split's K/V once.  Without RG
+    // (one group) the row offsets below are compile-time zeros.
+    const int rg = RG ? blockIdx.x % p.row_groups : 0;
+    const int split = RG ? blockIdx.x / p.row_groups : blockIdx.x;
     const int kvh = blockIdx.y, r = blockIdx.z;
 
     extern __shared__ unsigned char smem_raw[];
@@ -563,7 +563,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                                      p.bt_stride << (4 + p.page_shift), p.keys_per_split,
                                      reporter ? p.status : nullptr, ri, p.window_left, p.split_align,
                                      p.dense_block) &&
-                        split < ri.nsplits && rg * (p.rows_per_cta / p.group) < ri.w;
+                        split < ri.nsplits && (!RG || rg * p.window_rows_per_cta < ri.w);
     if (!active) {   // uniform across the CTA
         if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
         return;
@@ -574,9 +574,9 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         pre0 = pre1 = kNoPrefetch;
     }
     const int G = p.group;
-    const int Wg = p.rows_per_cta / G;                 // window rows per row group (Wg x G <= 128)
-    const int w_lo = rg * Wg;                          // this CTA's first window row
-    const int R = min(ri.w - w_lo, Wg) * G;            // its query rows
+    const int Wg = RG ? p.window_rows_per_cta : p.max_w;   // window rows per row group (Wg x G <= 128)
+    const int w_lo = RG ? rg * Wg : 0;                       // this CTA's first window row
+    const int R = (RG ? min(ri.w - w_lo, Wg) : ri.w) * G;   // its query rows
     const int key_hi = min(key_lo + p.keys_per_split, ri.cache_len);
     const int Tc = (key_hi - key_lo + kBN - 1) / kBN;   // cache tiles
     // with the dense block operand the request's last split ends with one more
@@ -596,16 +596,21 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         }
         __syncwarp();
         if constexpr (KV) {
-            const int issued = produce_raw<D>(p, r, kvh, key_lo, key_hi, T, sRaw, aux, &tmk, &tmv, &tmks, &tmvs,
-                                              abort, lane, pre0, pre1);
+            // testing (test_stall): nothing arrives, the decoders' waits run out
+            const int issued = p.test_stall ? 0
+                                            : produce_raw<D>(p, r, kvh, key_lo, key_hi, T, sRaw, aux, &tmk, &tmv,
+                                                             &tmks, &tmvs, abort, lane, pre0, pre1);
             if (*abort && lane == 0) {
                 drain_copies<L::kNR>(aux->raw_full, issued);
                 atomicOr(p.status, kDevWaitTimeout);
             }
         } else {
-            const int issued = produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK, aux->k_full,
-                                                            aux->k_empty, aux->list_k, aux, &tmk, abort, lane,
-                                                            pre0, pre1, Tc, ri.row0, &tmks);
+            // testing (test_stall): K never arrives, its consumers' waits run out
+            const int issued = p.test_stall ? 0
+                                            : produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK,
+                                                                           aux->k_full, aux->k_empty, aux->list_k,
+                                                                           aux, &tmk, abort, lane, pre0, pre1, Tc,
+                                                                           ri.row0, &tmks);
             if (*abort && lane == 0) {
                 drain_copies<NK>(aux->k_full, issued);
                 atomicOr(p.status, kDevWaitTimeout);
@@ -976,8 +981,6 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }
-    // whichever role gave up, the call reports it
-    if (tid == 0 && *abort != 0) atomicOr(p.status, kDevWaitTimeout);
     // ------------------------------------------------------------ copy-out (every thread)
     // The staged rows leave in coalesced 16-byte pieces, several loads in
     // flight per thread before their stores.  Split partials of this CTA are one
@@ -1046,28 +1049,38 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 }
             }
         }
+    } else if (tid == 0) {
+        atomicOr(p.status, kDevWaitTimeout);   // whichever role gave up, the call reports it
     }
 }
 
 using TcKernel = void (*)(const SplitParams, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                           const CUtensorMap, const CUtensorMap);
 
-template <int D, int KV>
+template <int D, int KV, bool RG>
 TcKernel pick_trace(bool traced) {
-    return traced ? &split_attn_tc_kernel<D, KV, true> : &split_attn_tc_kernel<D, KV, false>;
+    return traced ? &split_attn_tc_kernel<D, KV, true, RG> : &split_attn_tc_kernel<D, KV, false, RG>;
+}
+
+template <int D, int KV>
+TcKernel pick_rg(bool traced, bool row_groups) {
+    return row_groups ? pick_trace<D, KV, true>(traced) : pick_trace<D, KV, false>(traced);
 }
 
 template <int KV>
-TcKernel pick_d(int d, bool traced) {
+TcKernel pick_d(int d, bool traced, bool row_groups) {
     switch (d) {
-        case 64: return pick_trace<64, KV>(traced);
-        case 128: return pick_trace<128, KV>(traced);
-        case 256: return pick_trace<256, KV>(traced);
+        case 64: return pick_rg<64, KV>(traced, row_groups);
+        case 128: return pick_rg<128, KV>(traced, row_groups);
+        case 256: return pick_rg<256, KV>(traced, row_groups);
         default: return nullptr;
     }
 }
 
-TcKernel pick(int d, int kv, bool traced) { return kv ? pick_d<1>(d, traced) : pick_d<0>(d, traced); }
+// row_groups: the launch has more than one row group per (request, KV head, split)
+TcKernel pick(int d, int kv, bool traced, bool row_groups) {
+    return kv ? pick_d<1>(d, traced, row_groups) : pick_d<0>(d, traced, row_groups);
+}
 
 template <int KV>
 int smem_d(int d) {
@@ -1226,8 +1239,8 @@ int tc_smem_bytes(int head_dim, int kv_dtype) { return smem_for(head_dim, kv_dty
 int tc_threads(int kv_dtype) { return kv_dtype ? kTcThreadsFp4 : kTcThreadsBf16; }
 
 cudaError_t tc_prepare(int head_dim, int kv_dtype) {
-    for (int traced = 0; traced < 2; ++traced) {
-        TcKernel k = pick(head_dim, kv_dtype, traced != 0);
+    for (int v = 0; v < 4; ++v) {
+        TcKernel k = pick(head_dim, kv_dtype, (v & 1) != 0, (v & 2) != 0);
         if (!k) return cudaErrorInvalidValue;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem_for(head_dim, kv_dtype));
@@ -1239,7 +1252,7 @@ cudaError_t tc_prepare(int head_dim, int kv_dtype) {
 bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
     static_assert(sizeof(CUtensorMap) == sizeof(maps->q), "tensor map size");
     if (!encode_q_map(reinterpret_cast<CUtensorMap*>(maps->q), p.q, p.total_rows, p.num_q_heads, p.head_dim,
-                      p.group, p.rows_per_cta / p.group))
+                      p.group, p.window_rows_per_cta))
         return false;
     const int ps = 16 << p.page_shift;
     if (kv_dtype != 0)
@@ -1267,7 +1280,7 @@ bool tc_encode_maps(const SplitParams& p, int kv_dtype, TcMaps* maps) {
 
 cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bool traced, dim3 grid,
                       cudaStream_t stream, bool programmatic) {
-    TcKernel k = pick(p.head_dim, kv_dtype, traced);
+    TcKernel k = pick(p.head_dim, kv_dtype, traced, p.row_groups > 1);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = grid;
