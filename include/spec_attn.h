@@ -157,8 +157,10 @@ typedef struct spec_attn_problem {
     int32_t dense_block_kv;      /* 1: the window's own keys come from dense block
                                     tensors (spec_attn_run_dense_block), not the cache;
                                     bf16 caches only, not with w_invariant */
-    int32_t early_metadata;      /* 1: the caller vouches that the kernel launched
-                                    just before a run in its stream does not write
+    int32_t early_metadata;      /* 1: the caller vouches that no kernel still running
+                                    when a run starts in its stream (the one launched
+                                    just before it, and any earlier one that kernel
+                                    overlaps through a programmatic launch) writes
                                     seq_lens, q_indptr or block_table (true of every
                                     layer of a decode step that fills them once per
                                     step); the attention kernel then reads them while
