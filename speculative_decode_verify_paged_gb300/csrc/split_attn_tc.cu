@@ -156,8 +156,9 @@ struct TcAux {
     uint64_t p_free[2];
     uint64_t o_done;     // one phase per P V (rescale waits: at most one phase behind)
     uint64_t o_final;    // one phase after the last P V (the epilogue's wait)
-    uint64_t q_full;
-    uint64_t q_ready;    // NVFP4: the query tile converted to fp16 (one arrival per softmax warp)
+    uint64_t q_full;     // the query tile landed in the V slots (TMA bytes)
+    uint64_t q_ready;    // the query tile moved into TMEM (NVFP4: as fp16), its V slots free
+                         // (one arrival per softmax warp)
     uint64_t drain;
     uint64_t drain_pv;   // the P V issuer's own MMAs
     uint64_t raw_full[kMaxNR];             // NVFP4: codes/scales of a tile landed (32 lane arrivals)
