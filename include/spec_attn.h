@@ -93,7 +93,7 @@ typedef struct CUstream_st* spec_attn_stream_t;
 typedef enum spec_attn_status {
     SPEC_ATTN_OK = 0,
     SPEC_ATTN_E_INVALID_ARG = -1,          /* bad shape, pointer, alignment or value */
-    SPEC_ATTN_E_UNSUPPORTED = -2,          /* valid but outside this build's limits */
+    SPEC_ATTN_E_UNSUPPORTED = -2,          /* valid but outside the library's limits */
     SPEC_ATTN_E_WORKSPACE_TOO_SMALL = -3,  /* workspace_bytes below the plan's need */
     SPEC_ATTN_E_CUDA = -4,                 /* a CUDA runtime call failed; see spec_attn_last_cuda_error */
     SPEC_ATTN_E_DEVICE_CHECK = -5          /* a device-side check tripped (check_device_status) */
@@ -121,7 +121,7 @@ typedef enum spec_attn_kernel_variant {
 #define SPEC_ATTN_DEV_BAD_WINDOW    0x4u  /* W_r < 0, W_r > max_w, or rows past total_q_rows */
 #define SPEC_ATTN_DEV_WAIT_TIMEOUT  0x8u  /* a pipeline wait gave up (bounded spin) */
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define SPEC_ATTN_MAX_W 16
 #define SPEC_ATTN_MAX_GROUP 16       /* Hq / Hkv */
 #define SPEC_ATTN_MIN_PAGE_SIZE 16   /* page_size is 16, 32 or 64 */

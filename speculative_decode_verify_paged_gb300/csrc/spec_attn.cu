@@ -137,7 +137,7 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
     if (p->kernel_variant < SPEC_ATTN_VARIANT_AUTO || p->kernel_variant > SPEC_ATTN_VARIANT_TCGEN05)
         return SPEC_ATTN_E_INVALID_ARG;
     if (!(p->sm_scale >= 0.f) || std::isinf(p->sm_scale)) return SPEC_ATTN_E_INVALID_ARG;
-    // limits of this build: fail loudly, never truncate a window
+    // limits of the library: fail loudly, never truncate a window
     if (p->max_w > SPEC_ATTN_MAX_W) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->num_q_heads / p->num_kv_heads > SPEC_ATTN_MAX_GROUP) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return SPEC_ATTN_E_UNSUPPORTED;
@@ -200,7 +200,7 @@ const char* spec_attn_status_string(int status) {
     switch (status) {
         case SPEC_ATTN_OK: return "ok";
         case SPEC_ATTN_E_INVALID_ARG: return "invalid argument";
-        case SPEC_ATTN_E_UNSUPPORTED: return "unsupported by this build (W > 16, head_dim not in {64,128,256}, page_size not in {16,32,64}, group > 16, ...)";
+        case SPEC_ATTN_E_UNSUPPORTED: return "unsupported by the library (W > 16, head_dim not in {64,128,256}, page_size not in {16,32,64}, group > 16, ...)";
         case SPEC_ATTN_E_WORKSPACE_TOO_SMALL: return "workspace too small";
         case SPEC_ATTN_E_CUDA: return "CUDA runtime error";
         case SPEC_ATTN_E_DEVICE_CHECK: return "a device-side check tripped";
