@@ -4,7 +4,9 @@
 // One CTA = (split s of request r's keys) x (KV head kvh).  Its query tile is
 // all W x G rows of the request that read KV head kvh (row m = window row
 // m / G, query head kvh * G + m % G), padded to the MMA's M = 128, so every
-// K/V page of the split is streamed from HBM exactly once whatever W is --
+// K/V page of the split is streamed from HBM exactly once whatever W is
+// (above 128 rows per KV head, in row groups of whole window rows, one CTA
+// each; the template flag RG marks such launches) --
 // the single sweep per window that the page "ChunkedSmallT re-streams full
 // KV per query chunk (DFlash K>=8 verify at long context)" (section
 // "Finding") finds missing for W > 8.  No output is produced for context
@@ -13,7 +15,7 @@
 //
 // Warp roles, bf16 KV (256 threads):
 //   warp 0      loads the query tile once (TMA, one box per 64 head_dim
-//               elements covering G heads x max_w window rows, into the V
+//               elements covering G heads x the group's window rows, into the V
 //               slots), then streams the K tiles: 64 keys (four 16-key units,
 //               a unit being a 16-key page or a quarter/half of a 64/32-key
 //               page; one 2 KB box per unit and 64 head_dim elements, issued
