@@ -89,3 +89,20 @@ def test_write_traffic_averages_split_launches(tmp_path):
     d = json.loads(out.read_text())
     assert d["launches"] == 2 and d["dram_bytes_per_launch"] == 170
     assert d["kernel_source_hash"] == bench.kernel_source_hash()
+
+
+def test_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """The traffic record stays valid across comment edits of the kernel
+    sources, and goes stale on any change to the code itself."""
+    import shutil
+    src = os.path.join(ROOT, "speculative_decode_verify_paged_gb300", "csrc")
+    dst = tmp_path / "speculative_decode_verify_paged_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    f = dst / "merge_lse.cu"
+    text = f.read_text()
+    f.write_text("// a new comment line\n" + text.replace("\n", "\n\n", 3) + "/* and a block\n comment */\n")
+    assert bench.kernel_source_hash() == h0
+    f.write_text(text + "\nstatic int spec_attn_unused_probe_value = 1;\n")
+    assert bench.kernel_source_hash() != h0
