@@ -380,6 +380,40 @@ def test_full_size_sampled(name, make, variant):
     run_and_check(wl, variant, trace=True, sel=_sample(wl))
 
 
+def test_bench_main_step_as_timed():
+    """The timed step of bench.py exactly as it runs there: its three calls
+    (ctx 16384, W 1, 8, 16) with early_metadata, captured in one CUDA graph and
+    replayed with the L2 flush in between; sampled (row, head) pairs of every
+    call against the oracle, and the replayed bits equal to each call run
+    alone and eagerly."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    wls = bench.main_workloads()
+    dws = [sa.DeviceWorkload(wl, "cuda", early_metadata=1) for wl in wls]
+    cap = bench.Captured(dws, torch.cuda.current_stream())
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = (torch.empty(2 * l2, dtype=torch.uint8, device="cuda"),
+             torch.ones(2 * l2 // 4, dtype=torch.float32, device="cuda"))
+    for dw in dws:
+        dw.o.zero_()
+        dw.lse.zero_()
+    for _ in range(3):
+        bench.flush_l2(flush)
+        cap.replay()
+    torch.cuda.synchronize()
+    for dw, wl in zip(dws, wls):
+        assert dw.device_status() == 0
+        alone = sa.DeviceWorkload(wl, "cuda")
+        alone.run()
+        torch.cuda.synchronize()
+        assert torch.equal(dw.o, alone.o) and torch.equal(dw.lse, alone.lse), wl.name
+        sel = _sample(wl)
+        o_ref, lse_ref, _ = oracle.run_workload(wl, row_select=sel)
+        check_close(dw.o, dw.lse, o_ref, lse_ref, sel)
+
+
 # --------------------------------------------------------------------------- #
 # W-invariant mode: a window row equals the same row computed alone
 # --------------------------------------------------------------------------- #
