@@ -137,11 +137,13 @@ typedef struct spec_attn_problem {
     int32_t page_size;           /* keys per page: 16, 32 or 64 */
     int32_t num_pages;           /* pages in each pool (device bounds check); >= 1 when
                                     num_reqs > 0, even if no key is cached */
-    int32_t block_table_stride;  /* int32 entries per block-table row */
+    int32_t block_table_stride;  /* int32 entries per block-table row; a row's capacity,
+                                    stride x page_size keys, at most 2^31 - 1 */
     int32_t mask_mode;           /* spec_attn_mask_mode */
     int32_t kv_dtype;            /* spec_attn_kv_dtype */
     float sm_scale;              /* softmax scale; 0 selects 1/sqrt(head_dim) */
-    int64_t max_seq_len;         /* upper bound on every seq_len the plan will see */
+    int64_t max_seq_len;         /* upper bound on every seq_len the plan will see,
+                                    at most 2^31 - 1 */
     int32_t force_splits;        /* 0: heuristic; n > 0: split the longest request's keys n ways */
     int32_t kernel_variant;      /* spec_attn_kernel_variant */
     int32_t w_invariant;         /* 1: W-invariant mode (below); 0: off */

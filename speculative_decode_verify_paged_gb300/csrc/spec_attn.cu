@@ -156,6 +156,8 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
             return SPEC_ATTN_E_INVALID_ARG;
     }
     if (p->max_seq_len > INT32_MAX) return SPEC_ATTN_E_UNSUPPORTED;
+    // key positions, and a block-table row's capacity in keys, are 32-bit on the device
+    if (static_cast<int64_t>(p->block_table_stride) * p->page_size > INT32_MAX) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->num_kv_heads > 65535 || p->num_reqs > 65535) return SPEC_ATTN_E_UNSUPPORTED;
     if (p->num_reqs > 0) {
         if (p->max_seq_len < 1 || p->num_pages < 1) return SPEC_ATTN_E_INVALID_ARG;

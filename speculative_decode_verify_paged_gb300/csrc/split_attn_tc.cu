@@ -1097,16 +1097,18 @@ int smem_d(int d) {
 
 int smem_for(int d, int kv) { return kv ? smem_d<1>(d) : smem_d<0>(d); }
 
+// The driver's tensor-map encoder, looked up once (a function-local static:
+// initialised by the first caller, safely when plans are made from several
+// host threads).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+        const bool ok = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                                         &q) == cudaSuccess &&
+                        q == cudaDriverEntryPointSuccess;
+        return ok ? reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr) : nullptr;
+    }();
     return fn;
 }
 

@@ -77,6 +77,8 @@ def _problem(**over):
     (dict(mask_mode=2), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(kv_dtype=3), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(block_table_stride=16), sa.SPEC_ATTN_E_INVALID_ARG),  # 260 keys need 17 pages
+    (dict(block_table_stride=2 ** 26, page_size=64), sa.SPEC_ATTN_E_UNSUPPORTED),   # 2^32 keys a row
+    (dict(max_seq_len=2 ** 31), sa.SPEC_ATTN_E_UNSUPPORTED),
     (dict(sm_scale=-1.0), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(kernel_variant=7), sa.SPEC_ATTN_E_INVALID_ARG),
     (dict(num_reqs=-1), sa.SPEC_ATTN_E_INVALID_ARG),
