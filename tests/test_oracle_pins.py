@@ -485,3 +485,32 @@ def test_block_operand_equals_sdpa_on_concatenated_keys():
             ref_lse = torch.logsumexp((q @ k.T) * wl.sm_scale, 1)
             np.testing.assert_allclose(o[ind[r]:ind[r + 1], h], ref.numpy(), rtol=1e-12, atol=1e-13)
             np.testing.assert_allclose(lse[ind[r]:ind[r + 1], h], ref_lse.numpy(), rtol=1e-12)
+
+
+@pytest.mark.parametrize("make", [lambda: wlmod.verify_sweep(16), lambda: wlmod.long_verify(16)],
+                         ids=["verify_ctx16384_w16", "long_verify_ctx65536_w16_peaky"])
+def test_full_size_rows_equal_sdpa(make):
+    """The oracle at the measured sizes (the peaky 64K workload included), on
+    sampled (row, head) pairs, against SDPA in fp64 with the causal-in-block
+    mask of each row (keys 0 .. ctx + i) on the gathered K/V."""
+    wl = make()
+    G = wl.num_q_heads // wl.num_kv_heads
+    pairs = [(0, 0), (7, 13), (15, wl.num_q_heads - 1), (15, 5)]
+    sel = np.zeros((wl.total_rows, wl.num_q_heads), dtype=np.uint8)
+    for i, h in pairs:
+        sel[i, h] = 1
+    o, lse, _ = oracle.run_workload(wl, row_select=sel)
+    L = int(wl.seq_lens[0])
+    ctx = L - wl.total_rows
+    for kvh in sorted({h // G for _, h in pairs}):
+        k, v = _gather(wl, 0, kvh)
+        for i, h in pairs:
+            if h // G != kvh:
+                continue
+            q = wl.q[i, h].to(torch.float64)
+            vis = ctx + i + 1
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                q[None, None, None, :], k[None, None, :vis], v[None, None, :vis], scale=wl.sm_scale)[0, 0, 0]
+            ref_lse = torch.logsumexp((k[:vis] @ q) * wl.sm_scale, 0).item()
+            np.testing.assert_allclose(o[i, h], ref.numpy(), rtol=1e-10, atol=1e-12)
+            assert abs(lse[i, h] - ref_lse) <= 1e-11 * max(1.0, abs(ref_lse)), (i, h)
