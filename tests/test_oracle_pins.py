@@ -514,3 +514,52 @@ def test_full_size_rows_equal_sdpa(make):
             ref_lse = torch.logsumexp((k[:vis] @ q) * wl.sm_scale, 0).item()
             np.testing.assert_allclose(o[i, h], ref.numpy(), rtol=1e-10, atol=1e-12)
             assert abs(lse[i, h] - ref_lse) <= 1e-11 * max(1.0, abs(ref_lse)), (i, h)
+
+
+def test_full_size_nvfp4_and_noncausal_draft_rows_equal_sdpa():
+    """The other two measured workloads at full size, on sampled pairs: the
+    NVFP4 cache (4 requests x ctx 16384, W 8) decoded here from the OCP tables
+    and torch's e4m3, then SDPA with the global scales applied as the format
+    defines them; and the non-causal batched draft (8 requests, W 9, d 128),
+    where every row sees the whole context and block."""
+    tab = json.load(open(os.path.join(GOLDEN, "ocp_fp4_fp8_values.json")))
+    grid = torch.tensor(tab["e2m1_magnitudes"], dtype=torch.float64)
+
+    def gathered(wl, r, kvh, pool, scales):
+        L = int(wl.seq_lens[r])
+        j = torch.arange(L)
+        pages = wl.block_table[r, (j // wl.page_size)].long()
+        slots = (j % wl.page_size).long()
+        if scales is None:
+            return pool[pages, kvh, slots, :].to(torch.float64)
+        codes = pool[pages, kvh, slots, :]
+        c = torch.stack([(codes & 0xF).long(), (codes >> 4).long()], -1).reshape(L, -1)
+        val = grid[c & 7] * torch.where((c & 8) > 0, -1.0, 1.0).to(torch.float64)
+        sc = scales[pages, kvh, slots, :].view(torch.float8_e4m3fn).to(torch.float64)
+        return val * sc.repeat_interleave(16, dim=-1)
+
+    for wl, pairs in ((wlmod.nvfp4(), [(0, 0), (8, 23), (17, 6), (31, 12)]),
+                      (wlmod.batched_draft(), [(0, 0), (13, 31), (40, 9), (71, 17)])):
+        G = wl.num_q_heads // wl.num_kv_heads
+        sel = np.zeros((wl.total_rows, wl.num_q_heads), dtype=np.uint8)
+        for row, h in pairs:
+            sel[row, h] = 1
+        o, lse, _ = oracle.run_workload(wl, row_select=sel)
+        ind = wl.q_indptr.tolist()
+        fp4 = wl.kv_dtype == wlmod.KV_NVFP4
+        kscale = wl.sm_scale * (wl.k_gscale if fp4 else 1.0)
+        vscale = wl.v_gscale if fp4 else 1.0
+        for row, h in pairs:
+            r = max(i for i in range(wl.num_reqs) if ind[i] <= row)
+            i = row - ind[r]
+            L = int(wl.seq_lens[r])
+            w_r = ind[r + 1] - ind[r]
+            vis = (L - w_r + i + 1) if wl.mask_mode == wlmod.MASK_CAUSAL_IN_BLOCK else L
+            k = gathered(wl, r, h // G, wl.k_pool, wl.k_scales if fp4 else None)[:vis]
+            v = gathered(wl, r, h // G, wl.v_pool, wl.v_scales if fp4 else None)[:vis]
+            q = wl.q[row, h].to(torch.float64)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                q[None, None, None, :], k[None, None], v[None, None], scale=kscale)[0, 0, 0] * vscale
+            ref_lse = torch.logsumexp((k @ q) * kscale, 0).item()
+            np.testing.assert_allclose(o[row, h], ref.numpy(), rtol=1e-10, atol=1e-12)
+            assert abs(lse[row, h] - ref_lse) <= 1e-11 * max(1.0, abs(ref_lse)), (wl.name, row, h)
