@@ -128,3 +128,32 @@ def test_null_arguments(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         sa.load_library(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("cstruct,pystruct", [("spec_attn_problem", sa.spec_attn_problem),
+                                              ("spec_attn_plan_info", sa.spec_attn_plan_info)])
+def test_binding_structs_match_the_header_layout(tmp_path, cstruct, pystruct):
+    """The ctypes mirrors of the header's structs have the C compiler's size
+    and every field at the C compiler's offset (a field added to one side
+    only, or in another order, fails here)."""
+    names = [f[0] for f in pystruct._fields_]
+    lines = [f'printf("size %zu\\n", sizeof({cstruct}));']
+    lines += [f'printf("{n} %zu\\n", offsetof({cstruct}, {n}));' for n in names]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "spec_attn.h"\nint main(void) {\n    '
+                   + "\n    ".join(lines) + "\n    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    assert int(out["size"]) == ctypes.sizeof(pystruct)
+    for n in names:
+        assert int(out[n]) == getattr(pystruct, n).offset, n
+    # and the C struct has no field the binding lacks
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct " + cstruct + r"\s*\{(.*?)\}\s*" + cstruct + ";", text, flags=re.S).group(1)
+    c_fields = []
+    for stmt in body.split(";"):
+        if stmt.strip():   # "<type> a" or "<type> a, b, c" (the header's types are one word)
+            c_fields += [d.strip() for d in stmt.split(None, 1)[1].split(",")]
+    assert c_fields == names
