@@ -157,3 +157,38 @@ def test_binding_structs_match_the_header_layout(tmp_path, cstruct, pystruct):
         if stmt.strip():   # "<type> a" or "<type> a, b, c" (the header's types are one word)
             c_fields += [d.strip() for d in stmt.split(None, 1)[1].split(",")]
     assert c_fields == names
+
+
+def _header_prototypes():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?\w+\*?\s+\*?(spec_attn_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M | re.S):
+        params = [p.strip() for p in m.group(2).split(",")]
+        protos[m.group(1)] = [] if params == ["void"] else params
+    return protos
+
+
+def _kind(param):
+    """Argument class of a C parameter: pointer, size_t, 32-bit int or float."""
+    if "*" in param or param.startswith("spec_attn_stream_t"):
+        return "ptr"
+    t = param.split()[0]
+    return {"size_t": "size", "int": "i32", "int32_t": "i32", "uint32_t": "i32", "float": "f32"}[t]
+
+
+def _ctypes_kind(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "ptr"
+    return {ctypes.c_size_t: "size", ctypes.c_int32: "i32", ctypes.c_uint32: "i32", ctypes.c_float: "f32"}[t]
+
+
+def test_binding_argtypes_match_the_header_prototypes(lib):
+    """Every entry point's ctypes argtypes have the header's parameter count and,
+    position by position, its argument class (a missing or extra pointer
+    shifts every later argument: caught here, without a GPU)."""
+    protos = _header_prototypes()
+    assert sorted(protos) == declared_functions()
+    for name, params in protos.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert [_kind(p) for p in params] == [_ctypes_kind(t) for t in fn.argtypes], name
