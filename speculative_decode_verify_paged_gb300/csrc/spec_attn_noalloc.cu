@@ -21,13 +21,20 @@
 // Host code can not use the array's name as a device address, so the first
 // call on each device looks the address up (cudaGetSymbolAddress, with that
 // device current) and caches it; make that first call before any stream
-// capture begins.
+// capture begins.  The cached address belongs to the device's primary
+// context: after cudaDeviceReset it is stale, so a process that resets a
+// device must not call this entry point on it again.
+//
+// Each call clears the status word only after its host checks have passed,
+// so a rejected call writes nothing.  spec_attn_noalloc_check_device_status
+// reads (and clears) the word the last call on the device left.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/spec_attn.h"
+#include "spec_attn_internal.h"
 
 namespace {
 
@@ -65,9 +72,23 @@ extern "C" int spec_attn_run_noalloc(const spec_attn_plan* plan, const void* q, 
         }
         scratch = g_scratch_addr[dev];
     }
-    // the device-status word at the head of the scratch must start at zero
-    st = spec_attn_reset_device_status(scratch, stream);
-    if (st != SPEC_ATTN_OK) return st;
-    return spec_attn_run(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
-                         seq_lens, q_indptr, o, lse, scratch, kNoAllocScratchBytes, stream);
+    // the device-status word at the head of the scratch starts each call at zero
+    return spec_attn::run_clearing_status(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale,
+                                          block_table, seq_lens, q_indptr, o, lse, scratch, kNoAllocScratchBytes,
+                                          stream);
+}
+
+extern "C" int spec_attn_noalloc_check_device_status(spec_attn_stream_t stream, uint32_t* bits) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ATTN_E_CUDA;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        scratch = g_scratch_addr[dev];
+    }
+    if (!scratch) {   // no call has run on this device: nothing to report
+        if (bits) *bits = 0;
+        return SPEC_ATTN_OK;
+    }
+    return spec_attn_check_device_status(scratch, stream, bits);
 }
