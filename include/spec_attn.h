@@ -216,7 +216,14 @@ typedef struct spec_attn_plan_info {
 
 /*
  * Validate a problem and choose the split count (keys per split) and the
- * kernel variant.  Host only; no device allocation.  h_seq_lens [P] and
+ * kernel variant (the plan step of the scope table; its spec_attn_plan).
+ * The split count restates the key-splitting of the page "ChunkedSmallT
+ * re-streams full KV per query chunk (DFlash K>=8 verify at long context)",
+ * section "Finding", without its width cap: every CTA holds all W x G rows of
+ * one KV head, so widths up to 16 keep one sweep; wider ones fail here
+ * rather than truncate (page "perf(dflash): widen the verify window past the
+ * compact graph's four-row limit", section "What changed").  Host only; no
+ * device allocation.  h_seq_lens [P] and
  * h_q_indptr [P+1] are optional host copies: when given they are checked
  * and used by the split heuristic; otherwise max_seq_len and max_w stand in
  * for every request.  A plan may be reused for every layer of a step and
@@ -229,12 +236,22 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
                           const int32_t* h_q_indptr, spec_attn_plan** out,
                           size_t* workspace_bytes);
 
+/* Free a plan (host memory only).  NULL is accepted. */
 int spec_attn_plan_destroy(spec_attn_plan* plan);
 
 int spec_attn_plan_get_info(const spec_attn_plan* plan, spec_attn_plan_info* info);
 
 /*
- * Run one attention call asynchronously on `stream`.
+ * Run one attention call asynchronously on `stream`: the block attention of
+ * the page "DFlash2 leaves the paged graph fast path at every c>1 and
+ * re-attends the whole batch context every decode step" (sections "The
+ * route change" and "Scope": P x W rows over a shared paged pool through a
+ * batched block table, outputs for window rows only), swept once over each
+ * request's keys however wide its window (page "ChunkedSmallT re-streams full
+ * KV per query chunk (DFlash K>=8 verify at long context)", section
+ * "Finding"), reading only seq_len entries (page "perf(dflash): widen the
+ * verify window past the compact graph's four-row limit", section "What
+ * changed").
  *   q         [total_q_rows, Hq, d] bf16, 16-byte aligned
  *   k_pool, v_pool   pools as above, 16-byte aligned (NVFP4: code pools)
  *   k_scales, v_scales  NVFP4 scale pools, 16-byte aligned; NULL for bf16
@@ -299,8 +316,8 @@ int spec_attn_run_dense_block(const spec_attn_plan* plan, const void* q, const v
  * cache, later steps overwrite the rows a rejected tail leaves stale, and
  * attention reads only seq_len entries).  seq_len_r already counts the
  * window, so window row i of request r is written at key position
- * pos = seq_len_r - W_r + i: page block_table[r][pos / 16], slot pos % 16,
- * for every KV head.
+ * pos = seq_len_r - W_r + i: page block_table[r][pos / page_size], slot
+ * pos % page_size, for every KV head.
  *   k_new, v_new  [total_q_rows, Hkv, d] bf16, rows in q_indptr order,
  *                 16-byte aligned; read only
  *   k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table,
@@ -375,10 +392,14 @@ int spec_attn_version(void);
  * rejected with SPEC_ATTN_E_WORKSPACE_TOO_SMALL.  Every call on a device
  * shares the array, so calls that may overlap on the GPU race and must be
  * serialised by the caller; each call clears the device-status word at the
- * head of the array and does not report device-side checks.  The first call
- * on each device looks up the array's device address (with that device
- * current) and caches it; make that first call before any stream capture.
- * Allocates nothing; other arguments and errors as spec_attn_run.
+ * head of the array once its host checks have passed (a rejected call writes
+ * nothing), and spec_attn_noalloc_check_device_status reads what the last
+ * call left.  The first call on each device looks up the array's device
+ * address (with that device current) and caches it; make that first call
+ * before any stream capture.  The cached address belongs to the device's
+ * primary context: after cudaDeviceReset it is stale, so do not call this
+ * entry point again on a device the process has reset.  Allocates nothing;
+ * other arguments and errors as spec_attn_run.
  */
 #define SPEC_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int spec_attn_run_noalloc(const spec_attn_plan* plan, const void* q, const void* k_pool,
@@ -386,6 +407,15 @@ int spec_attn_run_noalloc(const spec_attn_plan* plan, const void* q, const void*
                           float k_gscale, float v_gscale, const int32_t* block_table,
                           const int32_t* seq_lens, const int32_t* q_indptr, void* o, float* lse,
                           spec_attn_stream_t stream);
+
+/*
+ * Device-status bits of the last spec_attn_run_noalloc call on the current
+ * device (read and cleared, synchronising `stream` like
+ * spec_attn_check_device_status); 0 in *bits, and SPEC_ATTN_OK, before any
+ * such call.  Returns SPEC_ATTN_E_DEVICE_CHECK when a bit is set.  Also no
+ * counterpart on the pages: it completes the no-alloc entry point.
+ */
+int spec_attn_noalloc_check_device_status(spec_attn_stream_t stream, uint32_t* bits);
 
 #ifdef __cplusplus
 }

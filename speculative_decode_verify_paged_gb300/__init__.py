@@ -49,7 +49,8 @@ EXPORTED_SYMBOLS = (
     "spec_attn_run", "spec_attn_run_traced", "spec_attn_plan_set_timing_events",
     "spec_attn_reset_device_status", "spec_attn_check_device_status",
     "spec_attn_status_string", "spec_attn_last_cuda_error", "spec_attn_version",
-    "spec_attn_run_noalloc", "spec_attn_append_kv", "spec_attn_run_append", "spec_attn_run_dense_block",
+    "spec_attn_run_noalloc", "spec_attn_noalloc_check_device_status", "spec_attn_append_kv",
+    "spec_attn_run_append", "spec_attn_run_dense_block",
 )
 
 
@@ -128,6 +129,8 @@ def load_library(path: Optional[str] = None):
         lib.spec_attn_version.argtypes = []
         lib.spec_attn_run_noalloc.restype = i32
         lib.spec_attn_run_noalloc.argtypes = run_args + [vp]
+        lib.spec_attn_noalloc_check_device_status.restype = i32
+        lib.spec_attn_noalloc_check_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         cache_args = [vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp, vp]
         lib.spec_attn_append_kv.restype = i32
         lib.spec_attn_append_kv.argtypes = [vp, vp, vp] + cache_args + [vp, sz, vp]
@@ -289,6 +292,16 @@ def spec_attn_run_noalloc(plan: Plan, q, k_pool, v_pool, block_table, seq_lens, 
     args = _run_args(plan, q, k_pool, v_pool, block_table, seq_lens, q_indptr, o, lse, k_scales,
                      v_scales, k_gscale, v_gscale)
     _check(lib.spec_attn_run_noalloc(*args, _stream_handle(stream)), "spec_attn_run_noalloc")
+
+
+def spec_attn_noalloc_check_device_status(stream=None) -> int:
+    """Device-status bits the last spec_attn_run_noalloc call on the current
+    device left (and clear them); 0 means no device check tripped."""
+    bits = ctypes.c_uint32()
+    st = load_library().spec_attn_noalloc_check_device_status(_stream_handle(stream), ctypes.byref(bits))
+    if st not in (SPEC_ATTN_OK, SPEC_ATTN_E_DEVICE_CHECK):
+        _check(st, "spec_attn_noalloc_check_device_status")
+    return int(bits.value)
 
 
 def _cache_args(plan, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,

@@ -60,9 +60,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile every CUDA source and link the shared library; return its path."""
     os.makedirs(BUILD, exist_ok=True)
     deps = _deps()
-    if not force and not extra_flags and not _stale(LIB, deps):
-        return LIB
     srcs = sources()
+    # the library is also stale when a source was added or removed since it was linked
+    stamp = os.path.join(BUILD, "sources.txt")
+    listing = "\n".join(os.path.basename(s) for s in srcs)
+    same_set = os.path.exists(stamp) and open(stamp).read() == listing
+    if not force and not extra_flags and same_set and not _stale(LIB, deps):
+        return LIB
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         results = list(ex.map(lambda s: _compile(s, extra_flags), srcs))
     objs = [o for o, _ in results]
@@ -76,6 +80,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
     os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(listing)
     return LIB
 
 

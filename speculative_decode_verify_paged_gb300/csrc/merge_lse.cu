@@ -9,25 +9,28 @@
 //   lse = log2 sum_s 2^(lse_s),  O = sum_s 2^(lse_s - lse) O_s,
 // written as bf16 O (round to nearest even) and natural-log LSE (lse * ln 2).
 //
-// Work layout.  A thread owns 8 consecutive output elements (two float4) of one
-// (window row, query head) pair and the splits g, g + SG, g + 2 SG, ... of it,
-// where SG (split groups) is chosen at launch so that a thread has at most
-// kBatch splits: all its loads (LSE and partial rows) are issued at once, one
-// memory round trip, and folded with a running maximum (online LSE
-// combination).  A 256-thread CTA covers 256 / (D/8 * SG) pairs, so short
-// split counts pack many pairs per CTA.  Groups are combined once through
-// shared memory.  Requests with a single split were finished by the split
-// kernel and are skipped, except in W-invariant mode, where every request is
-// merged and SG is the largest the CTA allows for D, a constant.  Split s
-// (counted from key 0, also when a sliding window lets the request's splits
-// start later) then always lands in group s mod SG, each group folds its
-// splits in ascending order and the groups are combined in group order, so
-// the sum order of a (row, head) pair never depends on the split count: a
-// row that sees fewer keys than its request's last row only has splits with
-// lse = -inf, which every fold step skips.  The kernel may be launched as a programmatic
-// dependent of the split kernel: it waits on griddepcontrol before touching
-// partials, and it lets the next kernel in the stream launch early (that
-// kernel waits for this grid's completion before reading its outputs).
+// Work layout.  The unit of work is one 8-element chunk of one (window row,
+// query head) pair: chunk u of a (KV head, request) block of partials, in the
+// partials' own chunk-major order (partial_chunk), so consecutive units are
+// consecutive 16-byte chunks.  A thread owns one unit and the splits g, g + SG,
+// g + 2 SG, ... of it, where SG (split groups) is chosen at launch so that a
+// thread has at most kBatch splits: all its loads (LSE and partial chunks) are
+// issued at once, one memory round trip, and folded with a running maximum
+// (online LSE combination).  A 256-thread CTA covers 256 / SG consecutive
+// units of one block (consecutive threads, consecutive chunks: coalesced), and
+// its SG groups are combined once through shared memory.  Requests with a
+// single split were finished by the split kernel and are skipped, except in
+// W-invariant mode, where every request is merged and SG is the largest the
+// CTA allows for D, a constant.  Split s (counted from key 0, also when a
+// sliding window lets the request's splits start later) then always lands in
+// group s mod SG, each group folds its splits in ascending order and the
+// groups are combined in group order, so the sum order of a (row, head) pair
+// never depends on the split count: a row that sees fewer keys than its
+// request's last row only has splits with lse = -inf, which every fold step
+// skips.  The kernel may be launched as a programmatic dependent of the split
+// kernel: it waits on griddepcontrol before touching partials, and it lets
+// the next kernel in the stream launch early (that kernel waits for this
+// grid's completion before reading its outputs).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,19 +44,15 @@ constexpr int kBatch = 5;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const MergeParams p, const int sg) {
-    constexpr int VEC = D / 8;                  // 8-float slices per row
+    constexpr int VEC = D / 8;                  // 8-element chunks per row
     __shared__ float4 part[kMergeThreads][2];
     __shared__ float part_m[kMergeThreads], part_l[kMergeThreads];
     const int tid = threadIdx.x;
     pdl_launch_dependents();
-    const int tpp = VEC * sg;                    // threads per pair
-    const int ppc = kMergeThreads / tpp;         // pairs per CTA
-    const int lp = tid / tpp, within = tid % tpp;
-    const int g = within / VEC, v = within % VEC;
-    const int pair = blockIdx.x * ppc + lp;
-    const int r = blockIdx.y;
-    const int i = pair / p.num_q_heads;
-    const int h = pair % p.num_q_heads;
+    const int upc = kMergeThreads / sg;         // units per CTA
+    const int g = tid / upc, lu = tid % upc;
+    const int kvh = blockIdx.y, r = blockIdx.z;
+    const int G = p.group;
 
     ReqInfo ri;
     bool req_ok;
@@ -68,18 +67,19 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
         req_ok = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len, p.bt_capacity_keys,
                               p.keys_per_split, nullptr, ri);
     }
-    const bool active = lp < ppc && req_ok && i < ri.w && (ri.nsplits > 1 || p.w_invariant);
+    // unit u of the request's (KV head) block: chunk c of row m (partial_chunk order)
+    const int rows = req_ok ? ri.w * G : 0;
+    const int u = blockIdx.x * upc + lu;
+    const bool active = req_ok && u < rows * VEC && (ri.nsplits > 1 || p.w_invariant);
+    const int c = active ? u / rows : 0, m = active ? u % rows : 0;
     // Wait for the split kernel's partials (no-op without a programmatic edge).
     pdl_wait_primary();
 
     float m_run = -INFINITY, l_run = 0.f;
     float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-    size_t oi = 0;
     if (active) {
-        oi = (size_t)(ri.row0 + i) * p.num_q_heads + h;
         const size_t split_stride = (size_t)p.total_rows * p.num_q_heads;
-        const size_t pair0 = partial_pair(0, p.total_rows, p.num_q_heads, p.group, h / p.group, ri.row0 + i,
-                                          h % p.group);
+        const size_t blk0 = partial_pair(0, p.total_rows, p.num_q_heads, G, kvh, ri.row0, 0);
         const int n = ri.nsplits;
         for (int s0 = first; s0 < n; s0 += sg * kBatch) {
             float ls[kBatch], sc[kBatch];
@@ -88,10 +88,10 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
             for (int k = 0; k < kBatch; ++k) {
                 const int s = s0 + k * sg;
                 if (s < n) {
-                    const float2 lsc = p.ws_ls[s * split_stride + pair0];
+                    const float2 lsc = p.ws_ls[s * split_stride + blk0 + m];
                     ls[k] = lsc.x;
                     sc[k] = lsc.y;
-                    hv[k] = *reinterpret_cast<const uint4*>(p.ws_o + (s * split_stride + pair0) * D + v * 8);
+                    hv[k] = *reinterpret_cast<const uint4*>(p.ws_o + (s * split_stride + blk0) * D + (size_t)u * 8);
                 } else {
                     ls[k] = -INFINITY;
                 }
@@ -102,9 +102,9 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
                 float4 o0, o1;
                 {
                     const float2 a = unpack_half2(hv[k].x), b = unpack_half2(hv[k].y);
-                    const float2 c = unpack_half2(hv[k].z), d = unpack_half2(hv[k].w);
+                    const float2 cc = unpack_half2(hv[k].z), d = unpack_half2(hv[k].w);
                     o0 = make_float4(a.x * sc[k], a.y * sc[k], b.x * sc[k], b.y * sc[k]);
-                    o1 = make_float4(c.x * sc[k], c.y * sc[k], d.x * sc[k], d.y * sc[k]);
+                    o1 = make_float4(cc.x * sc[k], cc.y * sc[k], d.x * sc[k], d.y * sc[k]);
                 }
                 if (ls[k] > m_run) {
                     const float a = fast_exp2(m_run - ls[k]);   // 0 while m_run is -inf
@@ -128,13 +128,12 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
     part_l[tid] = l_run;
     __syncthreads();
     if (!active || g != 0) return;
-    const int base = lp * tpp + v;               // thread of group k: base + k * VEC
     float mx = -INFINITY;
-    for (int k = 0; k < sg; ++k) mx = fmaxf(mx, part_m[base + k * VEC]);
+    for (int k = 0; k < sg; ++k) mx = fmaxf(mx, part_m[lu + k * upc]);
     float4 t0 = make_float4(0.f, 0.f, 0.f, 0.f), t1 = t0;
     float wsum = 0.f;
     for (int k = 0; k < sg; ++k) {
-        const int j = base + k * VEC;
+        const int j = lu + k * upc;
         if (part_m[j] == -INFINITY) continue;
         const float a = fast_exp2(part_m[j] - mx);
         const float4 q0 = part[j][0], q1 = part[j][1];
@@ -148,8 +147,9 @@ __global__ void __launch_bounds__(kMergeThreads, 3) merge_lse_kernel(const Merge
     out.y = float_to_bf16_bits(t0.z * inv) | ((uint32_t)float_to_bf16_bits(t0.w * inv) << 16);
     out.z = float_to_bf16_bits(t1.x * inv) | ((uint32_t)float_to_bf16_bits(t1.y * inv) << 16);
     out.w = float_to_bf16_bits(t1.z * inv) | ((uint32_t)float_to_bf16_bits(t1.w * inv) << 16);
-    *reinterpret_cast<uint4*>(p.o + oi * D + v * 8) = out;
-    if (p.lse && v == 0) p.lse[oi] = (mx + log2f(wsum)) * kLn2;
+    const size_t oi = (size_t)(ri.row0 + m / G) * p.num_q_heads + kvh * G + m % G;
+    *reinterpret_cast<uint4*>(p.o + oi * D + c * 8) = out;
+    if (p.lse && c == 0) p.lse[oi] = (mx + log2f(wsum)) * kLn2;
 }
 
 }  // namespace
@@ -160,9 +160,9 @@ cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool program
     if (sg < 1) sg = 1;
     if (sg > kMergeThreads / vec) sg = kMergeThreads / vec;
     if (p.w_invariant) sg = kMergeThreads / vec;   // a constant of D: the fold order is fixed
-    const int ppc = kMergeThreads / (vec * sg);
-    const int pairs = p.max_w * p.num_q_heads;
-    dim3 grid((pairs + ppc - 1) / ppc, p.num_reqs, 1);
+    const int upc = kMergeThreads / sg;            // units per CTA
+    const int chunks = p.max_w * p.group * vec;    // of the largest (KV head, request) block
+    dim3 grid((chunks + upc - 1) / upc, p.num_kv_heads, p.num_reqs);
     dim3 block(kMergeThreads, 1, 1);
     void (*k)(const MergeParams, const int) = nullptr;
     switch (p.head_dim) {

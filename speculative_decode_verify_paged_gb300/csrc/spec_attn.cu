@@ -354,12 +354,12 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     plan->grid = dim3(static_cast<unsigned>(plan->max_splits * plan->row_groups),
                       static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(std::max(1, p.num_reqs)));
 
-    // ---- workspace layout: [status 256 B][(lse, scale) partials][fp16 O partials] ----
-    plan->ws_ls_off = kStatusBytes;
+    // ---- workspace layout: [status region][(lse, scale) partials][fp16 O partials] ----
     size_t ws = kStatusBytes;
+    plan->ws_ls_off = ws;
     if (plan->uses_merge) {
         const size_t pairs = static_cast<size_t>(p.total_q_rows) * p.num_q_heads;
-        ws = align_up(plan->ws_ls_off + static_cast<size_t>(plan->max_splits) * pairs * 2 * sizeof(float), 256);
+        ws = align_up(ws + static_cast<size_t>(plan->max_splits) * pairs * 2 * sizeof(float), 256);
         plan->ws_o_off = ws;
         ws += static_cast<size_t>(plan->max_splits) * pairs * p.head_dim * sizeof(uint16_t);
     } else {
@@ -490,7 +490,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
                     const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr,
                     void* o, float* lse, int64_t* trace, void* workspace, size_t workspace_bytes,
                     spec_attn_stream_t stream_handle, const void* block_k = nullptr,
-                    const void* block_v = nullptr) {
+                    const void* block_v = nullptr, bool clear_status = false) {
     if (!plan) return SPEC_ATTN_E_INVALID_ARG;
     const spec_attn_problem& p = plan->prob;
     // a dense-block plan runs only with its block tensors, and they need such a plan
@@ -503,6 +503,11 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     if (chk != SPEC_ATTN_OK) return chk;
     cudaError_t e = cudaSuccess;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    if (clear_status) {
+        // only once every host check has passed: a rejected call writes nothing
+        e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     SplitParams sp;
@@ -554,6 +559,30 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.block_k = static_cast<const uint16_t*>(block_k);
     sp.block_v = static_cast<const uint16_t*>(block_v);
 
+    MergeParams mprm;
+    std::memset(&mprm, 0, sizeof(mprm));
+    mprm.seq_lens = seq_lens;
+    mprm.q_indptr = q_indptr;
+    mprm.ws_o = sp.ws_o;
+    mprm.ws_ls = sp.ws_ls;
+    mprm.o = sp.o;
+    mprm.lse = lse;
+    mprm.num_reqs = p.num_reqs;
+    mprm.total_rows = p.total_q_rows;
+    mprm.max_w = p.max_w;
+    mprm.num_q_heads = p.num_q_heads;
+    mprm.num_kv_heads = p.num_kv_heads;
+    mprm.group = p.num_q_heads / p.num_kv_heads;
+    mprm.head_dim = p.head_dim;
+    mprm.keys_per_split = plan->keys_per_split;
+    mprm.max_splits = plan->max_splits;
+    mprm.max_seq_len = p.max_seq_len;
+    mprm.bt_capacity_keys = p.block_table_stride * p.page_size;
+    mprm.w_invariant = plan->w_invariant ? 1 : 0;
+    mprm.window_left = p.window_left;
+    mprm.split_align = plan->split_align;
+    mprm.dense_block = p.dense_block_kv;
+
     spec_attn_plan* mp = const_cast<spec_attn_plan*>(plan);
     std::unique_lock<std::mutex> maps_lock(mp->maps_mutex, std::defer_lock);
     if (plan->variant == SPEC_ATTN_VARIANT_TCGEN05) {
@@ -589,35 +618,27 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (plan->uses_merge) {
-        MergeParams mp;
-        std::memset(&mp, 0, sizeof(mp));
-        mp.seq_lens = seq_lens;
-        mp.q_indptr = q_indptr;
-        mp.ws_o = sp.ws_o;
-        mp.ws_ls = sp.ws_ls;
-        mp.o = sp.o;
-        mp.lse = lse;
-        mp.num_reqs = p.num_reqs;
-        mp.total_rows = p.total_q_rows;
-        mp.max_w = p.max_w;
-        mp.num_q_heads = p.num_q_heads;
-        mp.group = p.num_q_heads / p.num_kv_heads;
-        mp.head_dim = p.head_dim;
-        mp.keys_per_split = plan->keys_per_split;
-        mp.max_splits = plan->max_splits;
-        mp.max_seq_len = p.max_seq_len;
-        mp.bt_capacity_keys = p.block_table_stride * p.page_size;
-        mp.w_invariant = plan->w_invariant ? 1 : 0;
-        mp.window_left = p.window_left;
-        mp.split_align = plan->split_align;
-        mp.dense_block = p.dense_block_kv;
         // programmatic launch lets the merge's CTAs become resident while the
         // split kernel drains; it is skipped when a timing event sits between.
-        e = merge_launch(mp, stream, plan->ev_end == nullptr);
+        e = merge_launch(mprm, stream, plan->ev_end == nullptr);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return SPEC_ATTN_OK;
 }
+
+}  // extern "C"
+
+namespace spec_attn {
+int run_clearing_status(const spec_attn_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                        const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
+                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return run_impl(plan, q, k_pool, v_pool, k_scales, v_scales, k_gscale, v_gscale, block_table, seq_lens,
+                    q_indptr, o, lse, nullptr, workspace, workspace_bytes, stream, nullptr, nullptr, true);
+}
+}  // namespace spec_attn
+
+extern "C" {
 
 int spec_attn_run(const spec_attn_plan* plan, const void* q, const void* k_pool, const void* v_pool,
                   const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,

@@ -6,7 +6,34 @@
 #include <stddef.h>
 #include <stdint.h>
 
+struct spec_attn_plan;   // the public ABI's opaque plan (spec_attn.cu)
+
 namespace spec_attn {
+
+// Everything the LSE merge of split partials needs (merge_lse.cu).
+struct MergeParams {
+    const int32_t* seq_lens;
+    const int32_t* q_indptr;
+    const uint16_t* ws_o;
+    const float2* ws_ls;
+    uint16_t* o;
+    float* lse;
+    int num_reqs;
+    int total_rows;
+    int max_w;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                  // Hq / Hkv
+    int head_dim;
+    int keys_per_split;
+    int max_splits;
+    long long max_seq_len;
+    int bt_capacity_keys;       // bt_stride * page_size
+    int w_invariant;            // merge every request (one split too), splits folded in order
+    int window_left;            // as SplitParams
+    int split_align;
+    int dense_block;
+};
 
 // Everything one split-KV launch needs.  Plain pointers and ints only.
 struct SplitParams {
@@ -56,28 +83,7 @@ struct SplitParams {
     const uint16_t* block_v;
 };
 
-struct MergeParams {
-    const int32_t* seq_lens;
-    const int32_t* q_indptr;
-    const uint16_t* ws_o;
-    const float2* ws_ls;
-    uint16_t* o;
-    float* lse;
-    int num_reqs;
-    int total_rows;
-    int max_w;
-    int num_q_heads;
-    int group;                  // Hq / Hkv
-    int head_dim;
-    int keys_per_split;
-    int max_splits;
-    long long max_seq_len;
-    int bt_capacity_keys;       // bt_stride * page_size
-    int w_invariant;            // merge every request (one split too), splits folded in order
-    int window_left;            // as SplitParams
-    int split_align;
-    int dense_block;
-};
+
 
 // Everything one KV-append launch needs (append_kv.cu).
 struct AppendParams {
@@ -115,11 +121,20 @@ struct AppendParams {
 //
 // Order of the (window row, query head) pairs in the split partials: split-major,
 // then KV head, then window row, then the G query heads of that KV head.  The
-// pairs one split CTA produces (one KV head, consecutive window rows) are one
-// contiguous block, so its epilogue writes a single dense run of memory.
+// W_r x G pairs of one (split, KV head, request) form one contiguous block;
+// the (lse, scale) pairs follow this order directly.
 __host__ __device__ __forceinline__ size_t partial_pair(int split, int total_rows, int num_q_heads, int group,
                                                         int kvh, int row, int g) {
     return (size_t)split * total_rows * num_q_heads + ((size_t)kvh * total_rows + row) * group + g;
+}
+
+// The fp16 values of such a block (rows x d, rows = W_r x G, row m = window row
+// x G + head) are stored chunk-major: element offset, from the block's start
+// (partial_pair of its first pair, times d), of the 8-element chunk c of row m.
+// Consecutive rows of one chunk are adjacent, so a warp holding 32 rows writes
+// (and the merge reads) 512 contiguous bytes per chunk.
+__host__ __device__ __forceinline__ size_t partial_chunk(int c, int rows, int m) {
+    return ((size_t)c * rows + m) * 8;
 }
 
 // Device-status bits (mirror the public SPEC_ATTN_DEV_* values).
@@ -166,6 +181,15 @@ cudaError_t tc_launch(const SplitParams& p, int kv_dtype, const TcMaps& maps, bo
 
 // ---- LSE merge (merge_lse.cu) ----
 cudaError_t merge_launch(const MergeParams& p, cudaStream_t stream, bool programmatic);
+
+// ---- no-alloc entry point (spec_attn_noalloc.cu) ----
+// spec_attn_run that, once every host check has passed, first zeroes the
+// workspace's device-status word on `stream` (the built-in scratch is shared
+// by every call, so each call starts from a clean word).
+int run_clearing_status(const ::spec_attn_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                        const void* k_scales, const void* v_scales, float k_gscale, float v_gscale,
+                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_indptr, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 // ---- KV append (append_kv.cu) ----
 // Always a programmatic dependent of the previous kernel in the stream (the

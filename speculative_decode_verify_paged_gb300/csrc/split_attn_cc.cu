@@ -380,7 +380,12 @@ split_attn_cc_kernel(const SplitParams p, const int stages) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
             const float sc = amax > 0.f ? inv_l / amax : 0.f;
-            uint32_t* wp = reinterpret_cast<uint32_t*>(p.ws_o + pi * D + lane * DPL);
+            // this lane's DPL values: elements lane * DPL .. of the row, inside
+            // chunk lane * DPL / 8 of the request's chunk-major block
+            const int rtot = ri.w * G, mg = (qrow[t] - ri.row0) * G + (hq[t] - kvh * G);
+            uint32_t* wp = reinterpret_cast<uint32_t*>(
+                p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0, 0) * D +
+                partial_chunk(lane * DPL / 8, rtot, mg) + (lane * DPL) % 8);
 #pragma unroll
             for (int e = 0; e < DPL; e += 2) wp[e / 2] = pack_half2(o_acc[t][e] * sc, o_acc[t][e + 1] * sc);
             if (lane == 0) p.ws_ls[pi] = make_float2(lse2, amax);

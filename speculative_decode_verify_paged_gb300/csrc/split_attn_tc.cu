@@ -55,19 +55,14 @@
 
 #include "common.cuh"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace spec_attn {
 
 namespace {
 
 using namespace sm100;
-
-// A 32-bit global load the compiler keeps in program order (not sunk past later loads).
-__device__ __forceinline__ int ld_volatile_i32(const int32_t* p) {
-    int v;
-    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
+using namespace tcc;
 
 constexpr int kBN = 64;        // keys per tile (a multiple of the 16-key unit; 32 or 64)
 constexpr int kPPT = kBN / 16;  // pages per tile
@@ -75,33 +70,30 @@ static_assert(kBN == 32 || kBN == 64, "tile");
 constexpr int kM = 128;        // MMA rows (query tile, padded)
 constexpr int kTcThreadsBf16 = 256;   // warps 0-7
 constexpr int kTcThreadsFp4 = 512;    // + warps 8-11 (K dequant) and 12-15 (V dequant)
-constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM cycles
-constexpr long long kDrainLimit = 200000000LL;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units: rescale when max grows by > 2^8
-constexpr int kPageListCap = 64;                 // page ids staged in shared memory at a time (2 per lane)
-constexpr int kNoPrefetch = INT_MIN;             // the producer fetches its first page ids itself
 constexpr int kMaxNR = 8;                        // NVFP4 raw (codes + scales) ring slots
 constexpr int kMaxNK = 8, kMaxNV = 16;
 
-// Shared memory: [P tile] | K ring | V ring | [NVFP4 raw ring] | barriers.
+// Shared memory: K ring | V ring | [NVFP4 raw ring] | barriers.
 // The query tile lands (bf16, by TMA) in the V slots before any V does; the
 // softmax warps move it into TMEM (NVFP4: converted to fp16), where the
 // S = Q K^T MMA reads its A operand.  An MMA with its A operand in TMEM issues
 // at about twice the rate of one reading it from shared memory, and the
-// 128-row tile costs no shared memory or shared-memory bandwidth.
-// bf16 KV: K and V arrive by TMA into rings of kNK / kNV slots; P (bf16) is an
-// A operand in shared memory.
+// 128-row tile costs no shared memory or shared-memory bandwidth.  P goes to
+// TMEM as well, where the P V MMA reads it as its A operand.
+// bf16 KV: K and V arrive by TMA into rings of kNK / kNV slots; P (bf16) takes
+// the first half of the S buffer it was computed from.  The CTA keeps below
+// 200 KB of shared memory, so that a CTA of the kernel that follows in the
+// stream (the LSE merge: 10 KB) can become resident beside it.
 // NVFP4 KV: codes and scales arrive by TMA into a ring of kNR raw slots and are
-// decoded into fp16 K and V operand tiles (two slots each); P (fp16) is
-// written to TMEM, where the P V MMA reads it.
+// decoded into fp16 K and V operand tiles (two slots each); P (fp16) has a
+// double buffer of its own in TMEM.
 template <int D, int KV>
 struct TcLayout {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along head_dim
     static constexpr int kQBytes = kM * D * 2;             // the query tile (16-bit elements)
     static constexpr int kQSmem = 0;                       // no region of its own: it lands in the V slots
-    // P: two tiles (double buffer).  32-key tiles share each 128-byte swizzle row
-    // (one half each); 64-key tiles fill a row, so the buffers are separate.
-    static constexpr int kPBytes = KV ? 0 : kM * 128 * (kBN == 64 ? 2 : 1);
+    static constexpr int kPBytes = 0;                      // P lives in TMEM
     static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile (16-bit elements)
     static constexpr int kPageBytes = 16 * D * 2;          // one 16-key unit of V (16-bit elements)
     // NVFP4 raw slot: the codes and scales of a tile's 16-key units, K then V.
@@ -117,7 +109,7 @@ struct TcLayout {
     static constexpr int kRawTile = 2 * kPPT * (kRawCodePage + kRawScalePage);
     static_assert(kRawCodePage % 128 == 0 && kRawScalePage % 128 == 0, "TMA destinations on 128 B");
     static constexpr int kAuxBytes = 1536;
-    static constexpr int kMaxDyn = 232448;                  // 227 KB opt-in limit
+    static constexpr int kMaxDyn = KV ? 232448 : 204800;    // 227 KB opt-in limit; bf16: 200 KB
     static constexpr int kFixed = 1024 + kQSmem + kPBytes + kAuxBytes;
     static constexpr int kRing = (kMaxDyn - kFixed) / kTileBytes;
     // bf16: the ring is split evenly: every tile needs its K and its V, and
@@ -128,12 +120,13 @@ struct TcLayout {
     static constexpr int kRawFit = (kMaxDyn - kFixed - (kNK + kNV) * kTileBytes) / kRawTile;
     static constexpr int kNR = KV ? (kRawFit > kMaxNR ? kMaxNR : kRawFit) : 0;
     static constexpr int kSmem = kFixed + (kNK + kNV) * kTileBytes + kNR * kRawTile;
-    // TMEM columns.  bf16: O [0, D), S double buffer [D, D + 2 BN), query tile
-    // (bf16 pairs) [D + 2 BN, D + 2 BN + D / 2).  NVFP4: O [0, D), S single
-    // buffer [D, D + BN), P double buffer (fp16 pairs) [D + BN, D + 2 BN),
-    // query tile (fp16 pairs) [D + 2 BN, D + 2 BN + D / 2).
+    // TMEM columns.  bf16: O [0, D), S double buffer [D, D + 2 BN) with P_b
+    // (bf16 pairs) in the first BN / 2 columns of S buffer b, query tile (bf16
+    // pairs) [D + 2 BN, D + 2 BN + D / 2).  NVFP4: O [0, D), S single buffer
+    // [D, D + BN), P double buffer (fp16 pairs) [D + BN, D + 2 BN), query tile
+    // (fp16 pairs) [D + 2 BN, D + 2 BN + D / 2).
     static constexpr int kSBufs = KV ? 1 : 2;
-    static constexpr int kPCol = D + kBN;
+    __host__ __device__ static constexpr int p_col(int b) { return KV ? D + kBN + b * (kBN / 2) : D + b * kBN; }
     static constexpr int kQCol = D + 2 * kBN;
     static constexpr int kTmemNeed = D + 2 * kBN + D / 2;
     static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128u : (kTmemNeed <= 256 ? 256u : 512u);
@@ -141,10 +134,9 @@ struct TcLayout {
     static_assert(kSmem <= kMaxDyn, "shared memory");
     static_assert(kTmemNeed <= 512, "tensor memory");
     static_assert(kQBytes <= kNV * kTileBytes, "the query tile lands in the V slots");
-    // the epilogue stages kM rows of fp32 O (+16 B padding) and kM row scales
-    // over the query/P/operand/raw buffers (all idle by then)
-    static_assert(kM * (D * 4 + 16) + kM * 4 <= kQSmem + kPBytes + (kNK + kNV) * kTileBytes + kNR * kRawTile,
-                  "epilogue staging");
+    // the final-output epilogue stages kM rows of bf16 O (+16 B padding), the
+    // partials epilogue 3 x kM floats, over the operand/raw buffers (idle by then)
+    static_assert(kM * (D * 2 + 16) <= (kNK + kNV) * kTileBytes + kNR * kRawTile, "epilogue staging");
 };
 
 struct TcAux {
@@ -153,9 +145,9 @@ struct TcAux {
     uint64_t v_full[kMaxNV];
     uint64_t v_empty[kMaxNV];
     uint64_t s_full[2];
-    uint64_t s_empty[2];
+    uint64_t s_empty[2];   // bf16: P V of the tile has read P from the buffer; NVFP4: S read
     uint64_t p_full[2];
-    uint64_t p_free[2];
+    uint64_t p_free[2];    // NVFP4: P V has read P buffer b
     uint64_t o_done;     // one phase per P V (rescale waits: at most one phase behind)
     uint64_t o_final;    // one phase after the last P V (the epilogue's wait)
     uint64_t q_full;     // the query tile landed in the V slots (TMA bytes)
@@ -173,26 +165,6 @@ struct TcAux {
     int32_t list_v[kPageListCap];
 };
 static_assert(sizeof(TcAux) <= 1536, "aux region");
-
-// Byte offset of P buffer b as seen by the MMA descriptor (32-key tiles: the
-// second half of each 128-byte row; 64-key tiles: a separate 16 KB buffer).
-__device__ __forceinline__ uint32_t p_tile_offset(int b) {
-    return kBN == 32 ? static_cast<uint32_t>(b * 64) : static_cast<uint32_t>(b * kM * 128);
-}
-
-// Warp-uniform bounded wait (all 32 lanes leave together).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    const long long t0 = clock64();
-    while (true) {
-        const bool ok = mbar_try_wait(bar, parity);
-        if (__all_sync(kFullMask, ok)) return true;
-        const bool give_up = (*abort != 0) || (clock64() - t0 > kWaitLimit);
-        if (__any_sync(kFullMask, give_up)) {
-            *abort = 1;
-            return false;
-        }
-    }
-}
 
 // One producer warp streams one of K or V: block-table entries are fetched by
 // all 32 lanes at once (coalesced) into a shared-memory list, then lane 0
@@ -285,15 +257,6 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
     return issued;
 }
 
-// Position of 16-byte code chunk ch (of D / 32) within key sl's row of a page's
-// codes in the raw ring.  The TMA copies them with the 128/64/32-byte swizzle
-// of d = 256/128/64 (16-byte chunk index XOR address bits 7..9), which places
-// one chunk of 8 consecutive keys in 8 different 16-byte bank groups.
-template <int D>
-__device__ __forceinline__ int raw_code_chunk(int sl, int ch) {
-    return D == 256 ? (ch ^ (sl & 7)) : D == 128 ? (ch ^ ((sl >> 1) & 3)) : (ch ^ ((sl >> 2) & 1));
-}
-
 // NVFP4: one warp streams each tile's e2m1 codes and e4m3 scales, K and V, into
 // a raw ring slot by TMA: per 16-key unit one box of codes (16 keys x d/2
 // bytes, swizzled) and one of scales (d bytes), issued from 4 lanes per unit.
@@ -367,32 +330,6 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
     return issued;
 }
 
-// Decode of NVFP4 K/V into fp16 MMA operands.  cvt.rn.f16x2.e2m1x2 turns one
-// code byte (two e2m1 values, the low nibble into the low half) into an fp16
-// pair and cvt.rn.f16x2.e4m3x2 one scale byte into (s, s); the products (at most
-// 5 significant bits, magnitudes 2^-10 .. 2688) are exact in fp16.
-__device__ __forceinline__ uint32_t e4m3_pair_f16x2(uint32_t byte) {
-    uint32_t d;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(byte * 0x0101u)));
-    return d;
-}
-// 8 e2m1 codes (one 32-bit word) times the fp16 scale pair s2, as 4 fp16 pairs.
-__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t s2, uint32_t& o0, uint32_t& o1, uint32_t& o2,
-                                           uint32_t& o3) {
-    uint32_t a0, a1, a2, a3;
-    asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4; "
-        "cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1; "
-        "cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
-        : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-        : "r"(w));
-    const __half2 s = *reinterpret_cast<const __half2*>(&s2);
-    __half2 h;
-    h = __hmul2(*reinterpret_cast<const __half2*>(&a0), s); o0 = *reinterpret_cast<const uint32_t*>(&h);
-    h = __hmul2(*reinterpret_cast<const __half2*>(&a1), s); o1 = *reinterpret_cast<const uint32_t*>(&h);
-    h = __hmul2(*reinterpret_cast<const __half2*>(&a2), s); o2 = *reinterpret_cast<const uint32_t*>(&h);
-    h = __hmul2(*reinterpret_cast<const __half2*>(&a3), s); o3 = *reinterpret_cast<const uint32_t*>(&h);
-}
-
 // One dequant warpgroup (128 threads) decodes the K (IS_V false) or V codes of
 // each tile from the raw ring into the fp16 operand tile the MMA reads: K
 // chunk-major across the tile's keys, V page by page, 128-byte swizzled like
@@ -460,15 +397,6 @@ __device__ __forceinline__ void dequant(const SplitParams& p, int key_lo, int ke
     }
 }
 
-template <int NSLOT>
-__device__ __forceinline__ void drain_copies(uint64_t* full, int issued) {
-    // let every copy still in flight land before the CTA's shared memory goes away
-    for (int t = max(0, issued - NSLOT); t < issued; ++t) {
-        volatile int no_abort = 0;
-        mbar_wait(&full[t % NSLOT], (t / NSLOT) & 1, &no_abort, kDrainLimit);
-    }
-}
-
 template <int D, int KV, bool TRACE, bool RG>
 __global__ void __launch_bounds__(KV ? kTcThreadsFp4 : kTcThreadsBf16, 1)
 split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tmq,
@@ -488,8 +416,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char* sP = smem + L::kQSmem;
-    unsigned char* sK = sP + L::kPBytes;
+    unsigned char* sK = smem + L::kQSmem;
     unsigned char* sV = sK + NK * L::kTileBytes;
     unsigned char* sQ = sV;   // the query tile lands in the V slots, then moves to TMEM
     unsigned char* sRaw = sV + NV * L::kTileBytes;   // NVFP4 only
@@ -513,7 +440,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&aux->s_full[b], 1);
-            mbar_init(&aux->s_empty[b], 4);
+            mbar_init(&aux->s_empty[b], KV ? 4 : 1);
             mbar_init(&aux->p_full[b], 4);
             mbar_init(&aux->p_free[b], 1);
         }
@@ -586,6 +513,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     // tile: the window's own keys (ctx .. len - 1, from the block tensors)
     const int T = Tc + ((p.dense_block && split == ri.nsplits - 1) ? 1 : 0);
 
+    // the request is finished by this kernel (one split), or leaves split partials
+    const bool final_out = (ri.nsplits == 1) && !p.always_partials;
+    float ep_inv = 0.f, ep_lse2 = -INFINITY;   // softmax threads: 1 / l and log2-sum-exp of their row
+
     if (warp == 0) {
         // ------------------------------------------------------------ query tile + K producer
         if (lane == 0) {
@@ -635,7 +566,6 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         __syncwarp();
     } else if (KV && warp >= 8) {
         // ------------------------------------------------------------ NVFP4 dequant (K: 8-11, V: 12-15)
-        // e4m3 -> bf16 table for the block scales, from the format definition
         if (warp < 12)
             dequant<D, false, TRACE>(p, key_lo, key_hi, T, sRaw, sK, aux, abort, tid - 256);
         else
@@ -650,7 +580,6 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             // bf16 KV: bf16 operands
             constexpr uint32_t idesc_s = KV ? idesc_f16_f32(kM, kBN, 0, 0) : idesc_bf16_f32(kM, kBN, 0, 0);
             constexpr uint32_t idesc_o = KV ? idesc_f16_f32(kM, D, 0, 1) : idesc_bf16_f32(kM, D, 0, 1);
-            const uint32_t p_addr = smem_addr(sP);
             const bool pv_issuer = (warp == 3);
             bool ok = pv_issuer || mbar_wait(&aux->q_ready, 0, abort, kWaitLimit);
             tc_fence_after();
@@ -681,17 +610,12 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                     // V page kk: [chunk][16 keys][128 B]; MN atoms (64 head_dim
                     // elements) 2 KB apart, 8-key groups 1 KB apart
                     const uint64_t bd = smem_desc_sw128(v_addr + kk * L::kPageBytes, 2048, 1024);
-                    if constexpr (KV) {
-                        // P keys 16 kk .. 16 kk + 15: TMEM columns 8 kk .. 8 kk + 7 of buffer b
-                        mma_ts(tmem, tmem + L::kPCol + b * (kBN / 2) + kk * 8, bd, idesc_o,
-                                   (n > 0 || kk > 0) ? 1u : 0u);
-                    } else {
-                        const uint64_t a = smem_desc_sw128(p_addr + p_tile_offset(b) + kk * 32, 16, 1024);
-                        mma_bf16_ss(tmem, a, bd, idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    // P keys 16 kk .. 16 kk + 15: TMEM columns 8 kk .. 8 kk + 7 of buffer b
+                    mma_ts(tmem, tmem + L::p_col(b) + kk * 8, bd, idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&aux->v_empty[vs]);
-                mma_commit(&aux->p_free[b]);
+                // bf16: P sat in S buffer b, which the S MMA of tile n + 2 may now overwrite
+                mma_commit(KV ? &aux->p_free[b] : &aux->s_empty[b]);
                 mma_commit(&aux->o_done);
             };
             long long t_idle = clock64();
@@ -783,7 +707,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&aux->s_empty[sb]);
+            // NVFP4: S is single-buffered and P has buffers of its own, so the
+            // next S may start now; bf16: P goes where S was, and the P V MMA
+            // frees the buffer
+            if (KV && lane == 0) mbar_arrive(&aux->s_empty[sb]);
 
             // tile t covers keys key0 .. key0 + 63 (the dense block tile: ctx .. ctx + W - 1)
             const bool block_tile = t >= Tc;
@@ -842,8 +769,9 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             l_sum = l_sum * alpha + psum;
             m_ref = ref;
 
-            // P half b was last read by PV_{t-2}
-            if (t >= 2 && !(ok = warp_wait(&aux->p_free[b], ((t >> 1) - 1) & 1, abort))) break;
+            // NVFP4: P buffer b was last read by PV_{t-2}.  (bf16: S_t, and so
+            // P_t, could only be written there after PV_{t-2} had finished.)
+            if (KV && t >= 2 && !(ok = warp_wait(&aux->p_free[b], ((t >> 1) - 1) & 1, abort))) break;
             if (__any_sync(kFullMask, need) && t > 0) {
                 // rescaling O needs every earlier P V finished
                 if (!(ok = warp_wait(&aux->o_done, (t - 1) & 1, abort))) break;
@@ -891,22 +819,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                                          : (long long)aux->pages_v[vs][c >> 4] * 16 + (key & 15);
                 }
             }
-            if constexpr (KV) {
-                // P row m (fp16 pairs, key 2c in the low half) into TMEM buffer b
-                static_assert(kBN == 64, "one 32-column store per P row");
-                tmem_st32u(lane_tmem + L::kPCol + b * (kBN / 2), pk);
-                tmem_wait_st();
-            } else {
-                // P row m into buffer b of the 128-byte-swizzled K-major A tile
-#pragma unroll
-                for (int j = 0; j < kBN / 8; ++j) {
-                    const int chunk = (kBN == 32 ? b * 4 : 0) + j;
-                    *reinterpret_cast<uint4*>(sP + (kBN == 64 ? b * (kM * 128) : 0) + m * 128 +
-                                              ((chunk ^ (m & 7)) << 4)) =
-                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                }
-                fence_proxy_async_smem();
-            }
+            // P row m (16-bit pairs, key 2c in the low half) into TMEM buffer b
+            static_assert(kBN == 64, "one 32-column store per P row");
+            tmem_st32u(lane_tmem + L::p_col(b), pk);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aux->p_full[b]);
@@ -915,60 +831,42 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         if (ok) ok = warp_wait(&aux->o_final, 0, abort);
         tc_fence_after();
         if (ok) {
-            // Every MMA and copy has completed (o_final), so the query, P and
-            // ring buffers are free: each thread stages its row of the
-            // normalised O there (bf16 output, or fp32 for a split partial,
-            // with the row's largest magnitude), row stride padded by 16 bytes
-            // so the 16-byte stores of a warp hit distinct banks.  All warps
-            // copy the rows out below.
-            const float inv = (valid && l_sum > 0.f) ? (p.out_scale / l_sum) : 0.f;
-            const float lse2 = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) : -INFINITY;
-            const bool final_out = (ri.nsplits == 1) && !p.always_partials;
-            const int rs = (final_out ? D * 2 : D * 4) + 16;
-            unsigned char* myrow = smem + m * rs;
-            float amax = 0.f;
-            // two 32-column TMEM loads in flight per wait
+            // Every MMA and copy has completed (o_final), so the ring buffers
+            // are free.  The row's normaliser and log-sum-exp go to the
+            // epilogue below; a request with a single split is finished here:
+            // each thread stages its row of bf16 O (row stride padded by 16
+            // bytes so the 16-byte stores of a warp hit distinct banks), which
+            // every warp then copies out.
+            ep_inv = (valid && l_sum > 0.f) ? (p.out_scale / l_sum) : 0.f;
+            ep_lse2 = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) : -INFINITY;
+            if (final_out && wq * 32 < R) {   // warps holding output rows only
+                unsigned char* myrow = smem + m * (D * 2 + 16);
+                // two 32-column TMEM loads in flight per wait
 #pragma unroll 1
-            for (int ch0 = 0; ch0 < D / 32; ch0 += 2) {
-                float ov[2][32];
-                tmem_ld32(lane_tmem + ch0 * 32, ov[0]);
-                tmem_ld32(lane_tmem + (ch0 + 1) * 32, ov[1]);
-                tmem_wait_ld();
+                for (int ch0 = 0; ch0 < D / 32; ch0 += 2) {
+                    float ov[2][32];
+                    tmem_ld32(lane_tmem + ch0 * 32, ov[0]);
+                    tmem_ld32(lane_tmem + (ch0 + 1) * 32, ov[1]);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int ch = ch0 + hh;
-                    if (final_out) {
+                    for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint32_t w[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[hh][q4 * 8 + 2 * e] * inv,
-                                                                                ov[hh][q4 * 8 + 2 * e + 1] * inv);
+                                const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                                    ov[hh][q4 * 8 + 2 * e] * ep_inv, ov[hh][q4 * 8 + 2 * e + 1] * ep_inv);
                                 w[e] = *reinterpret_cast<const uint32_t*>(&h2);
                             }
-                            *reinterpret_cast<uint4*>(myrow + ch * 64 + q4 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
-                            const float4 f = make_float4(ov[hh][q4 * 4] * inv, ov[hh][q4 * 4 + 1] * inv,
-                                                         ov[hh][q4 * 4 + 2] * inv, ov[hh][q4 * 4 + 3] * inv);
-                            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
-                            *reinterpret_cast<float4*>(myrow + ch * 128 + q4 * 16) = f;
+                            *reinterpret_cast<uint4*>(myrow + (ch0 + hh) * 64 + q4 * 16) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
             }
-            if (!final_out)   // 1 / scale of each staged row, after the rows
-                reinterpret_cast<float*>(smem + kM * rs)[m] = amax > 0.f ? 1.f / amax : 0.f;
             if (valid) {
-                if (final_out) {
-                    if (p.lse) p.lse[(size_t)qrow * p.num_q_heads + hq] = lse2 * kLn2;
-                } else {
-                    p.ws_ls[partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, qrow, m % G)] =
-                        make_float2(lse2, amax);
-                }
+                if (final_out && p.lse) p.lse[(size_t)qrow * p.num_q_heads + hq] = ep_lse2 * kLn2;
                 if (TRACE && p.trace) {
                     unsigned long long* tp =
                         reinterpret_cast<unsigned long long*>(p.trace + ((size_t)qrow * p.num_q_heads + hq) * 2);
@@ -980,80 +878,108 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    // Every role has finished, so the abort flag is final.  Nothing is written
+    // if any role gave up.
+    const bool ep_ok = (*abort == 0);
+    if (ep_ok && !final_out && warp < 8) {
+        // ------------------------------------------------------------ split partial (warps 0-7)
+        // Straight from TMEM to global memory, no staging: warp w reads TMEM
+        // lanes 32 (w % 4) .. + 31 (query rows), warps 4-7 the first half of
+        // the head_dim columns and warps 0-3 the second.  A partial is fp16 of
+        // O_s / scale_s with scale_s = max_e |O_s[e]| (the halves exchange
+        // their maxima through shared memory), stored chunk-major within the
+        // request's block of W_r x G rows (see partial_chunk), so that the 32
+        // rows of a warp fill 512 contiguous bytes per chunk.
         tc_fence_after();
-        tmem_dealloc(tmem, L::kTmemCols);
-    }
-    // ------------------------------------------------------------ copy-out (every thread)
-    // The staged rows leave in coalesced 16-byte pieces, several loads in
-    // flight per thread before their stores.  Split partials of this CTA are one
-    // dense block (rows m = window row * G + head, see partial_pair), written as
-    // fp16 of value / scale; bf16 output rows go to [row][head] with the G
-    // heads of a window row adjacent.  Nothing was staged if any role gave up
-    // (abort).
-    if (*abort == 0) {
-        constexpr int kBatchPieces = 8;
-        const int nt = blockDim.x;
-        const uint32_t sbase = smem_addr(smem);
-        if (ri.nsplits == 1 && !p.always_partials) {
-            constexpr int lg = (D == 64 ? 3 : D == 128 ? 4 : 5);   // 16-byte pieces per bf16 row
-            constexpr int rs = D * 2 + 16;
-            const int total = R << lg;
-            for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
-                uint4 v[kBatchPieces];
+        float* ep = reinterpret_cast<float*>(smem);   // [0, kM) 1 / l;  [kM, 3 kM) max |O| per half
+        const int mrow = (warp & 3) * 32 + lane;
+        const int half = warp < 4 ? 1 : 0;
+        if (warp >= 4) ep[mrow] = ep_inv;
+        named_barrier_sync(1, 256);
+        const bool rows_here = (warp & 3) * 32 < R;   // warp-uniform
+        const uint32_t taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + half * (D / 2);
+        const float inv = ep[mrow];
+        float amax = 0.f;
+        if (rows_here) {
+#pragma unroll 1
+            for (int ch = 0; ch < D / 64; ++ch) {
+                float ov[32];
+                tmem_ld32(taddr + ch * 32, ov);
+                tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < kBatchPieces; ++k) {
-                    const int u = u0 + k * nt;
-                    if (u < total) v[k] = ld_shared_v4(sbase + (u >> lg) * rs + (u & ((1 << lg) - 1)) * 16);
-                }
-#pragma unroll
-                for (int k = 0; k < kBatchPieces; ++k) {
-                    const int u = u0 + k * nt;
-                    if (u < total) {
-                        const int mm = u >> lg, c = u & ((1 << lg) - 1);
-                        unsigned char* dst = reinterpret_cast<unsigned char*>(p.o) +
-                                             (((size_t)(ri.row0 + w_lo + mm / G) * p.num_q_heads + kvh * G + mm % G) * D) * 2 +
-                                             c * 16;
-                        st_global_v4(dst, v[k]);
-                    }
-                }
+                for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(ov[e]));
             }
-        } else {
-            constexpr int lg = (D == 64 ? 3 : D == 128 ? 4 : 5);   // 8-value pieces per row
-            constexpr int rs = D * 4 + 16;
-            const int total = R << lg;
-            const float* rinv = reinterpret_cast<const float*>(smem + kM * rs);
-            unsigned char* blk = reinterpret_cast<unsigned char*>(
-                p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0 + w_lo, 0) * D);
-            for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
-                uint4 a[kBatchPieces], b[kBatchPieces];
-                float sc[kBatchPieces];
+            amax *= inv;
+        }
+        ep[kM * (1 + half) + mrow] = amax;
+        named_barrier_sync(1, 256);
+        if (rows_here) {
+            amax = fmaxf(ep[kM + mrow], ep[2 * kM + mrow]);
+            const float rsc = amax > 0.f ? inv / amax : 0.f;
+            const bool row_ok = mrow < R;
+            if (warp >= 4 && row_ok)
+                p.ws_ls[partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0 + w_lo + mrow / G,
+                                     mrow % G)] = make_float2(ep_lse2, amax);
+            uint16_t* blk = p.ws_o + partial_pair(split, p.total_rows, p.num_q_heads, G, kvh, ri.row0, 0) * D;
+            const int rtot = ri.w * G, mg = w_lo * G + mrow;   // the request's rows; this row among them
+#pragma unroll 1
+            for (int ch = 0; ch < D / 64; ++ch) {
+                float ov[32];
+                tmem_ld32(taddr + ch * 32, ov);
+                tmem_wait_ld();
+                if (row_ok) {
 #pragma unroll
-                for (int k = 0; k < kBatchPieces; ++k) {
-                    const int u = u0 + k * nt;
-                    if (u < total) {
-                        const uint32_t src = sbase + (u >> lg) * rs + (u & ((1 << lg) - 1)) * 32;
-                        a[k] = ld_shared_v4(src);
-                        b[k] = ld_shared_v4(src + 16);
-                        sc[k] = rinv[u >> lg];
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < kBatchPieces; ++k) {
-                    const int u = u0 + k * nt;
-                    if (u < total) {
+                    for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 h;
-                        h.x = pack_half2(__uint_as_float(a[k].x) * sc[k], __uint_as_float(a[k].y) * sc[k]);
-                        h.y = pack_half2(__uint_as_float(a[k].z) * sc[k], __uint_as_float(a[k].w) * sc[k]);
-                        h.z = pack_half2(__uint_as_float(b[k].x) * sc[k], __uint_as_float(b[k].y) * sc[k]);
-                        h.w = pack_half2(__uint_as_float(b[k].z) * sc[k], __uint_as_float(b[k].w) * sc[k]);
-                        st_global_v4(blk + (size_t)u * 16, h);
+                        h.x = pack_half2(ov[q4 * 8 + 0] * rsc, ov[q4 * 8 + 1] * rsc);
+                        h.y = pack_half2(ov[q4 * 8 + 2] * rsc, ov[q4 * 8 + 3] * rsc);
+                        h.z = pack_half2(ov[q4 * 8 + 4] * rsc, ov[q4 * 8 + 5] * rsc);
+                        h.w = pack_half2(ov[q4 * 8 + 6] * rsc, ov[q4 * 8 + 7] * rsc);
+                        const int c = half * (D / 16) + ch * 4 + q4;   // 8-element chunk of the row
+                        st_global_v4(blk + partial_chunk(c, rtot, mg), h);
                     }
                 }
             }
         }
-    } else if (tid == 0) {
-        atomicOr(p.status, kDevWaitTimeout);   // whichever role gave up, the call reports it
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+    if (!ep_ok) {
+        if (tid == 0) atomicOr(p.status, kDevWaitTimeout);   // whichever role gave up, the call reports it
+    } else if (final_out) {
+        // ------------------------------------------------------------ copy-out (every thread)
+        // The staged bf16 rows leave in coalesced 16-byte pieces, several
+        // loads in flight per thread before their stores, to [row][head] with
+        // the G heads of a window row adjacent.
+        constexpr int kBatchPieces = 8;
+        const int nt = blockDim.x;
+        const uint32_t sbase = smem_addr(smem);
+        constexpr int lg = (D == 64 ? 3 : D == 128 ? 4 : 5);   // 16-byte pieces per bf16 row
+        constexpr int rs = D * 2 + 16;
+        const int total = R << lg;
+        for (int u0 = tid; u0 < total; u0 += nt * kBatchPieces) {
+            uint4 v[kBatchPieces];
+#pragma unroll
+            for (int k = 0; k < kBatchPieces; ++k) {
+                const int u = u0 + k * nt;
+                if (u < total) v[k] = ld_shared_v4(sbase + (u >> lg) * rs + (u & ((1 << lg) - 1)) * 16);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatchPieces; ++k) {
+                const int u = u0 + k * nt;
+                if (u < total) {
+                    const int mm = u >> lg, c = u & ((1 << lg) - 1);
+                    unsigned char* dst = reinterpret_cast<unsigned char*>(p.o) +
+                                         (((size_t)(ri.row0 + w_lo + mm / G) * p.num_q_heads + kvh * G + mm % G) * D) * 2 +
+                                         c * 16;
+                    st_global_v4(dst, v[k]);
+                }
+            }
+        }
     }
 }
 
