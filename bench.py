@@ -144,8 +144,6 @@ def table_workloads():
             ("verify_w16_ctx16k_w_invariant", lambda: W.verify_sweep(16), {"w_invariant": 1}),
             ("verify_w1_ctx16k_w_invariant", lambda: W.verify_sweep(1), {"w_invariant": 1}),
             ("long_verify_w16_w_invariant", lambda: W.long_verify(16), {"w_invariant": 1}),
-            ("long_verify_w16_w_invariant_2048", lambda: W.long_verify(16),
-             {"w_invariant": 1, "fixed_keys_per_split": 2048}),
             ("verify_w16_ctx16k_run_append", lambda: W.verify_sweep(16), {"append": "run_append"}),
             ("nvfp4_run_append", W.nvfp4, {"append": "run_append"}),
             ("verify_w16_ctx16k_append_only", lambda: W.verify_sweep(16), {"append": "append"}),

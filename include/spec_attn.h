@@ -148,7 +148,8 @@ typedef struct spec_attn_problem {
     int32_t kernel_variant;      /* spec_attn_kernel_variant */
     int32_t w_invariant;         /* 1: W-invariant mode (below); 0: off */
     int32_t fixed_keys_per_split;/* W-invariant mode: keys per split, a multiple of 64
-                                    (0 selects 512); ignored otherwise */
+                                    (0 selects 64 x ceil(max_seq_len / 2048), at least
+                                    512); ignored otherwise */
     int32_t window_left;         /* causal sliding window in keys; 0 = none (required
                                     for the non-causal mask) */
     int64_t kv_page_stride;      /* bytes from a K (or V) page to the next: 0 = dense
@@ -193,7 +194,11 @@ typedef struct spec_attn_problem {
  * cost is the split count this fixes: one CTA per (split, KV head, request),
  * so the call is fastest when fixed_keys_per_split is near the typical
  * context length x P x Hkv / (number of SMs), e.g. 512 for one request with
- * 4 KV heads at 16K keys, 2048 at 64K.
+ * 4 KV heads at 16K keys, 2048 at 64K.  The default (0) derives it from
+ * max_seq_len (512 up to 16K keys, 2048 at 64K): plans that must agree
+ * bitwise with each other pass the same explicit value, or have max_seq_len
+ * values that round up to the same multiple of 2048 (or are both at most
+ * 16384).
  */
 
 typedef struct spec_attn_plan spec_attn_plan;   /* opaque */

@@ -78,7 +78,12 @@ size_t bytes_per_token_head(int kv_dtype, int d) {
 // Rough cost (microseconds) of one call with `c` keys per split.  Terms:
 //   waves of CTAs, each paying a fixed start/finish cost plus its keys at the
 //   per-CTA streaming (or compute) rate; the whole job can not beat HBM; and
-//   the merge reads every partial once more.
+//   the merge reads every partial once more.  Waves count the whole grid
+//   (max splits x KV heads x requests x row groups), not only the CTAs with
+//   work: the grid is laid out for the longest request, and a CTA of a shorter
+//   one past its last split still takes an SM for its prologue before it
+//   leaves, so blocks past the first wave start late even when the CTAs with
+//   work would fit in one.
 struct CostModel {
     double hbm_bytes_per_us = 6.5e6;   // ~6.5 TB/s
     double l2_bytes_per_us = 2.0e7;    // partials stay in L2
@@ -95,9 +100,8 @@ int choose_keys_per_split(const std::vector<int64_t>& lens, int64_t max_seq, int
     int best_c = static_cast<int>(max_units * kSplitUnit);
     for (int64_t u = 1; u <= max_units; ++u) {
         const int64_t c = u * kSplitUnit;
-        int64_t ctas = 0;
-        for (int64_t L : lens) ctas += static_cast<int64_t>(hkv) * row_groups * ((L + c - 1) / c);
         const int64_t splits = (max_seq + c - 1) / c;
+        const int64_t ctas = static_cast<int64_t>(lens.size()) * hkv * row_groups * splits;
         const int64_t waves = (ctas + slots - 1) / slots;
         const double t_cta = cm.cta_fixed_us + static_cast<double>(c) * cm.key_us;
         const double t_waves = static_cast<double>(waves) * t_cta;
@@ -285,7 +289,13 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
     // key_base = its first visible key rounded down to split_align (the key
     // tile, or the fixed split length in W-invariant mode); the lengths the
     // heuristic weighs are those spans.
-    const int fixed_kps = p.fixed_keys_per_split > 0 ? p.fixed_keys_per_split : 512;
+    // W-invariant default: about max_seq_len / 32 keys per split (a multiple of
+    // 64, at least 512), so that one request of the longest length fills the
+    // GPU with its KV heads' splits (512 at 16K keys, 2048 at 64K)
+    const int fixed_kps =
+        p.fixed_keys_per_split > 0
+            ? p.fixed_keys_per_split
+            : static_cast<int>(std::max<int64_t>(512, (p.max_seq_len + 2047) / 2048 * 64));
     plan->split_align = plan->w_invariant ? fixed_kps : kSplitUnit;
     // (dense block operand: the splits cover the cached context; the window's
     // own keys ride along in the last one)

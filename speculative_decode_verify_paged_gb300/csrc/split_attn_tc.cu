@@ -80,14 +80,14 @@ constexpr int kMaxNK = 8, kMaxNV = 16;
 // S = Q K^T MMA reads its A operand.  An MMA with its A operand in TMEM issues
 // at about twice the rate of one reading it from shared memory, and the
 // 128-row tile costs no shared memory or shared-memory bandwidth.  P goes to
-// TMEM as well, where the P V MMA reads it as its A operand.
-// bf16 KV: K and V arrive by TMA into rings of kNK / kNV slots; P (bf16) takes
-// the first half of the S buffer it was computed from.  The CTA keeps below
-// 200 KB of shared memory, so that a CTA of the kernel that follows in the
-// stream (the LSE merge: 10 KB) can become resident beside it.
+// TMEM as well, where the P V MMA reads it as its A operand: P (16-bit) takes
+// the first half of the S buffer it was computed from, and S is double
+// buffered, so the S MMA of tile t + 1 runs while the softmax works on tile t.
+// bf16 KV: K and V arrive by TMA into rings of kNK / kNV slots.  The CTA keeps
+// below 200 KB of shared memory, so that a CTA of the kernel that follows in
+// the stream (the LSE merge: 10 KB) can become resident beside it.
 // NVFP4 KV: codes and scales arrive by TMA into a ring of kNR raw slots and are
-// decoded into fp16 K and V operand tiles (two slots each); P (fp16) has a
-// double buffer of its own in TMEM.
+// decoded into fp16 K and V operand tiles (two slots each).
 template <int D, int KV>
 struct TcLayout {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along head_dim
@@ -120,13 +120,11 @@ struct TcLayout {
     static constexpr int kRawFit = (kMaxDyn - kFixed - (kNK + kNV) * kTileBytes) / kRawTile;
     static constexpr int kNR = KV ? (kRawFit > kMaxNR ? kMaxNR : kRawFit) : 0;
     static constexpr int kSmem = kFixed + (kNK + kNV) * kTileBytes + kNR * kRawTile;
-    // TMEM columns.  bf16: O [0, D), S double buffer [D, D + 2 BN) with P_b
-    // (bf16 pairs) in the first BN / 2 columns of S buffer b, query tile (bf16
-    // pairs) [D + 2 BN, D + 2 BN + D / 2).  NVFP4: O [0, D), S single buffer
-    // [D, D + BN), P double buffer (fp16 pairs) [D + BN, D + 2 BN), query tile
-    // (fp16 pairs) [D + 2 BN, D + 2 BN + D / 2).
-    static constexpr int kSBufs = KV ? 1 : 2;
-    __host__ __device__ static constexpr int p_col(int b) { return KV ? D + kBN + b * (kBN / 2) : D + b * kBN; }
+    // TMEM columns: O [0, D), S double buffer [D, D + 2 BN) with P_b (16-bit
+    // pairs: bf16, NVFP4 fp16) in the first BN / 2 columns of S buffer b, query
+    // tile (16-bit pairs) [D + 2 BN, D + 2 BN + D / 2).
+    static constexpr int kSBufs = 2;
+    __host__ __device__ static constexpr int p_col(int b) { return D + b * kBN; }
     static constexpr int kQCol = D + 2 * kBN;
     static constexpr int kTmemNeed = D + 2 * kBN + D / 2;
     static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128u : (kTmemNeed <= 256 ? 256u : 512u);
@@ -147,7 +145,6 @@ struct TcAux {
     uint64_t s_full[2];
     uint64_t s_empty[2];   // bf16: P V of the tile has read P from the buffer; NVFP4: S read
     uint64_t p_full[2];
-    uint64_t p_free[2];    // NVFP4: P V has read P buffer b
     uint64_t o_done;     // one phase per P V (rescale waits: at most one phase behind)
     uint64_t o_final;    // one phase after the last P V (the epilogue's wait)
     uint64_t q_full;     // the query tile landed in the V slots (TMA bytes)
@@ -440,9 +437,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&aux->s_full[b], 1);
-            mbar_init(&aux->s_empty[b], KV ? 4 : 1);
+            mbar_init(&aux->s_empty[b], 1);
             mbar_init(&aux->p_full[b], 4);
-            mbar_init(&aux->p_free[b], 1);
         }
         mbar_init(&aux->o_done, 1);
         mbar_init(&aux->o_final, 1);
@@ -615,7 +611,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                 }
                 mma_commit(&aux->v_empty[vs]);
                 // bf16: P sat in S buffer b, which the S MMA of tile n + 2 may now overwrite
-                mma_commit(KV ? &aux->p_free[b] : &aux->s_empty[b]);
+                mma_commit(&aux->s_empty[b]);
                 mma_commit(&aux->o_done);
             };
             long long t_idle = clock64();
@@ -705,12 +701,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             for (int h = 0; h < kBN / 32; ++h)
                 tmem_ld32(lane_tmem + D + sb * kBN + h * 32, *reinterpret_cast<float(*)[32]>(sv + h * 32));
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            // NVFP4: S is single-buffered and P has buffers of its own, so the
-            // next S may start now; bf16: P goes where S was, and the P V MMA
-            // frees the buffer
-            if (KV && lane == 0) mbar_arrive(&aux->s_empty[sb]);
+            // P goes where S was, and the P V MMA frees the buffer
 
             // tile t covers keys key0 .. key0 + 63 (the dense block tile: ctx .. ctx + W - 1)
             const bool block_tile = t >= Tc;
@@ -769,9 +760,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             l_sum = l_sum * alpha + psum;
             m_ref = ref;
 
-            // NVFP4: P buffer b was last read by PV_{t-2}.  (bf16: S_t, and so
-            // P_t, could only be written there after PV_{t-2} had finished.)
-            if (KV && t >= 2 && !(ok = warp_wait(&aux->p_free[b], ((t >> 1) - 1) & 1, abort))) break;
+            // (S_t, and so P_t, could only be written to buffer b once PV_{t-2}
+            // had finished with it)
             if (__any_sync(kFullMask, need) && t > 0) {
                 // rescaling O needs every earlier P V finished
                 if (!(ok = warp_wait(&aux->o_done, (t - 1) & 1, abort))) break;

@@ -130,15 +130,23 @@ class Workload:
 NVFP4_GSCALE = 0.3          # decode scale of both drawn tensors: element RMS ~ 1
 
 
-def _draw_nvfp4(lead_shape, d: int, gen: torch.Generator):
+NVFP4_SCALE_BYTES = (0x30, 0x40)     # default block-scale bytes: e4m3 0.5 .. 1.875
+NVFP4_SCALE_BYTES_FULL = (0x00, 0x7F)  # every non-negative finite e4m3 byte: 0, the
+                                       # subnormals 2^-9 .. 7 x 2^-9, normals up to 448
+
+
+def _draw_nvfp4(lead_shape, d: int, gen: torch.Generator, scale_bytes=NVFP4_SCALE_BYTES):
     """Random NVFP4 cache contents: codes uint8 [*lead_shape, d/2] (two
     independent uniform 4-bit codes per byte) and e4m3 block-scale bytes
-    [*lead_shape, d/16] drawn uniformly from 0x30..0x3F (values 0.5 .. 1.875).
-    Drawn rather than quantised, so this module holds no quantiser; with the
-    decode scale NVFP4_GSCALE the elements have an RMS near 1, like the bf16
-    pools' N(0, 1)."""
+    [*lead_shape, d/16] drawn uniformly from [scale_bytes[0], scale_bytes[1])
+    (by default 0x30..0x3F, values 0.5 .. 1.875).  Drawn rather than
+    quantised, so this module holds no quantiser; with the default bytes and
+    the decode scale NVFP4_GSCALE the elements have an RMS near 1, like the
+    bf16 pools' N(0, 1)."""
+    lo, hi = int(scale_bytes[0]), int(scale_bytes[1])
+    assert 0 <= lo < hi <= 0x7F, "non-negative finite e4m3 bytes (0x7F is NaN)"
     codes = torch.randint(0, 256, (*lead_shape, d // 2), generator=gen, dtype=torch.int32).to(torch.uint8)
-    scales = (0x30 + torch.randint(0, 16, (*lead_shape, d // 16), generator=gen, dtype=torch.int32)).to(torch.uint8)
+    scales = torch.randint(lo, hi, (*lead_shape, d // 16), generator=gen, dtype=torch.int32).to(torch.uint8)
     return codes, scales
 
 
@@ -179,7 +187,8 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
                   sm_scale: Optional[float] = None, bt_stride: Optional[int] = None,
                   q_mode: str = "randn", v_mode: str = "randn",
                   nvfp4_gscale: float = NVFP4_GSCALE, window_left: int = 0,
-                  dense_block: bool = False) -> Workload:
+                  dense_block: bool = False, nvfp4_v_gscale: Optional[float] = None,
+                  nvfp4_scale_bytes=NVFP4_SCALE_BYTES) -> Workload:
     """Draw one seeded workload.
 
     ``windows`` is one int (same W for every request) or a per-request list.
@@ -187,7 +196,10 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
     request's seq_len in its last page, and pages no request owns) with NaN
     (bf16) or NaN block scales (NVFP4).  ``q_mode``/``v_mode`` 'zero' and
     'const' (V only: a per-(kv head, dim) power of two) produce the closed-form
-    cases.  ``dense_block``: the windows' own keys are drawn as dense
+    cases.  NVFP4: ``nvfp4_gscale`` is the K (and, unless ``nvfp4_v_gscale``
+    is given, the V) per-tensor decode scale; ``nvfp4_scale_bytes`` the
+    half-open range the block-scale bytes are drawn from.
+    ``dense_block``: the windows' own keys are drawn as dense
     ``block_k`` / ``block_v`` [sum W, Hkv, d] bf16 tensors and kept out of the
     cache, whose pages then cover each request's context only (bf16 pools).
     """
@@ -259,9 +271,10 @@ def make_workload(name: str, ctx_lens: Sequence[int], windows, num_q_heads: int,
             k_pool[bad] = float("nan")
             v_pool[bad] = float("nan")
     else:
-        kc, ks = _draw_nvfp4((pool_pages, Hkv, ps), d, g)
-        vc, vs = _draw_nvfp4((pool_pages, Hkv, ps), d, g)
-        kg = vg = float(nvfp4_gscale)
+        kc, ks = _draw_nvfp4((pool_pages, Hkv, ps), d, g, nvfp4_scale_bytes)
+        vc, vs = _draw_nvfp4((pool_pages, Hkv, ps), d, g, nvfp4_scale_bytes)
+        kg = float(nvfp4_gscale)
+        vg = float(nvfp4_gscale if nvfp4_v_gscale is None else nvfp4_v_gscale)
         if poison_unread:
             bad = (~owned)[:, None, :, None]
             ks[bad.expand_as(ks)] = 0xFF  # e4m3 NaN

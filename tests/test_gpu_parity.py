@@ -380,6 +380,47 @@ def test_full_size_sampled(name, make, variant):
     run_and_check(wl, variant, trace=True, sel=_sample(wl))
 
 
+# Every row and head of the full-size single-GPU workloads (the 64K ones stay
+# sampled above: the oracle takes minutes there), in the bench's launch
+# configuration (tensor-core kernel, heuristic split count).
+EVERY_ROW = [
+    ("verify_sweep_w1", lambda: W.verify_sweep(1)),
+    ("verify_sweep_w8", lambda: W.verify_sweep(8)),
+    ("verify_sweep_w16", lambda: W.verify_sweep(16)),
+    ("batched_draft", lambda: W.batched_draft()),
+    ("nvfp4", lambda: W.nvfp4()),
+    # NVFP4 with block-scale bytes over the whole finite e4m3 range (0, the
+    # subnormals, up to 448); the V decode scale keeps |v| <= 6 x 448 / 800 =
+    # 3.36, as in the standard NVFP4 workload (6 x 1.875 x 0.3 = 3.375): the bf16
+    # output alone rounds by up to |O| x 2^-9, which stays under the 1e-2 bound
+    # only while |O| < 4
+    ("nvfp4_full_scale_range", lambda: W.nvfp4(nvfp4_scale_bytes=W.NVFP4_SCALE_BYTES_FULL,
+                                                nvfp4_gscale=0.3, nvfp4_v_gscale=1 / 800)),
+]
+
+
+@pytest.mark.parametrize("name,make", EVERY_ROW, ids=[n for n, _ in EVERY_ROW])
+def test_full_size_every_row(name, make):
+    wl = make()
+    run_and_check(wl, sa.SPEC_ATTN_VARIANT_TCGEN05, trace=True)
+
+
+# NVFP4 caches whose block scales span every non-negative finite e4m3 byte, at
+# several per-tensor decode scales (K's sets the score range, V's the output
+# size: max |v| = 6 x 448 x v_gscale stays below 4, where the bf16 output's own
+# rounding is within the 1e-2 bound), every head_dim, both kernels, split and
+# unsplit.
+@pytest.mark.parametrize("variant", VARIANTS[1:])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("kg,vg", [(0.3, 1 / 800), (1 / 448, 1 / 800), (0.02, 0.00125), (4.0, 0.0005)])
+def test_nvfp4_full_scale_range(variant, d, kg, vg):
+    wl = W.make_workload(f"fp4wide_d{d}", [2500, 700, 33], [8, 5, 1], 24, 4, d, W.MASK_CAUSAL_IN_BLOCK,
+                         kv_dtype=W.KV_NVFP4, seed=41 + d, pool_slack=0.1,
+                         nvfp4_scale_bytes=W.NVFP4_SCALE_BYTES_FULL, nvfp4_gscale=kg, nvfp4_v_gscale=vg)
+    for splits in (0, 3):
+        run_and_check(wl, variant, force_splits=splits, trace=False)
+
+
 def test_bench_main_step_as_timed():
     """The timed step of bench.py exactly as it runs there: its three calls
     (ctx 16384, W 1, 8, 16) with early_metadata, captured in one CUDA graph and

@@ -104,6 +104,19 @@ def test_nvfp4_pools_hold_codes_and_scales_in_their_documented_ranges():
     assert wl.kv_bytes == 4 * (16384 + 8) * 4 * 2 * (128 + 16)
 
 
+def test_nvfp4_full_scale_range_draws_zero_subnormal_and_large_scale_bytes():
+    wl = W.make_workload("wide", [3000], [8], 24, 4, 256, 0, kv_dtype=W.KV_NVFP4, seed=5,
+                         nvfp4_scale_bytes=W.NVFP4_SCALE_BYTES_FULL, nvfp4_gscale=0.3, nvfp4_v_gscale=1 / 448)
+    for s in (wl.k_scales, wl.v_scales):
+        vals = set(torch.unique(s).tolist())
+        assert max(vals) <= 0x7E and 0x00 in vals           # finite, non-negative, zero included
+        assert any(1 <= v <= 7 for v in vals)               # e4m3 subnormals
+        assert 0x7E in vals and len(vals) == 0x7F           # up to 448: every byte appears
+    assert wl.k_gscale == 0.3 and wl.v_gscale == 1 / 448
+    with pytest.raises(AssertionError):
+        W.make_workload("nan", [100], [4], 4, 1, 64, 0, kv_dtype=W.KV_NVFP4, nvfp4_scale_bytes=(0, 0x80))
+
+
 def test_dense_block_keeps_the_window_out_of_the_cache():
     wl = W.make_workload("db", [100, 0, 33], [16, 4, 9], 24, 4, 128, 0, seed=1, dense_block=True)
     _check_structure(wl, [100, 0, 33], [16, 4, 9])
