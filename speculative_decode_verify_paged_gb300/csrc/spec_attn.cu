@@ -39,6 +39,7 @@ struct spec_attn_plan {
     int smem;
     bool uses_merge;
     bool w_invariant;
+    bool compact;               // tensor-core kernel in compact block order (one-dimensional grid)
     int split_align;
     int64_t kv_page_stride;     // bytes, resolved (dense when the problem gives 0)
     int64_t scale_page_stride;
@@ -78,12 +79,13 @@ size_t bytes_per_token_head(int kv_dtype, int d) {
 // Rough cost (microseconds) of one call with `c` keys per split.  Terms:
 //   waves of CTAs, each paying a fixed start/finish cost plus its keys at the
 //   per-CTA streaming (or compute) rate; the whole job can not beat HBM; and
-//   the merge reads every partial once more.  Waves count the whole grid
-//   (max splits x KV heads x requests x row groups), not only the CTAs with
-//   work: the grid is laid out for the longest request, and a CTA of a shorter
-//   one past its last split still takes an SM for its prologue before it
-//   leaves, so blocks past the first wave start late even when the CTAs with
-//   work would fit in one.
+//   the merge reads every partial once more.  Waves count the CTAs with work
+//   when the kernel runs in compact block order (those come first in launch
+//   order); otherwise the whole grid (max splits x KV heads x requests x row
+//   groups): it is laid out for the longest request, and a CTA of a shorter one
+//   past its last split still takes an SM for its prologue before it leaves, so
+//   blocks past the first wave start late even when the CTAs with work would
+//   fit in one.
 struct CostModel {
     double hbm_bytes_per_us = 6.5e6;   // ~6.5 TB/s
     double l2_bytes_per_us = 2.0e7;    // partials stay in L2
@@ -94,14 +96,18 @@ struct CostModel {
 
 int choose_keys_per_split(const std::vector<int64_t>& lens, int64_t max_seq, int hkv, int row_groups,
                           int slots, double total_bytes, double partial_bytes_per_split,
-                          const CostModel& cm) {
+                          const CostModel& cm, bool compact) {
     const int64_t max_units = std::max<int64_t>(1, (max_seq + kSplitUnit - 1) / kSplitUnit);
     double best = 1e300;
     int best_c = static_cast<int>(max_units * kSplitUnit);
     for (int64_t u = 1; u <= max_units; ++u) {
         const int64_t c = u * kSplitUnit;
         const int64_t splits = (max_seq + c - 1) / c;
-        const int64_t ctas = static_cast<int64_t>(lens.size()) * hkv * row_groups * splits;
+        int64_t ctas = static_cast<int64_t>(lens.size()) * hkv * row_groups * splits;
+        if (compact) {
+            ctas = 0;
+            for (int64_t L : lens) ctas += static_cast<int64_t>(hkv) * row_groups * ((L + c - 1) / c);
+        }
         const int64_t waves = (ctas + slots - 1) / slots;
         const double t_cta = cm.cta_fixed_us + static_cast<double>(c) * cm.key_us;
         const double t_waves = static_cast<double>(waves) * t_cta;
@@ -320,6 +326,18 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         lens.push_back(L);
     }
     const int64_t max_seq = std::max<int64_t>(1, span_bound);
+    // Compact block order (tensor-core kernel, 2 to 64 requests): the CTAs
+    // with work come first in launch order.  It costs the CTAs one more round
+    // trip for metadata, so it is used only where the (splits x KV heads x
+    // requests) grid would hold idle slots: lengths unknown, or uneven spans or
+    // windows.
+    plan->compact = false;
+    if (use_tc && p.num_reqs >= 2 && p.num_reqs <= 64) {
+        plan->compact = !(h_seq_lens && h_q_indptr);
+        for (int r = 1; r < p.num_reqs && !plan->compact; ++r)
+            plan->compact = lens[r] != lens[0] ||
+                            (h_q_indptr[r + 1] - h_q_indptr[r]) != (h_q_indptr[1] - h_q_indptr[0]);
+    }
     const size_t bkh = bytes_per_token_head(p.kv_dtype, p.head_dim);
     double total_bytes = 0;
     for (int64_t L : lens) total_bytes += static_cast<double>(L) * p.num_kv_heads * 2.0 * bkh;
@@ -356,13 +374,21 @@ int spec_attn_plan_create(const spec_attn_problem* problem, const int32_t* h_seq
         plan->keys_per_split = static_cast<int>(std::max<int64_t>(c, kSplitUnit));
     } else {
         plan->keys_per_split = choose_keys_per_split(lens, max_seq, p.num_kv_heads, plan->row_groups,
-                                                     plan->num_sms * occ, total_bytes, partial_bytes, cm);
+                                                     plan->num_sms * occ, total_bytes, partial_bytes, cm,
+                                                     plan->compact);
     }
     plan->max_splits = static_cast<int>((max_seq + plan->keys_per_split - 1) / plan->keys_per_split);
     plan->uses_merge = plan->max_splits > 1 || plan->w_invariant;
 
-    plan->grid = dim3(static_cast<unsigned>(plan->max_splits * plan->row_groups),
-                      static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(std::max(1, p.num_reqs)));
+    if (plan->compact && static_cast<int64_t>(plan->max_splits) * plan->row_groups * p.num_kv_heads *
+                                 p.num_reqs > INT32_MAX)
+        plan->compact = false;   // the one-dimensional grid would not fit
+    if (plan->compact)
+        plan->grid = dim3(static_cast<unsigned>(static_cast<int64_t>(plan->max_splits) * plan->row_groups *
+                                                p.num_kv_heads * p.num_reqs));
+    else
+        plan->grid = dim3(static_cast<unsigned>(plan->max_splits * plan->row_groups),
+                          static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(std::max(1, p.num_reqs)));
 
     // ---- workspace layout: [status region][(lse, scale) partials][fp16 O partials] ----
     size_t ws = kStatusBytes;
@@ -564,6 +590,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.window_left = p.window_left;
     sp.split_align = plan->split_align;
     sp.dense_block = p.dense_block_kv;
+    sp.compact = plan->compact ? 1 : 0;
     sp.early_metadata = p.early_metadata;
     sp.test_stall = p.test_stall;
     sp.block_k = static_cast<const uint16_t*>(block_k);

@@ -79,6 +79,8 @@ struct SplitParams {
     int early_metadata;         // lengths, windows and block table are not written by the previous kernel
     int test_stall;             // testing: the K (NVFP4: raw) producer issues nothing
     int dense_block;            // the window's keys come from block_k / block_v (bf16 caches)
+    int compact;                // tensor-core kernel: one-dimensional grid, blocks in order of work units
+                                // (request, split, KV head, row group) that exist; the rest idle
     const uint16_t* block_k;    // [total_rows, Hkv, d] bf16 bits, or nullptr
     const uint16_t* block_v;
 };

@@ -108,7 +108,7 @@ struct TcLayout {
     static constexpr int kRawVS = kRawVC + kPPT * kRawCodePage;
     static constexpr int kRawTile = 2 * kPPT * (kRawCodePage + kRawScalePage);
     static_assert(kRawCodePage % 128 == 0 && kRawScalePage % 128 == 0, "TMA destinations on 128 B");
-    static constexpr int kAuxBytes = 1536;
+    static constexpr int kAuxBytes = 1664;
     static constexpr int kMaxDyn = KV ? 232448 : 204800;    // 227 KB opt-in limit; bf16: 200 KB
     static constexpr int kFixed = 1024 + kQSmem + kPBytes + kAuxBytes;
     static constexpr int kRing = (kMaxDyn - kFixed) / kTileBytes;
@@ -160,8 +160,10 @@ struct TcAux {
     int abort;
     int32_t list_k[kPageListCap];          // the split's page ids, one list per producer
     int32_t list_v[kPageListCap];
+    int32_t item[4];                       // compact block order: request (-1: none), split, KV head, row group
+    ReqInfo item_ri;                       // and that request's metadata
 };
-static_assert(sizeof(TcAux) <= 1536, "aux region");
+static_assert(sizeof(TcAux) <= TcLayout<64, 0>::kAuxBytes, "aux region");
 
 // One producer warp streams one of K or V: block-table entries are fetched by
 // all 32 lanes at once (coalesced) into a shared-memory list, then lane 0
@@ -394,6 +396,58 @@ __device__ __forceinline__ void dequant(const SplitParams& p, int key_lo, int ke
     }
 }
 
+// Compact block order (p.compact): block L of a one-dimensional grid takes the
+// L-th unit of work -- (request, split, KV head, row group), requests in
+// order, and within one split-major, then KV head, then row group -- counting
+// only the splits and row groups each request's length and window give it.
+// Blocks past the last unit have none.  The blocks with work thus come first
+// in launch order, so in a batch of uneven lengths they all start in the
+// first wave, instead of waiting behind the blocks of short requests' missing
+// splits that the (splits x KV heads x requests) grid lays out for the longest.
+// One warp: requests in chunks of 32, one lane each (their metadata in one
+// memory round trip a chunk), and a warp scan of the unit counts.  Writes
+// the unit and its request's metadata to item / item_ri.  Block 0 reports
+// the device status of requests with bad lengths or windows (which get no
+// work).
+template <bool RG>
+__device__ __forceinline__ void compact_item(const SplitParams& p, TcAux* aux, int lane) {
+    const int L = blockIdx.x;
+    int base = 0;
+    int found = 0;
+    // (block 0 scans every request, for the status report)
+    for (int r0 = 0; r0 < p.num_reqs && (!found || L == 0); r0 += 32) {
+        const int r = r0 + lane;
+        ReqInfo ri;
+        int cnt = 0, groups = 1;
+        if (r < p.num_reqs &&
+            load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
+                         p.bt_stride << (4 + p.page_shift), p.keys_per_split, blockIdx.x == 0 ? p.status : nullptr,
+                         ri, p.window_left, p.split_align, p.dense_block)) {
+            groups = RG ? (ri.w + p.window_rows_per_cta - 1) / p.window_rows_per_cta : 1;
+            cnt = ri.nsplits * p.num_kv_heads * groups;
+        }
+        int inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFullMask, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int lo = base + inc - cnt;
+        const bool mine = cnt > 0 && L >= lo && L < base + inc;
+        if (mine) {
+            const int local = L - lo;
+            aux->item[0] = r;
+            aux->item[1] = local / (groups * p.num_kv_heads);
+            aux->item[2] = (local / groups) % p.num_kv_heads;
+            aux->item[3] = local % groups;
+            aux->item_ri = ri;
+        }
+        found = __any_sync(kFullMask, mine);
+        base += __shfl_sync(kFullMask, inc, 31);
+    }
+    if (!found && lane == 0) aux->item[0] = -1;
+}
+
 template <int D, int KV, bool TRACE, bool RG>
 __global__ void __launch_bounds__(KV ? kTcThreadsFp4 : kTcThreadsBf16, 1)
 split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tmq,
@@ -406,9 +460,10 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     // window rows (all G heads of each), so windows of more than 128 rows per KV
     // head take several CTAs, each streaming the split's K/V once.  Without RG
     // (one group) the row offsets below are compile-time zeros.
-    const int rg = RG ? blockIdx.x % p.row_groups : 0;
-    const int split = RG ? blockIdx.x / p.row_groups : blockIdx.x;
-    const int kvh = blockIdx.y, r = blockIdx.z;
+    // (compact block order: replaced below by the block's unit of work)
+    int rg = RG ? blockIdx.x % p.row_groups : 0;
+    int split = RG ? blockIdx.x / p.row_groups : blockIdx.x;
+    int kvh = blockIdx.y, r = blockIdx.z;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -458,10 +513,20 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         }
     }
     if (warp == 1) tmem_alloc(&aux->tmem_base, L::kTmemCols);
+    if (p.compact && warp == 3) {
+        if (!p.early_metadata) pdl_wait_primary();
+        compact_item<RG>(p, aux, lane);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = aux->tmem_base;
+    if (p.compact) {
+        r = aux->item[0];
+        split = aux->item[1];
+        kvh = aux->item[2];
+        rg = aux->item[3];
+    }
 
     // Up to here the CTA touched only its own resources (and the kernel
     // parameters), which lets it start while the previous kernel in the stream
@@ -477,19 +542,25 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     // length: those entries are dropped and the producers fetch their own.
     int key_lo = split * p.keys_per_split;
     int pre0 = -1, pre1 = -1;
-    if ((warp == 0 || (!KV && warp == 2)) && r < p.num_reqs) {
+    if ((warp == 0 || (!KV && warp == 2)) && r >= 0 && r < p.num_reqs) {
         const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
         const int u0 = key_lo / 16 + lane;
         if ((u0 >> p.page_shift) < p.bt_stride) pre0 = ld_volatile_i32(bt + (u0 >> p.page_shift));
         if (((u0 + 32) >> p.page_shift) < p.bt_stride) pre1 = ld_volatile_i32(bt + ((u0 + 32) >> p.page_shift));
     }
     ReqInfo ri;
-    const bool reporter = (tid == 0 && blockIdx.x == 0 && kvh == 0);
-    const bool active = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
-                                     p.bt_stride << (4 + p.page_shift), p.keys_per_split,
-                                     reporter ? p.status : nullptr, ri, p.window_left, p.split_align,
-                                     p.dense_block) &&
-                        split < ri.nsplits && (!RG || rg * p.window_rows_per_cta < ri.w);
+    bool active;
+    if (p.compact) {
+        // the unit of work and its request's metadata (checked) came with the block order
+        active = r >= 0;
+        ri = aux->item_ri;
+    } else {
+        const bool reporter = (tid == 0 && blockIdx.x == 0 && kvh == 0);
+        active = load_request(p.seq_lens, p.q_indptr, r, p.max_w, p.total_rows, p.max_seq_len,
+                              p.bt_stride << (4 + p.page_shift), p.keys_per_split, reporter ? p.status : nullptr,
+                              ri, p.window_left, p.split_align, p.dense_block) &&
+                 split < ri.nsplits && (!RG || rg * p.window_rows_per_cta < ri.w);
+    }
     if (!active) {   // uniform across the CTA
         if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
         return;
