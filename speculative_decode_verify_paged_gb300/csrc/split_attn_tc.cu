@@ -587,13 +587,13 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     if (warp == 0) {
         // ------------------------------------------------------------ query tile + K producer
         if (lane == 0) {
-            // one box of 64 head_dim elements x G heads x Wg window rows per
-            // 128-byte atom column; rows past total_q_rows are zero-filled by TMA,
-            // rows past the group's share of W_r x G belong to no output.
+            // one box: 64 head_dim elements x G heads x Wg window rows x the
+            // d / 64 chunks, landing chunk-major ([chunk][row][head][128 B]);
+            // rows past total_q_rows are zero-filled by TMA, rows past the
+            // group's share of W_r x G belong to no output.
             const uint32_t qbytes = static_cast<uint32_t>(L::kChunks * 128 * G * Wg);
             mbar_arrive_expect_tx(&aux->q_full, qbytes);
-            for (int c = 0; c < L::kChunks; ++c)
-                tma_load_3d(sQ + c * (kM * 128), &tmq, c * 64, kvh * G, ri.row0 + w_lo, &aux->q_full);
+            tma_load_4d(sQ, &tmq, 0, kvh * G, ri.row0 + w_lo, 0, &aux->q_full);
         }
         __syncwarp();
         if constexpr (KV) {
@@ -732,15 +732,20 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             // two elements per column, the lower one in the low half.  NVFP4:
             // its MMAs take fp16, so the row is converted on the way (saturating
             // at +-65504; exact for every bf16 value of magnitude 2^-14 .. 65504).
+            // Rows past R (padding) are zero: their scores are exactly 0.
             if ((ok = warp_wait(&aux->q_full, 0, abort))) {
                 const uint32_t qb = smem_addr(sQ);
+                const int box_rows = G * Wg;   // rows per chunk of the landed box
 #pragma unroll 1
                 for (int c = 0; c < L::kChunks; ++c) {
                     uint32_t w[32];
+                    // the box's row (c, m) is 128-byte row c * box_rows + m of the
+                    // landing area, its 16-byte pieces swizzled by that row's index
+                    const int lr = c * box_rows + m;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        // logical 16-byte piece q of row m sits at piece q ^ (m & 7)
-                        const uint4 v = ld_shared_v4(qb + c * (kM * 128) + m * 128 + ((q ^ (m & 7)) << 4));
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (valid) v = ld_shared_v4(qb + lr * 128 + ((q ^ (lr & 7)) << 4));
                         if constexpr (KV) {
                             w[4 * q + 0] = bf16x2_to_f16x2_sat(v.x);
                             w[4 * q + 1] = bf16x2_to_f16x2_sat(v.y);
@@ -1206,11 +1211,13 @@ bool encode_block_v_map(CUtensorMap* map, const void* t, int total_rows, int hkv
 bool encode_q_map(CUtensorMap* map, const void* q, int total_rows, int hq, int d, int group, int max_w) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)total_rows};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * hq};
-    cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)max_w};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+    // Q [total_rows, Hq, d] bf16 as (64 elements, head, row, 64-element chunk):
+    // one box takes every chunk of G heads x max_w rows, chunk-major
+    cuuint64_t dims[4] = {64, (cuuint64_t)hq, (cuuint64_t)total_rows, (cuuint64_t)d / 64};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * hq, 128};
+    cuuint32_t box[4] = {64, (cuuint32_t)group, (cuuint32_t)max_w, (cuuint32_t)d / 64};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS;
