@@ -442,7 +442,7 @@ __device__ __forceinline__ void compact_item(const SplitParams& p, TcAux* aux, i
             aux->item[3] = local % groups;
             aux->item_ri = ri;
         }
-        found = __any_sync(kFullMask, mine);
+        found |= __any_sync(kFullMask, mine);
         base += __shfl_sync(kFullMask, inc, 31);
     }
     if (!found && lane == 0) aux->item[0] = -1;

@@ -257,6 +257,54 @@ def test_constant_values_come_back_bit_exactly(kv, variant):
 
 
 # --------------------------------------------------------------------------- #
+# Compact block order (tensor-core kernel, 2..64 requests of uneven lengths)
+# --------------------------------------------------------------------------- #
+def _ragged(name, num_reqs, seed, **kw):
+    g = np.random.default_rng(seed)
+    ctx = g.integers(0, 900, size=num_reqs).tolist()
+    ws = g.integers(1, 17, size=num_reqs).tolist()
+    return W.make_workload(name, ctx, ws, 24, 4, 128, W.MASK_CAUSAL_IN_BLOCK, seed=seed, pool_slack=0.1, **kw)
+
+
+def test_compact_order_over_two_request_chunks_reports_a_bad_request():
+    """40 requests (two 32-request chunks of the block-order scan): the grid is
+    one-dimensional, every row matches the oracle, and a request made invalid
+    on the device (length below its window) sets the status bit -- reported by
+    block 0 from the second chunk -- while the other requests' rows stay right."""
+    wl = _ragged("compact40", 40, 81)
+    dw = make_dw(wl, sa.SPEC_ATTN_VARIANT_TCGEN05, force_splits=3)
+    assert dw.plan.info["grid_y"] == 1 and dw.plan.info["grid_z"] == 1
+    o_ref, lse_ref, _ = oracle.run_workload(wl, want_trace=False)
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() == 0
+    check_close(dw.o, dw.lse, o_ref, lse_ref)
+    bad = 37
+    a, b = int(wl.q_indptr[bad]), int(wl.q_indptr[bad + 1])
+    dw.seq_lens[bad] = b - a - 1            # shorter than its own window
+    dw.o.zero_()
+    dw.lse.zero_()
+    dw.run()
+    torch.cuda.synchronize()
+    assert dw.device_status() & sa.SPEC_ATTN_DEV_BAD_SEQ_LEN
+    keep = np.ones((wl.total_rows, wl.num_q_heads), dtype=np.uint8)
+    keep[a:b] = 0
+    check_close(dw.o, dw.lse, o_ref, lse_ref, sel=keep)
+
+
+def test_more_than_64_requests_keep_the_three_dimensional_grid():
+    wl = _ragged("grid70", 70, 82)
+    dw = run_and_check(wl, sa.SPEC_ATTN_VARIANT_TCGEN05, trace=True)
+    assert dw.plan.info["grid_z"] == 70
+
+
+def test_even_batches_keep_the_three_dimensional_grid():
+    wl = W.make_workload("even", [700] * 4, 8, 24, 4, 128, W.MASK_CAUSAL_IN_BLOCK, seed=83)
+    dw = run_and_check(wl, sa.SPEC_ATTN_VARIANT_TCGEN05, trace=False)
+    assert dw.plan.info["grid_z"] == 4
+
+
+# --------------------------------------------------------------------------- #
 # Device-side checks: bad inputs become a status bit, never a fault
 # --------------------------------------------------------------------------- #
 @pytest.mark.parametrize("variant", VARIANTS[1:])
