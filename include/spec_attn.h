@@ -400,10 +400,11 @@ int spec_attn_version(void);
  * head of the array once its host checks have passed (a rejected call writes
  * nothing), and spec_attn_noalloc_check_device_status reads what the last
  * call left.  The first call on each device looks up the array's device
- * address (with that device current) and caches it; make that first call
- * before any stream capture.  The cached address belongs to the device's
- * primary context: after cudaDeviceReset it is stale, so do not call this
- * entry point again on a device the process has reset.  Allocates nothing;
+ * address (with that device current) and caches it with the id of the
+ * context it belongs to; make that first call before any stream capture.  A
+ * call made in another context of the device (after cudaDeviceReset, which
+ * creates the primary context anew) looks the address up again, so make the
+ * first call after a reset outside stream capture too.  Allocates nothing;
  * other arguments and errors as spec_attn_run.
  */
 #define SPEC_ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
