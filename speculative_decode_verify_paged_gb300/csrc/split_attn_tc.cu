@@ -14,8 +14,8 @@
 // section "The cost").
 //
 // Warp roles, bf16 KV (256 threads):
-//   warp 0      loads the query tile once (TMA, one box per 64 head_dim
-//               elements covering G heads x the group's window rows, into the V
+//   warp 0      loads the query tile once (one TMA box: every 64-element
+//               chunk of G heads x the group's window rows, into the V
 //               slots), then streams the K tiles: 64 keys (four 16-key units,
 //               a unit being a 16-key page or a quarter/half of a 64/32-key
 //               page; one 2 KB box per unit and 64 head_dim elements, issued
@@ -25,23 +25,28 @@
 //   warp 1      allocates TMEM and issues S_t = Q K_t^T (M 128, N 64, query
 //               tile from TMEM, -> fp32 in TMEM, double-buffered).
 //   warp 3      issues O += P_t V_t (M 128, N head_dim, one MMA per unit, P
-//               from shared memory, V MN-major).  Each issuer waits only on its
-//               own inputs, in tile order.
+//               from TMEM, V MN-major), then frees the S buffer P sat in.  Each
+//               issuer waits only on its own inputs, in tile order.
 //   warps 4-7   softmax: thread m owns row m (TMEM lane m).  First it moves its
 //               query row into TMEM.  Per tile it reads its 64 scores, applies
 //               the causal-in-block / non-causal mask and the sliding window
 //               by key index (rows past W x G run unmasked), updates a
 //               base-2 online softmax whose reference maximum moves only when a
 //               score exceeds it by more than 2^8 (then the row of O in TMEM is
-//               rescaled), and writes P into one half of a double buffer; at
-//               the end it normalises O and stages the row for the output (or a
-//               split partial), which every warp then copies out.
+//               rescaled), and writes P (16-bit) over the first half of its S
+//               buffer in TMEM.  At the end a request finished by this split
+//               has its rows normalised, staged and copied out by every warp;
+//               a split partial goes straight from TMEM to global memory
+//               (warps 0-7, chunk-major fp16 of O / its row maximum).
+//   (multi-request batches of uneven lengths: the grid is one-dimensional,
+//   each block taking the next existing (request, split, KV head, row group)
+//   unit, so the CTAs with work come first in launch order)
 // With the dense block operand, the request's last split ends with one more
 // tile: the window's own keys, one unit loaded from the block tensors.
 // NVFP4 KV (512 threads): warp 0 streams the tiles' codes and scales by TMA
 // into a raw ring; warps 8-11 decode K and 12-15 decode V into fp16 operand
-// tiles; the query row is converted to fp16 on its way into TMEM, S is single-
-// buffered, and P (fp16) goes to TMEM, where the P V MMA reads it.
+// tiles; the query row is converted to fp16 on its way into TMEM, and P is
+// fp16; the rest as for bf16.
 //
 // Every wait on an mbarrier is bounded: on time-out the CTA raises the
 // device-status bit, stops issuing, drains its in-flight copies and MMAs,
@@ -143,7 +148,7 @@ struct TcAux {
     uint64_t v_full[kMaxNV];
     uint64_t v_empty[kMaxNV];
     uint64_t s_full[2];
-    uint64_t s_empty[2];   // bf16: P V of the tile has read P from the buffer; NVFP4: S read
+    uint64_t s_empty[2];   // the P V of the buffer's tile has read its P (committed by the MMA)
     uint64_t p_full[2];
     uint64_t o_done;     // one phase per P V (rescale waits: at most one phase behind)
     uint64_t o_final;    // one phase after the last P V (the epilogue's wait)
