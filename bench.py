@@ -321,8 +321,8 @@ def interleaved_ratio(make_a, make_b, flush, steps, stream, sa, dev, variant):
     import torch
     import statistics
     wa, wb = make_a(), make_b()
-    da = sa.DeviceWorkload(wa, dev, kernel_variant=variant, early_metadata=1)
-    db = sa.DeviceWorkload(wb, dev, kernel_variant=variant, early_metadata=1)
+    da = sa.DeviceWorkload(wa, dev, kernel_variant=variant, early_metadata=1, early_context_kv=1)
+    db = sa.DeviceWorkload(wb, dev, kernel_variant=variant, early_metadata=1, early_context_kv=1)
     ta, tb = [], []
     for order in ("ab", "ba", "ab", "ba"):
         for c in order:
@@ -371,8 +371,11 @@ def run_ours(args, rank, world, local_rank):
 
     wls = main_workloads()
     # the step's lengths and block tables are filled once, before its first
-    # call, and never by the kernel preceding a call: early_metadata holds
-    dws = [sa.DeviceWorkload(wl, dev, kernel_variant=args.variant, early_metadata=1) for wl in wls]
+    # call, and never by the kernel preceding a call: early_metadata holds;
+    # no call writes another call's cache, and each call's own window slots
+    # are the only keys an append writes: early_context_kv holds
+    dws = [sa.DeviceWorkload(wl, dev, kernel_variant=args.variant, early_metadata=1, early_context_kv=1)
+           for wl in wls]
     kv_bytes = [wl.kv_bytes for wl in wls]
     launches_per_step = sum(1 + dw.plan.info["uses_merge"] for dw in dws)
 
@@ -424,7 +427,8 @@ def run_ours(args, rank, world, local_rank):
     if not args.quick:
         for name, make, *extra in table_workloads():
             wl = make()
-            kw = dict(extra[0]) if extra else {}
+            kw = dict(early_metadata=1, early_context_kv=1)
+            kw.update(extra[0] if extra else {})
             mode = kw.pop("append", "run")
             if mode != "run":
                 kw.update(mode=mode, append_rows=W.window_kv_rows(wl.total_rows, wl.num_kv_heads, wl.head_dim,
@@ -501,7 +505,7 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1), bf16)",
             "config": {"workload": MAIN_WORKLOAD, "calls_per_step": len(dws),
-                       "kv_bytes_per_step": sum(kv_bytes), "early_metadata": True, "l2": "flushed before every step, untimed: write of a 2 x L2 buffer, then read of a second one (clean L2); value_dirty_l2_flush = write only",
+                       "kv_bytes_per_step": sum(kv_bytes), "early_metadata": True, "early_context_kv": True, "l2": "flushed before every step, untimed: write of a 2 x L2 buffer, then read of a second one (clean L2); value_dirty_l2_flush = write only",
                        "timing": "CUDA events around one CUDA-graph replay of the step's three spec_attn_run calls (device time); per_call: each call alone in its own graph, and us_eager",
                        "us_per_call": {c["workload"]: c["us"] for c in per_call},
                        "parallelism": "replicas" if world > 1 else "single GPU"},

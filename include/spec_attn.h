@@ -174,6 +174,16 @@ typedef struct spec_attn_problem {
                                     call then sets SPEC_ATTN_DEV_WAIT_TIMEOUT, frees its
                                     tensor memory and returns, leaving O undefined and
                                     the context usable.  0 in every real call. */
+    int32_t early_context_kv;    /* 1 (needs early_metadata = 1): the caller also
+                                    vouches that no such kernel writes a cached key
+                                    below its request's ctx_r (the window's own keys
+                                    may be written, e.g. by spec_attn_append_kv just
+                                    before); the bf16 tensor-core kernel then starts
+                                    the copies of each split's first K and V tile
+                                    (when it holds context keys only, and with no
+                                    sliding window or dense block operand) while that
+                                    kernel drains.  Results are bit-identical either
+                                    way.  0: it waits first (safe). */
 } spec_attn_problem;
 
 /*

@@ -72,6 +72,7 @@ class spec_attn_problem(ctypes.Structure):
         ("window_left", ctypes.c_int32), ("kv_page_stride", ctypes.c_int64),
         ("scale_page_stride", ctypes.c_int64), ("dense_block_kv", ctypes.c_int32),
         ("early_metadata", ctypes.c_int32), ("test_stall", ctypes.c_int32),
+        ("early_context_kv", ctypes.c_int32),
     ]
 
 
@@ -219,14 +220,14 @@ def spec_attn_plan_create(*, num_reqs, total_q_rows, max_w, num_q_heads, num_kv_
                           page_size=16, sm_scale=0.0, force_splits=0, kernel_variant=0,
                           seq_lens=None, q_indptr=None, w_invariant=0, fixed_keys_per_split=0,
                           window_left=0, kv_page_stride=0, scale_page_stride=0, dense_block_kv=0,
-                          early_metadata=0, test_stall=0) -> Plan:
+                          early_metadata=0, test_stall=0, early_context_kv=0) -> Plan:
     lib = load_library()
     prob = spec_attn_problem(num_reqs, total_q_rows, max_w, num_q_heads, num_kv_heads, head_dim,
                              page_size, num_pages, block_table_stride, mask_mode, kv_dtype,
                              float(sm_scale), int(max_seq_len), force_splits, kernel_variant,
                              int(w_invariant), int(fixed_keys_per_split), int(window_left),
                              int(kv_page_stride), int(scale_page_stride), int(dense_block_kv),
-                             int(early_metadata), int(test_stall))
+                             int(early_metadata), int(test_stall), int(early_context_kv))
     sl, _k1 = _host_i32(seq_lens)
     qi, _k2 = _host_i32(q_indptr)
     handle = ctypes.c_void_p()
@@ -392,7 +393,8 @@ class DeviceWorkload:
     """A workload's tensors moved to a CUDA device, plus output and workspace buffers."""
 
     def __init__(self, wl, device="cuda", force_splits=0, kernel_variant=0, host_lens=True, w_invariant=0,
-                 fixed_keys_per_split=0, append_rows=None, mode="run", interleave=False, early_metadata=0):
+                 fixed_keys_per_split=0, append_rows=None, mode="run", interleave=False, early_metadata=0,
+                 early_context_kv=0):
         """``append_rows``: (k_new, v_new) [total_rows, Hkv, d] bf16 for the KV
         append.  ``mode``: what :meth:`run` launches -- "run" (attention),
         "run_append" (append, then attention) or "append" (the append alone).
@@ -438,7 +440,7 @@ class DeviceWorkload:
             q_indptr=wl.q_indptr if host_lens else None, w_invariant=w_invariant,
             fixed_keys_per_split=fixed_keys_per_split, window_left=wl.window_left, kv_page_stride=kv_stride,
             scale_page_stride=sc_stride, dense_block_kv=int(wl.block_k is not None),
-            early_metadata=early_metadata)
+            early_metadata=early_metadata, early_context_kv=early_context_kv)
         self.workspace = torch.zeros(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device=dev)
         self.block_k = None if wl.block_k is None else wl.block_k.to(dev)
         self.block_v = None if wl.block_v is None else wl.block_v.to(dev)

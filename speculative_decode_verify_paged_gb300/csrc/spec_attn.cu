@@ -133,6 +133,8 @@ int validate_problem(const spec_attn_problem* p, const int32_t* h_seq_lens, cons
     if (p->w_invariant != 0 && p->w_invariant != 1) return SPEC_ATTN_E_INVALID_ARG;
     if (p->dense_block_kv != 0 && p->dense_block_kv != 1) return SPEC_ATTN_E_INVALID_ARG;
     if (p->early_metadata != 0 && p->early_metadata != 1) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->early_context_kv != 0 && p->early_context_kv != 1) return SPEC_ATTN_E_INVALID_ARG;
+    if (p->early_context_kv && !p->early_metadata) return SPEC_ATTN_E_INVALID_ARG;   // its tiles need the metadata
     if (p->test_stall != 0 && p->test_stall != 1) return SPEC_ATTN_E_INVALID_ARG;
     // the stall exercises the tensor-core kernel's bounded waits
     if (p->test_stall && p->kernel_variant != SPEC_ATTN_VARIANT_TCGEN05) return SPEC_ATTN_E_INVALID_ARG;
@@ -592,6 +594,7 @@ static int run_impl(const spec_attn_plan* plan, const void* q, const void* k_poo
     sp.dense_block = p.dense_block_kv;
     sp.compact = plan->compact ? 1 : 0;
     sp.early_metadata = p.early_metadata;
+    sp.early_context_kv = p.early_context_kv;
     sp.test_stall = p.test_stall;
     sp.block_k = static_cast<const uint16_t*>(block_k);
     sp.block_v = static_cast<const uint16_t*>(block_v);

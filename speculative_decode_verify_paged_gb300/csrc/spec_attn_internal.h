@@ -77,6 +77,7 @@ struct SplitParams {
     int window_left;            // causal sliding window (keys), 0 = none
     int split_align;            // first split of a request starts at a multiple of this (keys)
     int early_metadata;         // lengths, windows and block table are not written by the previous kernel
+    int early_context_kv;       // nor the cached keys below ctx_r: the first K/V tile may be read before the wait
     int test_stall;             // testing: the K (NVFP4: raw) producer issues nothing
     int dense_block;            // the window's keys come from block_k / block_v (bf16 caches)
     int compact;                // tensor-core kernel: one-dimensional grid, blocks in order of work units

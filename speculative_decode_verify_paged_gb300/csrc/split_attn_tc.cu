@@ -137,6 +137,11 @@ struct TcLayout {
     static_assert(kSmem <= kMaxDyn, "shared memory");
     static_assert(kTmemNeed <= 512, "tensor memory");
     static_assert(kQBytes <= kNV * kTileBytes, "the query tile lands in the V slots");
+    // With early_context_kv it lands in the last V slots instead, so that the
+    // first kVFree V tiles may be copied while it is still there.
+    static constexpr int kQOff = kNV * kTileBytes - kQBytes;
+    static constexpr int kVFree = kQOff / kTileBytes;
+    static_assert(kQOff % 1024 == 0, "the query tile's box lands on 1024-byte swizzle atoms");
     // the final-output epilogue stages kM rows of bf16 O (+16 B padding), the
     // partials epilogue 3 x kM floats, over the operand/raw buffers (idle by then)
     static_assert(kM * (D * 2 + 16) <= (kNK + kNV) * kTileBytes + kNR * kRawTile, "epilogue staging");
@@ -176,11 +181,15 @@ static_assert(sizeof(TcAux) <= TcLayout<64, 0>::kAuxBytes, "aux region");
 // With the dense block operand, tile Tc (the last of the request's last
 // split) holds the window's own keys: one 16-key unit of rows row0 .. row0 + 15
 // of the block tensor (tm_block), laid out like a page unit.
-template <int D, int NSLOT, bool IS_V, bool TRACE>
+// V: the slots from q_gate on hold the query tile until it is in TMEM, so the
+// producer waits for that before it first fills one.  after_first() runs once
+// the first tile's copies are issued (or, if the loop stops before, at its end).
+template <int D, int NSLOT, bool IS_V, bool TRACE, class F>
 __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int key_lo, int key_hi, int T,
                                        unsigned char* ring, uint64_t* full, uint64_t* empty, int32_t* list,
                                        TcAux* aux, const CUtensorMap* tm, volatile int* abort, int lane,
-                                       int pre0, int pre1, int Tc, int row0, const CUtensorMap* tm_block) {
+                                       int pre0, int pre1, int Tc, int row0, const CUtensorMap* tm_block,
+                                       int q_gate, const F& after_first) {
     using L = TcLayout<D, 0>;
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
     const int u_lo = key_lo / 16;                    // first 16-key unit of the split
@@ -214,6 +223,7 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
     for (int t = 0; t < T; ++t) {
         const int slot = t % NSLOT;
         if (t >= NSLOT && !warp_wait(&empty[slot], ((t / NSLOT) - 1) & 1, abort)) break;
+        if (IS_V && t == q_gate && !warp_wait(&aux->q_ready, 0, abort)) break;
         unsigned char* dst = ring + slot * L::kTileBytes;
         if (t >= Tc) {   // the dense block unit
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(L::kChunks * 2048));
@@ -225,6 +235,7 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
             }
             __syncwarp();
             issued = t + 1;
+            if (t == 0) after_first();
             continue;
         }
         const int rel = t * kPPT;  // first page of the tile, relative to the split
@@ -257,7 +268,9 @@ __device__ __forceinline__ int produce(const SplitParams& p, int r, int kvh, int
         }
         __syncwarp();
         issued = t + 1;
+        if (t == 0) after_first();
     }
+    if (issued == 0) after_first();
     return issued;
 }
 
@@ -475,7 +488,14 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char* sK = smem + L::kQSmem;
     unsigned char* sV = sK + NK * L::kTileBytes;
-    unsigned char* sQ = sV;   // the query tile lands in the V slots, then moves to TMEM
+    // early_context_kv (bf16, no sliding window, no dense block operand): the K
+    // and V producers issue each split's first tile, if it holds context keys
+    // only, before the programmatic wait; the query tile then lands in the last
+    // V slots (it is issued after the wait), so the first V tile need not wait
+    // for it to move to TMEM
+    const bool early_kv = !KV && p.early_context_kv && p.early_metadata && p.window_left == 0 && !p.dense_block;
+    // the query tile lands in the V slots, then moves to TMEM
+    unsigned char* sQ = sV + (early_kv ? L::kQOff : 0);
     unsigned char* sRaw = sV + NV * L::kTileBytes;   // NVFP4 only
     TcAux* aux = reinterpret_cast<TcAux*>(sRaw + L::kNR * L::kRawTile);
     volatile int* abort = &aux->abort;
@@ -570,7 +590,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
         return;
     }
-    if (p.early_metadata) pdl_wait_primary();
+    if (p.early_metadata && !(early_kv && (warp == 0 || warp == 2))) pdl_wait_primary();
     if (p.window_left > 0) {
         key_lo = ri.key_base + split * p.keys_per_split;
         pre0 = pre1 = kNoPrefetch;
@@ -589,18 +609,31 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     const bool final_out = (ri.nsplits == 1) && !p.always_partials;
     float ep_inv = 0.f, ep_lse2 = -INFINITY;   // softmax threads: 1 / l and log2-sum-exp of their row
 
+    // the split's first tile holds context keys only (its copies may start early)
+    const bool first_early = early_kv && key_lo + kBN <= ri.ctx;
     if (warp == 0) {
         // ------------------------------------------------------------ query tile + K producer
-        if (lane == 0) {
-            // one box: 64 head_dim elements x G heads x Wg window rows x the
-            // d / 64 chunks, landing chunk-major ([chunk][row][head][128 B]);
-            // rows past total_q_rows are zero-filled by TMA, rows past the
-            // group's share of W_r x G belong to no output.
-            const uint32_t qbytes = static_cast<uint32_t>(L::kChunks * 128 * G * Wg);
-            mbar_arrive_expect_tx(&aux->q_full, qbytes);
-            tma_load_4d(sQ, &tmq, 0, kvh * G, ri.row0 + w_lo, 0, &aux->q_full);
-        }
-        __syncwarp();
+        auto issue_q = [&]() {
+            if (lane == 0) {
+                // one box: 64 head_dim elements x G heads x Wg window rows x the
+                // d / 64 chunks, landing chunk-major ([chunk][row][head][128 B]);
+                // rows past total_q_rows are zero-filled by TMA, rows past the
+                // group's share of W_r x G belong to no output.
+                const uint32_t qbytes = static_cast<uint32_t>(L::kChunks * 128 * G * Wg);
+                mbar_arrive_expect_tx(&aux->q_full, qbytes);
+                tma_load_4d(sQ, &tmq, 0, kvh * G, ri.row0 + w_lo, 0, &aux->q_full);
+            }
+            __syncwarp();
+        };
+        // early: the first K tile, then the wait, then the query tile
+        if (early_kv && !first_early) pdl_wait_primary();
+        if (!first_early) issue_q();
+        auto after_first_k = [&]() {
+            if (first_early) {
+                pdl_wait_primary();
+                issue_q();
+            }
+        };
         if constexpr (KV) {
             // testing (test_stall): nothing arrives, the decoders' waits run out
             const int issued = p.test_stall ? 0
@@ -616,7 +649,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
                                             : produce<D, NK, false, TRACE>(p, r, kvh, key_lo, key_hi, T, sK,
                                                                            aux->k_full, aux->k_empty, aux->list_k,
                                                                            aux, &tmk, abort, lane, pre0, pre1, Tc,
-                                                                           ri.row0, &tmks);
+                                                                           ri.row0, &tmks, 0, after_first_k);
+            if (p.test_stall) after_first_k();
             if (*abort && lane == 0) {
                 drain_copies<NK>(aux->k_full, issued);
                 atomicOr(p.status, kDevWaitTimeout);
@@ -626,14 +660,17 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
     } else if (warp == 2) {
         // ------------------------------------------------------------ V producer (bf16)
         if constexpr (!KV) {
-            // the query tile sits in the V slots until the softmax warps have
-            // moved it into TMEM
-            if (warp_wait(&aux->q_ready, 0, abort)) {
-                const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
-                                                               aux->v_empty, aux->list_v, aux, &tmv, abort, lane,
-                                                               pre0, pre1, Tc, ri.row0, &tmvs);
-                if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
-            }
+            // the query tile sits in V slots until the softmax warps have moved
+            // it into TMEM: all of them, or (early_kv) the last ones, from kVFree
+            if (early_kv && !first_early) pdl_wait_primary();
+            auto after_first_v = [&]() {
+                if (first_early) pdl_wait_primary();
+            };
+            const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
+                                                           aux->v_empty, aux->list_v, aux, &tmv, abort, lane,
+                                                           pre0, pre1, Tc, ri.row0, &tmvs,
+                                                           early_kv ? L::kVFree : 0, after_first_v);
+            if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
         }
         __syncwarp();
     } else if (KV && warp >= 8) {

@@ -70,6 +70,8 @@ def _problem(**over):
     (dict(dense_block_kv=1, w_invariant=1), sa.SPEC_ATTN_E_INVALID_ARG),     # exactness is a cache-only rule
     (dict(dense_block_kv=1, kv_dtype=1), sa.SPEC_ATTN_E_UNSUPPORTED),       # the block operand is bf16
     (dict(early_metadata=2), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(early_context_kv=2, early_metadata=1), sa.SPEC_ATTN_E_INVALID_ARG),
+    (dict(early_context_kv=1), sa.SPEC_ATTN_E_INVALID_ARG),                 # needs early_metadata
     (dict(test_stall=1), sa.SPEC_ATTN_E_INVALID_ARG),                       # the stall hook needs TCGEN05
     (dict(num_q_heads=34, num_kv_heads=2), sa.SPEC_ATTN_E_UNSUPPORTED),  # group 17
     (dict(num_q_heads=6, num_kv_heads=4), sa.SPEC_ATTN_E_INVALID_ARG),

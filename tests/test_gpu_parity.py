@@ -617,9 +617,11 @@ def test_early_metadata_changes_no_bit(variant):
     wls = [W.make_workload(f"em{k}", *sh, seed=90 + k, pool_slack=0.1) for k, sh in enumerate(shapes)]
     late = [make_dw(wl, variant) for wl in wls]
     early = [make_dw(wl, variant, early_metadata=1) for wl in wls]
+    # and the first context K/V tile read before the wait too
+    early_kv = [make_dw(wl, variant, early_metadata=1, early_context_kv=1) for wl in wls]
     s = torch.cuda.Stream()
     outs = []
-    for dws in (late, early):
+    for dws in (late, early, early_kv):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for dw in dws:
@@ -627,8 +629,31 @@ def test_early_metadata_changes_no_bit(variant):
         g.replay()
         torch.cuda.synchronize()
         outs.append([(dw.o.clone(), dw.lse.clone()) for dw in dws])
-    for (o0, l0), (o1, l1), wl in zip(outs[0], outs[1], wls):
-        assert torch.equal(o0, o1) and torch.equal(l0, l1)
-    for dw, wl in zip(early, wls):
+    for other in outs[1:]:
+        for (o0, l0), (o1, l1) in zip(outs[0], other):
+            assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    for dw, wl in zip(early_kv, wls):
         o_ref, lse_ref, _ = oracle.run_workload(wl)
         check_close(dw.o, dw.lse, o_ref, lse_ref)
+
+
+def test_early_context_kv_after_the_append_changes_no_bit():
+    """The KV append writes the window's slots just before the attention call,
+    which with early_context_kv starts copying its first context tiles while
+    the append runs: bits equal to waiting first, for splits whose first tile
+    holds context keys only and for splits that start at the window."""
+    wl = W.make_workload("ekv_app", [3000, 40, 0, 700], [16, 9, 4, 1], 24, 4, 256, 0, seed=97, pool_slack=0.2)
+    rows = W.window_kv_rows(wl.total_rows, wl.num_kv_heads, wl.head_dim, seed=3, mix=False)
+    outs = []
+    for kw in (dict(), dict(early_metadata=1, early_context_kv=1)):
+        dw = sa.DeviceWorkload(wl, "cuda", kernel_variant=sa.SPEC_ATTN_VARIANT_TCGEN05, force_splits=5,
+                               mode="run_append", append_rows=rows, **kw)
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            dw.run(s)
+        g.replay()
+        torch.cuda.synchronize()
+        assert dw.device_status() == 0
+        outs.append((dw.o.clone(), dw.lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
