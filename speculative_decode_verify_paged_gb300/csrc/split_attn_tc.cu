@@ -138,9 +138,11 @@ struct TcLayout {
     static_assert(kTmemNeed <= 512, "tensor memory");
     static_assert(kQBytes <= kNV * kTileBytes, "the query tile lands in the V slots");
     // With early_context_kv it lands in the last V slots instead, so that the
-    // first kVFree V tiles may be copied while it is still there.
+    // first V tile may be copied while it is still there (only the first: more
+    // V copies ahead of the query tile would delay it, and the first scores
+    // wait for it).
     static constexpr int kQOff = kNV * kTileBytes - kQBytes;
-    static constexpr int kVFree = kQOff / kTileBytes;
+    static_assert(KV || kQOff >= kTileBytes, "a V slot free of the query tile (bf16)");
     static_assert(kQOff % 1024 == 0, "the query tile's box lands on 1024-byte swizzle atoms");
     // the final-output epilogue stages kM rows of bf16 O (+16 B padding), the
     // partials epilogue 3 x kM floats, over the operand/raw buffers (idle by then)
@@ -661,7 +663,8 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
         // ------------------------------------------------------------ V producer (bf16)
         if constexpr (!KV) {
             // the query tile sits in V slots until the softmax warps have moved
-            // it into TMEM: all of them, or (early_kv) the last ones, from kVFree
+            // it into TMEM: the producer waits for that before its first tile,
+            // or (early_kv) before its second
             if (early_kv && !first_early) pdl_wait_primary();
             auto after_first_v = [&]() {
                 if (first_early) pdl_wait_primary();
@@ -669,7 +672,7 @@ split_attn_tc_kernel(const SplitParams p, const __grid_constant__ CUtensorMap tm
             const int issued = produce<D, NV, true, TRACE>(p, r, kvh, key_lo, key_hi, T, sV, aux->v_full,
                                                            aux->v_empty, aux->list_v, aux, &tmv, abort, lane,
                                                            pre0, pre1, Tc, ri.row0, &tmvs,
-                                                           early_kv ? L::kVFree : 0, after_first_v);
+                                                           early_kv ? 1 : 0, after_first_v);
             if (*abort && lane == 0) drain_copies<NV>(aux->v_full, issued);
         }
         __syncwarp();
