@@ -93,6 +93,22 @@ constexpr int kMaxNK = 8, kMaxNV = 16;
 // the stream (the LSE merge: 10 KB) can become resident beside it.
 // NVFP4 KV: codes and scales arrive by TMA into a ring of kNR raw slots and are
 // decoded into fp16 K and V operand tiles (two slots each).
+// NVFP4 raw slot: the codes and scales of a tile's 16-key units, K then V.
+// Every TMA tile copy lands on a 128-byte boundary (the tensor copy's
+// shared-memory alignment), so a unit's scales (d bytes: 64 at d = 64) take at
+// least 128.
+template <int D>
+struct RawLayout {
+    static constexpr int kCodePage = 16 * D / 2;           // codes of one 16-key unit
+    static constexpr int kScaleBox = 16 * D / 16;          // scales of one unit (bytes copied)
+    static constexpr int kScalePage = kScaleBox < 128 ? 128 : kScaleBox;   // their spacing
+    static constexpr int kKS = kPPT * kCodePage;           // offsets inside a raw slot
+    static constexpr int kVC = kKS + kPPT * kScalePage;
+    static constexpr int kVS = kVC + kPPT * kCodePage;
+    static constexpr int kTile = 2 * kPPT * (kCodePage + kScalePage);
+    static_assert(kCodePage % 128 == 0 && kScalePage % 128 == 0, "TMA destinations on 128 B");
+};
+
 template <int D, int KV>
 struct TcLayout {
     static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms along head_dim
@@ -101,18 +117,7 @@ struct TcLayout {
     static constexpr int kPBytes = 0;                      // P lives in TMEM
     static constexpr int kTileBytes = kBN * D * 2;         // one K or V tile (16-bit elements)
     static constexpr int kPageBytes = 16 * D * 2;          // one 16-key unit of V (16-bit elements)
-    // NVFP4 raw slot: the codes and scales of a tile's 16-key units, K then V.
-    // Every TMA tile copy lands on a 128-byte boundary (the tensor copy's
-    // shared-memory alignment), so a unit's scales (d bytes: 64 at d = 64)
-    // take at least 128.
-    static constexpr int kRawCodePage = 16 * D / 2;        // NVFP4 codes of one 16-key unit
-    static constexpr int kRawScaleBox = 16 * D / 16;       // NVFP4 scales of one unit (bytes copied)
-    static constexpr int kRawScalePage = kRawScaleBox < 128 ? 128 : kRawScaleBox;   // their spacing
-    static constexpr int kRawKS = kPPT * kRawCodePage;     // offsets inside a raw slot
-    static constexpr int kRawVC = kRawKS + kPPT * kRawScalePage;
-    static constexpr int kRawVS = kRawVC + kPPT * kRawCodePage;
-    static constexpr int kRawTile = 2 * kPPT * (kRawCodePage + kRawScalePage);
-    static_assert(kRawCodePage % 128 == 0 && kRawScalePage % 128 == 0, "TMA destinations on 128 B");
+    static constexpr int kRawTile = RawLayout<D>::kTile;   // one NVFP4 raw slot
     static constexpr int kAuxBytes = 1664;
     static constexpr int kMaxDyn = KV ? 232448 : 204800;    // 227 KB opt-in limit; bf16: 200 KB
     static constexpr int kFixed = 1024 + kQSmem + kPBytes + kAuxBytes;
@@ -285,6 +290,7 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
                                            const CUtensorMap* tvc, const CUtensorMap* tks, const CUtensorMap* tvs,
                                            volatile int* abort, int lane, int pre0, int pre1) {
     using L = TcLayout<D, 1>;
+    using RL = RawLayout<D>;
     constexpr int NR = L::kNR;
     const int32_t* bt = p.block_table + (size_t)r * p.bt_stride;
     const int u_lo = key_lo / 16;
@@ -325,23 +331,23 @@ __device__ __forceinline__ int produce_raw(const SplitParams& p, int r, int kvh,
             fill_list(list_base);
         }
         const int np = min(kPPT, (key_hi - (key_lo + t * kBN) + 15) / 16);
-        unsigned char* dst = raw + slot * L::kRawTile;
+        unsigned char* dst = raw + slot * RL::kTile;
         // the slot's page ids (index trace) are published by the arrival below
         if (lane < np) aux->raw_pages[slot][lane] = list[rel - list_base + lane];
         __syncwarp();
         if (lane == 0)
             mbar_arrive_expect_tx(&aux->raw_full[slot],
-                                  static_cast<uint32_t>(np * 2 * (L::kRawCodePage + L::kRawScaleBox)));
+                                  static_cast<uint32_t>(np * 2 * (RL::kCodePage + RL::kScaleBox)));
         __syncwarp();
         if (lane < 4 * np) {
             const int pp = lane >> 2, kind = lane & 3;
             const int pg = list[rel - list_base + pp];
             const int page = pg >> p.page_shift, sub = pg & sub_mask;
             uint64_t* bar = &aux->raw_full[slot];
-            if (kind == 0) tma_load_4d(dst + pp * L::kRawCodePage, tkc, 0, sub * 16, kvh, page, bar);
-            else if (kind == 1) tma_load_4d(dst + L::kRawVC + pp * L::kRawCodePage, tvc, 0, sub * 16, kvh, page, bar);
-            else if (kind == 2) tma_load_3d(dst + L::kRawKS + pp * L::kRawScalePage, tks, sub * D, kvh, page, bar);
-            else tma_load_3d(dst + L::kRawVS + pp * L::kRawScalePage, tvs, sub * D, kvh, page, bar);
+            if (kind == 0) tma_load_4d(dst + pp * RL::kCodePage, tkc, 0, sub * 16, kvh, page, bar);
+            else if (kind == 1) tma_load_4d(dst + RL::kVC + pp * RL::kCodePage, tvc, 0, sub * 16, kvh, page, bar);
+            else if (kind == 2) tma_load_3d(dst + RL::kKS + pp * RL::kScalePage, tks, sub * D, kvh, page, bar);
+            else tma_load_3d(dst + RL::kVS + pp * RL::kScalePage, tvs, sub * D, kvh, page, bar);
         }
         __syncwarp();
         issued = t + 1;
@@ -360,6 +366,7 @@ template <int D, bool IS_V, bool TRACE>
 __device__ __forceinline__ void dequant(const SplitParams& p, int key_lo, int key_hi, int T, const unsigned char* raw,
                                         unsigned char* tile_ring, TcAux* aux, volatile int* abort, int dt) {
     using L = TcLayout<D, 1>;
+    using RL = RawLayout<D>;
     constexpr int NR = L::kNR;
     constexpr int NS = IS_V ? L::kNV : L::kNK;   // operand tile slots
     constexpr int CPK = D / 64;                  // 64-element chunks per key
@@ -374,9 +381,9 @@ __device__ __forceinline__ void dequant(const SplitParams& p, int key_lo, int ke
         if (!warp_wait(&aux->raw_full[slot], (t / NR) & 1, abort)) break;
         if (t >= NS && !warp_wait(&empty[ts], ((t / NS) - 1) & 1, abort)) break;
         const int nvalid = key_hi - (key_lo + t * kBN);
-        const unsigned char* src = raw + slot * L::kRawTile;
-        const unsigned char* codes = src + (IS_V ? L::kRawVC : 0);
-        const unsigned char* scales = src + (IS_V ? L::kRawVS : L::kRawKS);
+        const unsigned char* src = raw + slot * RL::kTile;
+        const unsigned char* codes = src + (IS_V ? RL::kVC : 0);
+        const unsigned char* scales = src + (IS_V ? RL::kVS : RL::kKS);
         unsigned char* tile = tile_ring + ts * L::kTileBytes;
         for (int u = dt; u < kUnits; u += 128) {
             // u -> (group of 8 keys, chunk c, key within the group)
@@ -385,10 +392,10 @@ __device__ __forceinline__ void dequant(const SplitParams& p, int key_lo, int ke
             const int pg = j >> 4, sl = j & 15;
             uint4 outp[8];
             if (j < nvalid) {
-                const unsigned char* kr = codes + pg * L::kRawCodePage + sl * (D / 2);
+                const unsigned char* kr = codes + pg * RL::kCodePage + sl * (D / 2);
                 const uint4 w0 = *reinterpret_cast<const uint4*>(kr + raw_code_chunk<D>(sl, 2 * c) * 16);
                 const uint4 w1 = *reinterpret_cast<const uint4*>(kr + raw_code_chunk<D>(sl, 2 * c + 1) * 16);
-                const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + pg * L::kRawScalePage +
+                const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(scales + pg * RL::kScalePage +
                                                                         sl * (D / 16) + c * 4);
                 const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
