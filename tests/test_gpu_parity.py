@@ -437,6 +437,9 @@ EVERY_ROW = [
     ("verify_sweep_w16", lambda: W.verify_sweep(16)),
     ("batched_draft", lambda: W.batched_draft()),
     ("nvfp4", lambda: W.nvfp4()),
+    # 64 query heads over 4 KV heads (G 16): 256 rows per KV head, two row groups
+    ("verify_w16_ctx16k_hq64_g16", lambda: W.make_workload("verify_ctx16384_w16_hq64", [16384], 16, 64, 4, 256,
+                                                          W.MASK_CAUSAL_IN_BLOCK, pool_pages=2048)),
     # NVFP4 with block-scale bytes over the whole finite e4m3 range (0, the
     # subnormals, up to 448); the V decode scale keeps |v| <= 6 x 448 / 800 =
     # 3.36, as in the standard NVFP4 workload (6 x 1.875 x 0.3 = 3.375): the bf16
